@@ -1,0 +1,375 @@
+"""Benchmark: materialized GB/s (destination bytes) and fraction of the HBM
+roofline for st_materialize on one GB300, next to the CPU oracle.
+
+One step = one pass of the whole path over one checkpoint: every selected
+tensor gathered from the device-resident data section and cast into its
+destination (one kernel launch for the default single-chunk plan).  The
+default workload is the UNet-shaped checkpoint: 716 F16 tensors (2.668 GB),
+rename view 'model.diffusion_model.' -> 'unet.', materialized to BF16.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload unet|tiny|scaled_fp8|llm8b|stress]
+
+Prints one JSON line (rank 0).  Under torchrun each rank materializes its own
+replica (no data-path collective; weak scaling), timings are max-reduced.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "materialize_kernel_unet.md")
+KERNEL_SRC = os.path.join(ROOT, "safetensors_materialization_gb300", "csrc", "st_kernels.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="unet")
+    ap.add_argument("--e2e-chunk-mb", type=int, default=128)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback 6.8 TB/s"
+
+
+def kernel_sha():
+    import hashlib
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on this workload with the current kernel source; else None."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            for line in f:
+                if line.startswith("<!-- bench:"):
+                    d = json.loads(line[len("<!-- bench:"):].rsplit("-->", 1)[0])
+                    if d.get("kernel_sha256") == kernel_sha() and d.get("workload") == workload:
+                        return int(d["traffic_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def build_workload(name):
+    from safetensors_materialization_gb300 import synth
+    w = synth.WORKLOADS[name]()
+    return w
+
+
+def view_of(w):
+    if w.rename:
+        return lambda ix: ix.view_rename(w.rename)
+    if w.prefix:
+        return lambda ix: ix.view_prefix(w.prefix)
+    return lambda ix: ix
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_sample(w, seconds, reps=1):
+    """Times the oracle on a bounded sample of the workload: whole outputs in
+    plan order until about `seconds` of single-core work.  Returns
+    (dst GB/s, description)."""
+    from oracle import oracle as O
+    from safetensors_materialization_gb300 import synth
+    lay = w.files[0]
+    # only the sampled tensors' bytes are generated
+    img = synth.build_workload_file(w, 0)
+    ix = view_of(w)(O.parse(img))
+    sel = ix.select(dst=w.dst[0], scale_suffix=w.scale_suffix)
+    data = img[lay.data_start:]
+    outs = sel.outputs()
+    # calibrate on the first output, then pick a prefix of outputs
+    t0 = time.perf_counter()
+    sel.materialize(0, data)
+    rate = outs[0]["bytes"] / max(1e-9, time.perf_counter() - t0)
+    budget = rate * seconds
+    k, acc = 0, 0
+    while k < len(outs) and acc < budget:
+        acc += outs[k]["bytes"]
+        k += 1
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        for i in range(k):
+            sel.materialize(i, data)
+        times.append(time.perf_counter() - t0)
+    dt = min(times)
+    desc = f"first {k} of {len(outs)} outputs ({acc / 1e6:.1f} MB dst) of {w.name}, single thread"
+    return acc / dt / 1e9, desc, acc, dt
+
+
+def run_reference(args, rank, world):
+    """The reference arm is the oracle (no reference implementation exists):
+    each step materializes a bounded sample of the workload on one host core."""
+    if rank != 0:
+        return
+    w = build_workload(args.workload)
+    per_step = max(0.5, min(8.0, 60.0 / max(1, args.steps + args.warmup)))
+    from oracle import oracle as O
+    from safetensors_materialization_gb300 import synth
+    lay = w.files[0]
+    img = synth.build_workload_file(w, 0)
+    sel = view_of(w)(O.parse(img)).select(dst=w.dst[0], scale_suffix=w.scale_suffix)
+    data = img[lay.data_start:]
+    outs = sel.outputs()
+    t0 = time.perf_counter()
+    sel.materialize(0, data)
+    rate = outs[0]["bytes"] / max(1e-9, time.perf_counter() - t0)
+    k, acc = 0, 0
+    while k < len(outs) and acc < rate * per_step:
+        acc += outs[k]["bytes"]
+        k += 1
+    for _ in range(args.warmup):
+        for i in range(k):
+            sel.materialize(i, data)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for i in range(k):
+            sel.materialize(i, data)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = acc / dt / 1e9
+    sample = f"first {k} of {len(outs)} outputs ({acc / 1e6:.1f} MB dst) of {w.name} per step"
+    line = {
+        "impl": "reference", "metric": "materialized GB/s (dst bytes)", "value": round(value, 4),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- ours
+
+def run_ours(args, rank, world, local):
+    import torch
+    from safetensors_materialization_gb300 import stmat, synth
+    stmat.lib()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    w = build_workload(args.workload)
+    lay = w.files[0]
+    # file image in pinned host memory (the e2e source); data section on the device
+    host = torch.empty(lay.file_bytes, dtype=torch.uint8, pin_memory=True)
+    synth.build_workload_file(w, 0, out=host.numpy())
+    ix = view_of(w)(stmat.Index.from_file(host.numpy()))
+    plan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix)
+    dev = torch.empty(lay.file_bytes + 256, dtype=torch.uint8, device="cuda")
+    if w.whole_file_on_device:
+        dev[:lay.file_bytes].copy_(host)
+        data_ptr = dev.data_ptr() + lay.data_start
+    else:
+        dev[:lay.data_bytes].copy_(host[lay.data_start:])
+        data_ptr = dev.data_ptr()
+    outs = stmat.Outputs(plan)
+    infos = plan.outputs()
+    dst_bytes = sum(o["bytes"] for o in infos)
+    src_bytes = sum(o["numel"] * {"F16": 2, "BF16": 2, "F32": 4, "F8_E4M3": 1, "F8_E5M2": 1, "I64": 8,
+                                  "BOOL": 1}.get(o["src_dtype"], 1) for o in infos)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(3, args.warmup)):
+        plan.materialize(data_ptr, outs.ptrs, stream=stream)
+    torch.cuda.synchronize()
+    if plan.check() != 0:
+        raise RuntimeError("materialize flagged a bad destination")
+
+    # ---- device-timed region: K launches, per-launch events on the launching stream
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for k in range(args.steps):
+        plan.materialize(data_ptr, outs.ptrs, stream=stream)
+        evs[k + 1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    per = [evs[k].elapsed_time(evs[k + 1]) for k in range(args.steps)]
+    total_ms = evs[0].elapsed_time(evs[-1])
+    ms = total_ms / args.steps
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    launches_per_step = 1
+    gb_dst = dst_bytes / 1e9
+    value = gb_dst * world / (ms / 1e3)
+    peak, peak_src = measured_peak()
+    kernel_ms = statistics.mean(per)
+    achieved = (src_bytes + dst_bytes) / 1e9 / (kernel_ms / 1e3)
+
+    # ---- end to end through the C ABI: pinned host -> device copies overlapped
+    # with per-chunk kernels (st_load), then a device->host read of the status word
+    e2e = None
+    if not args.no_e2e:
+        eplan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, chunk_bytes=args.e2e_chunk_mb << 20)
+        copy = torch.cuda.Stream()
+        hdata = host[lay.data_start:]
+        ddata = dev[:lay.data_bytes]
+        for _ in range(2):
+            eplan.load(hdata, ddata, outs.ptrs, copy_stream=copy, compute_stream=stream)
+            eplan.check(stream)
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        esteps = max(3, min(args.steps, 10))
+        for _ in range(esteps):
+            eplan.load(hdata, ddata, outs.ptrs, copy_stream=copy, compute_stream=stream)
+            if eplan.check(stream) != 0:
+                raise RuntimeError("st_load flagged a bad destination")
+        es = (time.perf_counter() - t0) / esteps
+        if dist:
+            t = torch.tensor([es], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            es = float(t.item())
+        e2e = {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "h2d_bytes_per_step": lay.data_bytes,
+               "d2h_bytes_per_step": 4, "ms_per_step": round(es * 1e3, 3),
+               "chunk_bytes": args.e2e_chunk_mb << 20, "chunks": eplan.stats()["chunks"]}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, nbytes, dt = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+               "seconds": round(dt, 2)}
+
+    if rank == 0:
+        st = plan.stats()
+        line = {
+            "metric": "materialized GB/s (dst bytes)", "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "src_bytes": src_bytes, "dst_bytes": dst_bytes,
+                       "tensors": len(infos), "src_dtypes": sorted({o["src_dtype"] for o in infos}),
+                       "dst_dtype": w.dst[0], "l2": "inputs exceed L2 (no flush): "
+                       f"{(src_bytes + dst_bytes) / 1e9:.2f} GB per step vs 0.129 GB L2",
+                       "workers": st["workers"], "pieces": st["pieces"], "launches_per_step": launches_per_step,
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
+                         "peak_source": peak_src, "kernel": "materialize_kernel",
+                         "kernel_ms_mean": round(kernel_ms, 4), "kernel_ms_min": round(min(per), 4),
+                         "algorithmic_bytes_per_launch": src_bytes + dst_bytes},
+            "gpu_launches": args.steps * launches_per_step,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

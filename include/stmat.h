@@ -1,0 +1,272 @@
+/*
+ * stmat.h -- C ABI of libstmat: materialize tensors from a safetensors
+ * checkpoint on one GB300 GPU (sm_103a).
+ *
+ * What the library computes follows "Disk tier safetensors streaming design
+ * audit (ComfyUI)":
+ *   - "FastSageTensors (fastsafetensors) capability audit": the header is parsed
+ *     into per-tensor dtype, shape and data_offsets without allocating tensors
+ *     (st_index_build and the index queries);
+ *   - "Strategy summary (implemented)", "Streaming safetensors mapping": a
+ *     metadata-only index with lazy Prefix/Filter/Rename views (st_view_*);
+ *   - "Range reads and tiering", Disk->RAM->GPU: read the byte range into
+ *     (pinned) host memory and copy it to the GPU (st_stage_h2d, st_load);
+ *   - "ComfyUI load path + eager materialization sites" (scaled-FP8
+ *     conversion in comfy/sd.py) and "VRAM/RAM offload logic"
+ *     (comfy_cast_weights): each selected tensor is gathered from its byte
+ *     range and cast, fp8 weights dequantized by their per-tensor scale
+ *     (st_plan, st_materialize).
+ * The byte layout is not printed on the pages; the library reads the public
+ * safetensors layout: bytes [0,8) hold N, an unsigned 64-bit little-endian
+ * header length; bytes [8, 8+N) hold a UTF-8 JSON object mapping each tensor
+ * name to {"dtype", "shape", "data_offsets": [begin, end]} plus an optional
+ * "__metadata__" object of strings; the data section starts at byte 8+N and
+ * [begin, end) are offsets into it.
+ *
+ * Element conversion (bit-exact, deterministic):
+ *   - float sources (F32, F16, BF16, F8_E4M3, F8_E5M2) are decoded exactly,
+ *     fp8 values are multiplied by their per-tensor binary32 scale in one IEEE
+ *     binary32 multiply, and the result is rounded to the output dtype with
+ *     round-to-nearest-even, gradual underflow and overflow to infinity;
+ *   - any NaN result becomes the output's positive quiet NaN (BF16 0x7FC0,
+ *     F16 0x7E00, F32 0x7FC00000);
+ *   - integer and BOOL tensors, and tensors whose output dtype equals their
+ *     own dtype (without a scale), are copied byte for byte.
+ *
+ * Conventions: every call returns an st_status; ST_OK is 0.  On failure the
+ * thread-local message from st_last_error() says what failed, with the numbers
+ * involved.  No call throws, aborts or traps, and nothing falls back to the
+ * CPU: a CUDA failure is ST_E_CUDA.  Handles are not thread-safe; distinct
+ * handles may be used from different threads.
+ */
+#ifndef STMAT_H_
+#define STMAT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum st_status {
+  ST_OK = 0,
+  ST_E_INVAL = 1,            /* bad argument (NULL pointer, bad option, bad handle use) */
+  ST_E_TRUNCATED = 2,        /* fewer than 8 bytes, or 8 + N beyond the bytes given */
+  ST_E_HEADER_JSON = 3,      /* header is not the JSON the format requires */
+  ST_E_HEADER_TOO_LARGE = 4, /* N > 100,000,000 */
+  ST_E_DUP_KEY = 5,          /* a tensor name (or output name) appears twice */
+  ST_E_DTYPE = 6,            /* unknown dtype string */
+  ST_E_SHAPE = 7,            /* dimension not a non-negative integer, or size overflow */
+  ST_E_OFFSETS = 8,          /* offsets invalid, out of range, wrong size, overlap, hole */
+  ST_E_NOT_FOUND = 9,        /* a named tensor does not exist */
+  ST_E_UNSUPPORTED_CAST = 10,/* the requested output dtype cannot be produced */
+  ST_E_ALIGN = 11,           /* a pointer is not aligned as required */
+  ST_E_NOMEM = 12,           /* host allocation failed */
+  ST_E_CUDA = 13,            /* a CUDA runtime call failed (message has the CUDA error) */
+  ST_E_DEVICE = 14           /* the kernel reported a bad destination (st_plan_check) */
+} st_status;
+
+/* Dtypes in the header's spelling; ST_KEEP is only an output request. */
+typedef enum st_dtype {
+  ST_BOOL = 0, ST_U8 = 1, ST_I8 = 2, ST_I16 = 3, ST_U16 = 4, ST_I32 = 5, ST_U32 = 6,
+  ST_I64 = 7, ST_U64 = 8, ST_F16 = 9, ST_BF16 = 10, ST_F32 = 11, ST_F64 = 12,
+  ST_F8_E4M3 = 13, ST_F8_E5M2 = 14, ST_KEEP = 15
+} st_dtype;
+
+typedef struct st_index st_index_t; /* a parsed header, or a view of one */
+typedef struct st_plan_s st_plan_t; /* a selection turned into device work */
+
+/* ---------------------------------------------------------------- header */
+
+/* Reads N from the first 8 bytes of a file.  len < 8 -> ST_E_TRUNCATED;
+ * N > 100,000,000 -> ST_E_HEADER_TOO_LARGE. */
+st_status st_header_size(const uint8_t *first8, size_t len, uint64_t *header_len);
+
+/* Builds the metadata-only index from the first 8 + N bytes of a file
+ * (`header_bytes`, `len` bytes; the caller keeps ownership, the index copies
+ * what it needs) and the size of the data section (`data_bytes` = file size -
+ * 8 - N).  Validates: JSON syntax and schema, unique names, known dtypes,
+ * shapes, end - begin == numel * itemsize, end <= data_bytes, and that the
+ * ranges, sorted by offset, tile [0, data_bytes) with no hole or overlap.
+ * Errors: ST_E_TRUNCATED (len < 8 + N), ST_E_HEADER_TOO_LARGE, then the
+ * first defect: JSON syntax first, then per member in document order
+ * (duplicate name, schema, dtype, shape, offsets), then the tiling.
+ * Index order: ascending (begin, end, name bytewise). */
+st_status st_index_build(const uint8_t *header_bytes, size_t len, uint64_t data_bytes,
+                         st_index_t **out);
+
+/* Same, from a whole in-memory file image of `file_len` bytes. */
+st_status st_index_build_file(const uint8_t *file, uint64_t file_len, st_index_t **out);
+
+/* Releases an index or view.  Views and plans stay valid after their parent
+ * is freed (they share the parsed header by reference count). */
+void st_index_free(st_index_t *index);
+
+typedef struct st_tensor_info {
+  const char *name;      /* the name under this index/view; UTF-8, NUL-terminated */
+  st_dtype dtype;
+  int32_t ndim;
+  const int64_t *shape;  /* ndim entries */
+  uint64_t numel;        /* product of shape; 1 for [] */
+  uint64_t begin, end;   /* [begin, end) in the data section */
+} st_tensor_info;
+/* Pointers in st_tensor_info stay valid while `index` lives. */
+
+st_status st_index_count(const st_index_t *index, size_t *count);
+st_status st_index_get(const st_index_t *index, size_t i, st_tensor_info *info);
+/* Position of `name` in this index/view; ST_E_NOT_FOUND if absent. */
+st_status st_index_find(const st_index_t *index, const char *name, size_t *i);
+/* N and data_bytes of the underlying file. */
+st_status st_index_sizes(const st_index_t *index, uint64_t *header_len, uint64_t *data_bytes);
+/* Sum of numel, and per-dtype element counts (counts[15], may be NULL):
+ * metadata-only parameter count and dominant dtype ("Pipeline refactors":
+ * calculate_parameters / weight_dtype made metadata-aware). */
+st_status st_index_numel(const st_index_t *index, uint64_t *total, uint64_t *counts);
+/* "__metadata__" entries, in document order. */
+st_status st_index_metadata_count(const st_index_t *index, size_t *count);
+st_status st_index_metadata_get(const st_index_t *index, size_t i, const char **key,
+                                const char **value);
+
+/* ----------------------------------------------------------------- views */
+/* Views are new indexes over the same header, in the parent's order: they
+ * narrow or rename the metadata and never read tensor bytes.  The caller
+ * frees them with st_index_free. */
+
+/* Keeps names that start with `prefix` and strips the prefix. */
+st_status st_view_prefix(const st_index_t *parent, const char *prefix, st_index_t **out);
+/* Keeps the `n` listed names; each must exist (ST_E_NOT_FOUND). */
+st_status st_view_filter(const st_index_t *parent, const char *const *names, size_t n,
+                         st_index_t **out);
+/* Ordered prefix rules from[i] -> to[i]: the first rule whose `from` starts
+ * the name replaces that prefix; names no rule matches are kept.  Two
+ * entries mapping to one name -> ST_E_DUP_KEY (state_dict_prefix_replace). */
+st_status st_view_rename(const st_index_t *parent, const char *const *from, const char *const *to,
+                         size_t n, st_index_t **out);
+
+/* ------------------------------------------------------------------ plan */
+
+typedef struct st_selection {
+  /* Names to materialize, in output order; NULL selects every tensor of the
+   * index in index order. */
+  const char *const *names;
+  size_t n_names;
+  /* Optional, n_names entries: scale tensor name per selected name (NULL
+   * entry: unscaled).  Requires `names`. */
+  const char *const *scale_names;
+  /* Optional pairing by name when scale_names is NULL: an fp8 tensor
+   * "<stem><scale_suffix_from>" uses "<stem><scale_suffix_to>" if present. */
+  const char *scale_suffix_from;
+  const char *scale_suffix_to;
+  /* Keep part `part` of `n_parts` (0/0 or 0/1: everything): outputs are
+   * split into contiguous runs balanced by output bytes; output i (b_i bytes,
+   * c_i bytes before it, T in total) belongs to part
+   * floor(n_parts * (2 c_i + b_i) / (2 T)). */
+  uint32_t part, n_parts;
+} st_selection;
+/* A scale must be a one-element F32 tensor and may scale only an fp8 tensor
+ * (ST_E_INVAL otherwise); scale tensors are consumed, not output.  Output
+ * dtype: integers and BOOL keep theirs, ST_KEEP keeps every dtype (no
+ * scales allowed), float sources take dst_dtype (ST_BF16, ST_F16, ST_F32);
+ * F64 -> 16/32-bit floats is ST_E_UNSUPPORTED_CAST. */
+
+typedef struct st_plan_options {
+  uint32_t workers;     /* warps to balance over; 0 = every resident warp of the current device */
+  uint64_t chunk_bytes; /* 0 = one launch over the whole data section; otherwise the data
+                           section is split in chunks of this size for st_load's pipeline */
+  int32_t host_only;    /* nonzero: build the plan without touching the GPU (requires workers) */
+} st_plan_options;
+
+/* Builds the plan: outputs, then pieces (output element ranges) balanced by
+ * bytes across `workers` warps per chunk.  Unless host_only, allocates the
+ * plan's device tables on the current device (cudaMalloc) and uploads them
+ * synchronously; call it outside stream capture.  opts may be NULL. */
+st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst_dtype,
+                  const st_plan_options *opts, st_plan_t **out);
+void st_plan_free(st_plan_t *plan);
+
+typedef struct st_output_info {
+  const char *name;       /* output name */
+  st_dtype dtype;         /* output dtype */
+  st_dtype src_dtype;
+  int32_t ndim;
+  const int64_t *shape;
+  uint64_t numel;
+  uint64_t bytes;         /* numel * itemsize(dtype) */
+  uint64_t src_begin;     /* data-section offset of the source bytes */
+  const char *scale_name; /* scale tensor, or NULL */
+} st_output_info;
+
+st_status st_plan_count(const st_plan_t *plan, size_t *count);
+st_status st_plan_output(const st_plan_t *plan, size_t i, st_output_info *info);
+/* Offsets of every output in one buffer, each aligned to `align` (a power of
+ * two >= 16); offsets has st_plan_count entries.  `total` is the size. */
+st_status st_plan_arena(const st_plan_t *plan, uint64_t align, uint64_t *offsets, uint64_t *total);
+/* Piece/worker layout (for tests and tuning). */
+st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chunks, uint64_t *pieces);
+/* Piece k as {src, dst, scale, count, output, class} (host copy). */
+st_status st_plan_piece(const st_plan_t *plan, uint64_t k, uint64_t *src, uint64_t *dst,
+                        uint64_t *scale, uint32_t *count, uint32_t *output, uint32_t *cls);
+/* Pieces of worker w in chunk c: [first, last). */
+st_status st_plan_worker(const st_plan_t *plan, uint32_t chunk, uint32_t w, uint64_t *first,
+                         uint64_t *last);
+
+/* ------------------------------------------------------------ device path */
+
+/* Materializes every output of the plan on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream), asynchronously, with no host synchronization.
+ *   data_dev  device pointer to the data section (any alignment; the plan's
+ *             data_bytes bytes must be readable).  Only bytes inside it are read.
+ *   dst_ptrs  DEVICE array of st_plan_count pointers: output i is written to
+ *             dst_ptrs[i], which must be aligned to the output's itemsize and
+ *             hold st_output_info.bytes bytes.  A NULL or misaligned pointer
+ *             of a non-empty output is skipped and recorded for st_plan_check.
+ *   scales    NULL, or a DEVICE array of st_plan_count binary32 values that
+ *             replace the file's scale for fp8 outputs (entries of other
+ *             outputs are ignored).  With NULL, fp8 outputs use their paired
+ *             scale tensor's value from the data section, or 1.0.
+ * Errors: ST_E_INVAL (NULL plan/data/dst_ptrs, host-only plan), ST_E_CUDA
+ * (launch failure).  Outputs may not overlap each other or the data section. */
+st_status st_materialize(const void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
+                         const float *scales, void *stream);
+
+/* Copies `bytes` from host memory to device memory on `stream` in chunks of
+ * `chunk_bytes` (0 = one copy) with cudaMemcpyAsync, then records
+ * `done_event` (a cudaEvent_t; may be NULL) on `stream`.  src_host should be
+ * pinned (page-locked) for the copies to be asynchronous.  ST_E_INVAL on NULL
+ * pointers with bytes > 0. */
+st_status st_stage_h2d(void *dst_dev, const void *src_host, uint64_t bytes, uint64_t chunk_bytes,
+                       void *stream, void *done_event);
+
+/* Stages the data section from host memory (pinned, data_bytes long) into
+ * data_dev on `copy_stream` chunk by chunk (the plan's chunk_bytes) and
+ * materializes each chunk's pieces on `compute_stream` as soon as that
+ * chunk's copy completes, so copies and kernels overlap.  The first copy
+ * waits for work already queued on compute_stream.  Arguments as for
+ * st_materialize.  Returns without synchronizing. */
+st_status st_load(const void *data_host, void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
+                  const float *scales, void *copy_stream, void *compute_stream);
+
+/* Waits for `stream`, then reads and clears the plan's device error flags:
+ * bit 0 = a non-empty output had a NULL or misaligned destination.
+ * Returns ST_E_DEVICE when any flag was set. */
+st_status st_plan_check(const st_plan_t *plan, void *stream, uint32_t *flags);
+
+/* ----------------------------------------------------------------- misc */
+
+/* Message of the calling thread's last failure ("" if none). */
+const char *st_last_error(void);
+/* "ST_OK", "ST_E_INVAL", ... */
+const char *st_status_name(st_status status);
+/* Itemsize in bytes of a dtype (0 for ST_KEEP / unknown). */
+size_t st_dtype_size(st_dtype dtype);
+/* Header spelling of a dtype ("F32", ...; "KEEP"), or NULL. */
+const char *st_dtype_name(st_dtype dtype);
+/* Library version, e.g. 0x000100 for 0.1.0. */
+uint32_t st_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STMAT_H_ */

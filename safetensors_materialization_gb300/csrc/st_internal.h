@@ -1,0 +1,96 @@
+// st_internal.h -- structures shared by the host library (index, planner,
+// C ABI) and the sm_103a kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include "stmat.h"
+
+#if defined(__CUDACC__)
+#define ST_HD __host__ __device__
+#else
+#define ST_HD
+#endif
+
+namespace stmat {
+
+// Conversion classes.  A piece of class CLS_COPY counts bytes; every other
+// class counts elements of its source dtype.
+enum Cls : uint32_t {
+  CLS_COPY = 0,
+  CLS_F32_BF16,
+  CLS_F32_F16,
+  CLS_F16_BF16,
+  CLS_F16_F32,
+  CLS_BF16_F16,
+  CLS_BF16_F32,
+  CLS_E4M3_BF16,
+  CLS_E4M3_F16,
+  CLS_E4M3_F32,
+  CLS_E5M2_BF16,
+  CLS_E5M2_F16,
+  CLS_E5M2_F32,
+  CLS_COUNT
+};
+
+// One contiguous element range of one output: the unit a warp processes.
+struct alignas(16) Piece {
+  uint64_t src;      // data-section byte offset of the range's first element
+  uint64_t dst;      // byte offset of that element inside its output buffer
+  uint64_t scale;    // data-section byte offset of the binary32 scale, or kNoScale
+  uint32_t count;    // elements (bytes for CLS_COPY)
+  uint32_t out_cls;  // output index << kClsBits | class
+};
+static_assert(sizeof(Piece) == 32, "piece layout");
+
+constexpr uint64_t kNoScale = ~0ull;
+constexpr uint32_t kClsBits = 5;
+constexpr uint32_t kMaxOutputs = 1u << (32 - kClsBits);
+constexpr int kWarpsPerBlock = 8;
+
+// Bit set in the device error word when an output's destination is NULL or
+// not aligned to its itemsize.
+constexpr uint32_t kErrBadDst = 1u;
+
+struct LaunchArgs {
+  const uint8_t *data;     // data section on the device
+  uint64_t data_bytes;
+  const Piece *pieces;     // all pieces of the plan
+  const uint32_t *parts;   // workers + 1 piece indices: worker w owns [parts[w], parts[w+1])
+  uint32_t workers;
+  void *const *dst;        // device array: output index -> destination
+  const float *scales;     // device array of per-output scales, or nullptr
+  uint32_t *err;           // device error word
+};
+
+// Output itemsize of a class (bytes written per counted unit).
+ST_HD inline int cls_out_size(uint32_t c) {
+  switch (c) {
+    case CLS_COPY: return 1;
+    case CLS_F32_BF16: case CLS_F32_F16: case CLS_F16_BF16: case CLS_BF16_F16:
+    case CLS_E4M3_BF16: case CLS_E4M3_F16: case CLS_E5M2_BF16: case CLS_E5M2_F16: return 2;
+    default: return 4;
+  }
+}
+
+// Source itemsize of a class (bytes read per counted unit).
+ST_HD inline int cls_in_size(uint32_t c) {
+  switch (c) {
+    case CLS_COPY: return 1;
+    case CLS_F32_BF16: case CLS_F32_F16: return 4;
+    case CLS_F16_BF16: case CLS_F16_F32: case CLS_BF16_F16: case CLS_BF16_F32: return 2;
+    default: return 1;
+  }
+}
+
+// Kernels (st_kernels.cu).
+// Resident 256-thread blocks per SM for the materialize kernel, and SM count
+// of the current device.
+st_status kernel_occupancy(int *sms, int *blocks_per_sm);
+// Launches the materialize kernel over `a.workers` warps.
+st_status launch_materialize(const LaunchArgs &a, void *stream);
+
+// Error reporting shared by the host files.
+st_status set_error(st_status s, const char *fmt, ...);
+
+}  // namespace stmat

@@ -1,0 +1,568 @@
+// st_plan.cpp -- selection, output dtypes, scale pairing, byte-balanced work
+// partition, device tables, and the stream-ordered entry points
+// (st_materialize, st_stage_h2d, st_load).
+//
+// "Disk tier safetensors streaming design audit (ComfyUI)":
+//  - "ComfyUI load path + eager materialization sites": the scaled-FP8
+//    conversion (comfy/sd.py) pairs fp8 weights with per-tensor scales;
+//    BaseModel.load_model_weights selects tensors by name/prefix;
+//  - "VRAM/RAM offload logic": weights are cast at load (comfy_cast_weights);
+//  - "Range reads and tiering", Disk->RAM->GPU: only the tensors' byte ranges
+//    are staged from (pinned) host memory and copied to the GPU.
+//
+// Work layout: every output is cut into pieces (element ranges); pieces are
+// balanced by bytes (source + destination, plus a fixed per-piece cost) over
+// W warps, so that huge tensors and 100k tiny tensors spread evenly over the
+// GPU.  With chunking, the data section is split into chunks and each chunk
+// has its own balanced partition, so a chunk can be materialized as soon as
+// its bytes are on the device.
+#include <cuda_runtime_api.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <memory>
+#include <new>
+#include <string>
+#include <string_view>
+#include <vector>
+
+#include "st_index.h"
+#include "st_internal.h"
+
+namespace stmat {
+namespace {
+
+constexpr uint64_t kSplitUnits = 64;        // pieces of one output start at multiples of this
+constexpr uint64_t kPieceCost = 1024;       // fixed cost of a piece, in bytes of traffic
+constexpr uint64_t kMinWorkerCost = 4096;   // no more warps than total cost / this
+constexpr uint64_t kMaxPieceUnits = 1ull << 30;
+
+bool is_fp8(int d) { return d == ST_F8_E4M3 || d == ST_F8_E5M2; }
+bool is_float(int d) {
+  return d == ST_F16 || d == ST_BF16 || d == ST_F32 || d == ST_F64 || d == ST_F8_E4M3 || d == ST_F8_E5M2;
+}
+
+// Output dtype for a source dtype and a request, or -1.
+int out_dtype_of(int src, int req) {
+  if (req == ST_KEEP || !is_float(src)) return src;
+  if (src == ST_F64) return -1;
+  return req;
+}
+
+// Conversion class for (source, output); scaled outputs are never copies.
+int class_of(int src, int out, bool scaled) {
+  if (src == out && !scaled) return CLS_COPY;
+  switch (src) {
+    case ST_F32: return out == ST_BF16 ? CLS_F32_BF16 : out == ST_F16 ? CLS_F32_F16 : -1;
+    case ST_F16: return out == ST_BF16 ? CLS_F16_BF16 : out == ST_F32 ? CLS_F16_F32 : -1;
+    case ST_BF16: return out == ST_F16 ? CLS_BF16_F16 : out == ST_F32 ? CLS_BF16_F32 : -1;
+    case ST_F8_E4M3:
+      return out == ST_BF16 ? CLS_E4M3_BF16 : out == ST_F16 ? CLS_E4M3_F16 : out == ST_F32 ? CLS_E4M3_F32 : -1;
+    case ST_F8_E5M2:
+      return out == ST_BF16 ? CLS_E5M2_BF16 : out == ST_F16 ? CLS_E5M2_F16 : out == ST_F32 ? CLS_E5M2_F32 : -1;
+    default: return -1;
+  }
+}
+
+std::string cuda_msg(cudaError_t e) {
+  return std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
+}
+
+}  // namespace
+
+struct Output {
+  std::string name;
+  uint32_t pos;        // position in the index/view
+  uint32_t entry;      // core tensor
+  int out_dtype;
+  int64_t scale = -1;  // core tensor of the scale
+  uint32_t cls;
+  uint64_t units;      // counted units (elements, or bytes for copies)
+};
+
+}  // namespace stmat
+
+using namespace stmat;
+
+struct st_plan_s {
+  std::shared_ptr<const IndexData> index;
+  std::vector<Output> outs;
+  uint32_t workers = 1;
+  uint64_t chunk_bytes = 0;
+  uint32_t n_chunks = 1;
+  std::vector<Piece> pieces;
+  std::vector<uint32_t> parts;  // n_chunks * (workers + 1)
+  // device side
+  bool on_device = false;
+  int device = -1;
+  Piece *d_pieces = nullptr;
+  uint32_t *d_parts = nullptr;
+  uint32_t *d_err = nullptr;
+  std::vector<cudaEvent_t> events;  // one per chunk + one for st_load's start
+  ~st_plan_s() {
+    if (!on_device) return;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != device) cudaSetDevice(device);
+    for (cudaEvent_t e : events) cudaEventDestroy(e);
+    cudaFree(d_pieces);
+    cudaFree(d_parts);
+    cudaFree(d_err);
+    if (cur != device && cur >= 0) cudaSetDevice(cur);
+  }
+};
+
+namespace {
+
+// Selection -> outputs (order, dtype, scale), with the part filter.
+st_status select_outputs(const IndexData &ix, const st_selection *sel, int req, std::vector<Output> *outs) {
+  const Core &core = *ix.core;
+  const bool all = !sel || !sel->names;
+  const size_t n = all ? ix.ent.size() : sel->n_names;
+  uint32_t n_parts = sel ? sel->n_parts : 0, part = sel ? sel->part : 0;
+  if (n_parts == 0) n_parts = 1;
+  if (part >= n_parts) return set_error(ST_E_INVAL, "part %u of %u", part, n_parts);
+  if (req != ST_BF16 && req != ST_F16 && req != ST_F32 && req != ST_KEEP)
+    return set_error(ST_E_UNSUPPORTED_CAST, "output dtype must be BF16, F16, F32 or KEEP");
+  if (sel && sel->scale_names && all) return set_error(ST_E_INVAL, "scale_names needs names");
+  std::vector<uint32_t> pos(n);
+  std::vector<char> taken(ix.ent.size(), 0);
+  for (size_t i = 0; i < n; ++i) {
+    if (all) {
+      pos[i] = static_cast<uint32_t>(i);
+    } else {
+      const char *nm = sel->names[i];
+      if (!nm) return set_error(ST_E_INVAL, "NULL name at %zu", i);
+      auto it = ix.pos.find(std::string_view(nm));
+      if (it == ix.pos.end()) return set_error(ST_E_NOT_FOUND, "no tensor named \"%s\"", nm);
+      pos[i] = it->second;
+    }
+    if (taken[pos[i]]) return set_error(ST_E_DUP_KEY, "\"%s\" selected twice", ix.names[pos[i]]);
+    taken[pos[i]] = 1;
+  }
+  // Scale pairing.
+  std::vector<int64_t> scale(n, -1);  // position of the scale in the view
+  std::vector<char> consumed(ix.ent.size(), 0);
+  const char *from = sel ? sel->scale_suffix_from : nullptr;
+  const char *to = sel ? sel->scale_suffix_to : nullptr;
+  const size_t flen = from ? strlen(from) : 0;
+  std::string cand;
+  for (size_t i = 0; i < n; ++i) {
+    const Tensor &t = core.tensors[ix.ent[pos[i]]];
+    if (sel && sel->scale_names) {
+      const char *sn = sel->scale_names[i];
+      if (sn) {
+        auto it = ix.pos.find(std::string_view(sn));
+        if (it == ix.pos.end()) return set_error(ST_E_NOT_FOUND, "no scale tensor named \"%s\"", sn);
+        scale[i] = it->second;
+      }
+    } else if (from && to && is_fp8(t.dtype)) {
+      std::string_view nm(ix.names[pos[i]]);
+      if (nm.size() >= flen && nm.substr(nm.size() - flen) == from) {
+        cand.assign(nm.data(), nm.size() - flen);
+        cand += to;
+        auto it = ix.pos.find(std::string_view(cand));
+        if (it != ix.pos.end()) scale[i] = it->second;
+      }
+    }
+    if (scale[i] >= 0) {
+      const Tensor &s = core.tensors[ix.ent[scale[i]]];
+      if (!is_fp8(t.dtype) || s.dtype != ST_F32 || s.numel != 1)
+        return set_error(ST_E_INVAL, "\"%s\" cannot scale \"%s\": scales are one-element F32 tensors of fp8 weights",
+                         ix.names[scale[i]], ix.names[pos[i]]);
+      if (req == ST_KEEP) return set_error(ST_E_UNSUPPORTED_CAST, "KEEP cannot apply a scale");
+      consumed[scale[i]] = 1;
+    }
+  }
+  for (size_t i = 0; i < n; ++i) {
+    if (consumed[pos[i]]) continue;
+    const Tensor &t = core.tensors[ix.ent[pos[i]]];
+    int od = out_dtype_of(t.dtype, req);
+    if (od < 0)
+      return set_error(ST_E_UNSUPPORTED_CAST, "\"%s\": %s cannot be materialized as %s", ix.names[pos[i]],
+                       st_dtype_name(static_cast<st_dtype>(t.dtype)), st_dtype_name(static_cast<st_dtype>(req)));
+    Output o;
+    o.name = ix.names[pos[i]];
+    o.pos = pos[i];
+    o.entry = ix.ent[pos[i]];
+    o.out_dtype = od;
+    o.scale = scale[i] >= 0 ? static_cast<int64_t>(ix.ent[scale[i]]) : -1;
+    int c = class_of(t.dtype, od, o.scale >= 0);
+    if (c < 0) return set_error(ST_E_UNSUPPORTED_CAST, "no conversion for \"%s\"", o.name.c_str());
+    o.cls = static_cast<uint32_t>(c);
+    o.units = c == CLS_COPY ? t.numel * dtype_size(t.dtype) : t.numel;
+    outs->push_back(std::move(o));
+  }
+  if (n_parts > 1) {
+    // Output i goes to part floor(n_parts * (2 c_i + b_i) / (2 T)).
+    unsigned __int128 T = 0, c = 0;
+    for (const Output &o : *outs)
+      T += static_cast<unsigned __int128>(core.tensors[o.entry].numel) * dtype_size(o.out_dtype);
+    std::vector<Output> kept;
+    for (Output &o : *outs) {
+      unsigned __int128 b = static_cast<unsigned __int128>(core.tensors[o.entry].numel) * dtype_size(o.out_dtype);
+      uint64_t owner = 0;
+      if (T > 0) {
+        unsigned __int128 q = ((2 * c + b) * n_parts) / (2 * T);
+        owner = q >= n_parts ? n_parts - 1 : static_cast<uint64_t>(q);
+      }
+      c += b;
+      if (owner == part) kept.push_back(std::move(o));
+    }
+    outs->swap(kept);
+  }
+  if (outs->size() >= kMaxOutputs) return set_error(ST_E_INVAL, "at most %u outputs", kMaxOutputs - 1);
+  return ST_OK;
+}
+
+struct Segment {
+  uint32_t out;
+  uint64_t u0, u1;
+};
+
+// Builds pieces and per-chunk worker partitions.
+void build_pieces(st_plan_s *p) {
+  const Core &core = *p->index->core;
+  const uint64_t C = p->chunk_bytes;
+  const uint64_t data = core.data_bytes;
+  p->n_chunks = C ? static_cast<uint32_t>(std::max<uint64_t>(1, (data + C - 1) / C)) : 1;
+  std::vector<std::vector<Segment>> per_chunk(p->n_chunks);
+  // Outputs in source order.
+  std::vector<uint32_t> order(p->outs.size());
+  for (uint32_t i = 0; i < order.size(); ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](uint32_t a, uint32_t b) {
+    return core.tensors[p->outs[a].entry].begin < core.tensors[p->outs[b].entry].begin;
+  });
+  for (uint32_t oi : order) {
+    const Output &o = p->outs[oi];
+    if (o.units == 0) continue;
+    const Tensor &t = core.tensors[o.entry];
+    const uint64_t si = cls_in_size(o.cls);
+    if (!C) {
+      per_chunk[0].push_back({oi, 0, o.units});
+      continue;
+    }
+    uint64_t scale_chunk = o.scale >= 0 ? (core.tensors[o.scale].end - 1) / C : 0;
+    uint64_t u = 0;
+    for (uint64_t k = t.begin / C; u < o.units; ++k) {
+      // units whose last byte lies before the end of chunk k
+      uint64_t end = (k + 1) * C;
+      uint64_t ue = end <= t.begin ? 0 : std::min<uint64_t>(o.units, (end - t.begin) / si);
+      if (ue > u) {
+        per_chunk[std::max<uint64_t>(k, scale_chunk)].push_back({oi, u, ue});
+        u = ue;
+      }
+    }
+  }
+  const uint32_t W = p->workers;
+  p->pieces.clear();
+  p->parts.assign(static_cast<size_t>(p->n_chunks) * (W + 1), 0);
+  for (uint32_t k = 0; k < p->n_chunks; ++k) {
+    auto &segs = per_chunk[k];
+    std::stable_sort(segs.begin(), segs.end(), [&](const Segment &a, const Segment &b) {
+      const Output &oa = p->outs[a.out], &ob = p->outs[b.out];
+      return core.tensors[oa.entry].begin + a.u0 * cls_in_size(oa.cls) <
+             core.tensors[ob.entry].begin + b.u0 * cls_in_size(ob.cls);
+    });
+    double total = 0;
+    for (const Segment &s : segs) {
+      const Output &o = p->outs[s.out];
+      total += kPieceCost + double(s.u1 - s.u0) * (cls_in_size(o.cls) + cls_out_size(o.cls));
+    }
+    // A boundary that falls inside a segment splits it and adds one piece.
+    const double share = (total + double(W - 1) * kPieceCost) / W;
+    uint32_t *parts = &p->parts[static_cast<size_t>(k) * (W + 1)];
+    uint32_t w = 0;
+    double used = 0;  // cost assigned so far (workers < w and worker w's part)
+    parts[0] = static_cast<uint32_t>(p->pieces.size());
+    auto emit = [&](const Segment &s, uint64_t a, uint64_t b) {
+      const Output &o = p->outs[s.out];
+      const Tensor &t = core.tensors[o.entry];
+      const uint64_t si = cls_in_size(o.cls), so = cls_out_size(o.cls);
+      for (uint64_t x = a; x < b; x += kMaxPieceUnits) {
+        uint64_t y = std::min(b, x + kMaxPieceUnits);
+        Piece pc;
+        pc.src = t.begin + x * si;
+        pc.dst = x * so;
+        pc.scale = o.scale >= 0 ? core.tensors[o.scale].begin : kNoScale;
+        pc.count = static_cast<uint32_t>(y - x);
+        pc.out_cls = (s.out << kClsBits) | o.cls;
+        p->pieces.push_back(pc);
+      }
+    };
+    auto next_worker = [&]() {
+      ++w;
+      parts[w] = static_cast<uint32_t>(p->pieces.size());
+    };
+    for (const Segment &s : segs) {
+      const Output &o = p->outs[s.out];
+      const double per = cls_in_size(o.cls) + cls_out_size(o.cls);
+      uint64_t u = s.u0;
+      while (u < s.u1) {
+        double rest = kPieceCost + double(s.u1 - u) * per;
+        double room = (w + 1) * share - used;
+        if (w + 1 == W || rest <= room + 0.5 * kPieceCost) {
+          emit(s, u, s.u1);
+          used += rest;
+          u = s.u1;
+          if (w + 1 < W && used >= (w + 1) * share) next_worker();
+          break;
+        }
+        // Fill the rest of worker w with a prefix that ends on a split boundary.
+        double take = std::floor((room - kPieceCost) / per);
+        uint64_t cut = take > 0 ? u + static_cast<uint64_t>(take) : u;
+        cut -= cut % kSplitUnits;
+        if (cut > u) {
+          emit(s, u, cut);
+          used += kPieceCost + double(cut - u) * per;
+          u = cut;
+        }
+        // Boundaries are absolute, so the slack this cut left rolls over to
+        // the next worker instead of piling up on the last one.
+        next_worker();
+      }
+    }
+    while (w < W) next_worker();
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst_dtype,
+                  const st_plan_options *opts, st_plan_t **out) {
+  if (!index || !out) return set_error(ST_E_INVAL, "NULL argument");
+  *out = nullptr;
+  try {
+    auto p = std::make_unique<st_plan_s>();
+    p->index = index_ref(index);
+    st_status s = select_outputs(*p->index, sel, dst_dtype, &p->outs);
+    if (s != ST_OK) return s;
+    const bool host_only = opts && opts->host_only;
+    uint32_t workers = opts ? opts->workers : 0;
+    p->chunk_bytes = opts ? opts->chunk_bytes : 0;
+    int sms = 0, blocks = 0;
+    if (!host_only || workers == 0) {
+      if (host_only) return set_error(ST_E_INVAL, "a host-only plan needs options.workers");
+      s = kernel_occupancy(&sms, &blocks);
+      if (s != ST_OK) return s;
+      if (workers == 0) workers = static_cast<uint32_t>(sms) * static_cast<uint32_t>(blocks) * kWarpsPerBlock;
+    }
+    // No more warps than the work can use.
+    uint64_t cost = 0;
+    for (const Output &o : p->outs) cost += kPieceCost + o.units * (cls_in_size(o.cls) + cls_out_size(o.cls));
+    uint64_t cap = std::max<uint64_t>(1, cost / kMinWorkerCost);
+    p->workers = static_cast<uint32_t>(std::min<uint64_t>(workers, cap));
+    build_pieces(p.get());
+    if (!host_only) {
+      cudaError_t e = cudaGetDevice(&p->device);
+      size_t pb = p->pieces.size() * sizeof(Piece), qb = p->parts.size() * sizeof(uint32_t);
+      if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&p->d_pieces), std::max<size_t>(pb, sizeof(Piece)));
+      if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&p->d_parts), qb);
+      if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&p->d_err), sizeof(uint32_t));
+      p->on_device = true;  // from here the destructor releases what was made
+      if (e == cudaSuccess && pb) e = cudaMemcpy(p->d_pieces, p->pieces.data(), pb, cudaMemcpyHostToDevice);
+      if (e == cudaSuccess) e = cudaMemcpy(p->d_parts, p->parts.data(), qb, cudaMemcpyHostToDevice);
+      if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(uint32_t));
+      for (uint32_t k = 0; e == cudaSuccess && k <= p->n_chunks; ++k) {
+        cudaEvent_t ev;
+        e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e == cudaSuccess) p->events.push_back(ev);
+      }
+      if (e != cudaSuccess)
+        return set_error(ST_E_CUDA, "uploading the plan (%zu pieces): %s", p->pieces.size(), cuda_msg(e).c_str());
+    }
+    *out = p.release();
+    return ST_OK;
+  } catch (const std::bad_alloc &) {
+    return set_error(ST_E_NOMEM, "out of host memory while planning");
+  }
+}
+
+void st_plan_free(st_plan_t *plan) { delete plan; }
+
+st_status st_plan_count(const st_plan_t *p, size_t *count) {
+  if (!p || !count) return set_error(ST_E_INVAL, "NULL argument");
+  *count = p->outs.size();
+  return ST_OK;
+}
+
+st_status st_plan_output(const st_plan_t *p, size_t i, st_output_info *info) {
+  if (!p || !info) return set_error(ST_E_INVAL, "NULL argument");
+  if (i >= p->outs.size()) return set_error(ST_E_INVAL, "output %zu out of range", i);
+  const Output &o = p->outs[i];
+  const Tensor &t = p->index->core->tensors[o.entry];
+  info->name = o.name.c_str();
+  info->dtype = static_cast<st_dtype>(o.out_dtype);
+  info->src_dtype = static_cast<st_dtype>(t.dtype);
+  info->ndim = static_cast<int32_t>(t.shape.size());
+  info->shape = t.shape.data();
+  info->numel = t.numel;
+  info->bytes = t.numel * dtype_size(o.out_dtype);
+  info->src_begin = t.begin;
+  info->scale_name = o.scale >= 0 ? p->index->core->tensors[o.scale].name.c_str() : nullptr;
+  return ST_OK;
+}
+
+st_status st_plan_arena(const st_plan_t *p, uint64_t align, uint64_t *offsets, uint64_t *total) {
+  if (!p || (!offsets && !p->outs.empty()) || !total) return set_error(ST_E_INVAL, "NULL argument");
+  if (align < 16 || (align & (align - 1))) return set_error(ST_E_INVAL, "alignment %llu is not a power of two >= 16",
+                                                            (unsigned long long)align);
+  uint64_t at = 0;
+  for (size_t i = 0; i < p->outs.size(); ++i) {
+    at = (at + align - 1) & ~(align - 1);
+    offsets[i] = at;
+    at += p->index->core->tensors[p->outs[i].entry].numel * dtype_size(p->outs[i].out_dtype);
+  }
+  *total = at;
+  return ST_OK;
+}
+
+st_status st_plan_stats(const st_plan_t *p, uint32_t *workers, uint32_t *chunks, uint64_t *pieces) {
+  if (!p) return set_error(ST_E_INVAL, "NULL plan");
+  if (workers) *workers = p->workers;
+  if (chunks) *chunks = p->n_chunks;
+  if (pieces) *pieces = p->pieces.size();
+  return ST_OK;
+}
+
+st_status st_plan_piece(const st_plan_t *p, uint64_t k, uint64_t *src, uint64_t *dst, uint64_t *scale,
+                        uint32_t *count, uint32_t *output, uint32_t *cls) {
+  if (!p || !src || !dst || !scale || !count || !output || !cls) return set_error(ST_E_INVAL, "NULL argument");
+  if (k >= p->pieces.size()) return set_error(ST_E_INVAL, "piece %llu out of range", (unsigned long long)k);
+  const Piece &pc = p->pieces[k];
+  *src = pc.src;
+  *dst = pc.dst;
+  *scale = pc.scale;
+  *count = pc.count;
+  *output = pc.out_cls >> kClsBits;
+  *cls = pc.out_cls & ((1u << kClsBits) - 1);
+  return ST_OK;
+}
+
+st_status st_plan_worker(const st_plan_t *p, uint32_t chunk, uint32_t w, uint64_t *first, uint64_t *last) {
+  if (!p || !first || !last) return set_error(ST_E_INVAL, "NULL argument");
+  if (chunk >= p->n_chunks || w >= p->workers) return set_error(ST_E_INVAL, "chunk/worker out of range");
+  const uint32_t *parts = &p->parts[static_cast<size_t>(chunk) * (p->workers + 1)];
+  *first = parts[w];
+  *last = parts[w + 1];
+  return ST_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+st_status check_device_plan(const st_plan_t *p) {
+  if (!p->on_device) return set_error(ST_E_INVAL, "the plan was built host-only");
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "cudaGetDevice: %s", cuda_msg(e).c_str());
+  if (cur != p->device) return set_error(ST_E_INVAL, "the plan belongs to device %d, device %d is current", p->device, cur);
+  return ST_OK;
+}
+
+st_status launch_chunk(const st_plan_t *p, uint32_t k, const void *data_dev, void *const *dst, const float *scales,
+                       void *stream) {
+  if (p->pieces.empty()) return ST_OK;
+  const uint32_t *parts = &p->parts[static_cast<size_t>(k) * (p->workers + 1)];
+  if (parts[0] == parts[p->workers]) return ST_OK;  // nothing in this chunk
+  LaunchArgs a;
+  a.data = static_cast<const uint8_t *>(data_dev);
+  a.data_bytes = p->index->core->data_bytes;
+  a.pieces = p->d_pieces;
+  a.parts = p->d_parts + static_cast<size_t>(k) * (p->workers + 1);
+  a.workers = p->workers;
+  a.dst = dst;
+  a.scales = scales;
+  a.err = p->d_err;
+  return launch_materialize(a, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+st_status st_materialize(const void *data_dev, const st_plan_t *p, void *const *dst_ptrs, const float *scales,
+                         void *stream) {
+  if (!p) return set_error(ST_E_INVAL, "NULL plan");
+  st_status s = check_device_plan(p);
+  if (s != ST_OK) return s;
+  if (p->pieces.empty()) return ST_OK;
+  if (!data_dev || !dst_ptrs) return set_error(ST_E_INVAL, "NULL data or destination array");
+  for (uint32_t k = 0; k < p->n_chunks; ++k) {
+    s = launch_chunk(p, k, data_dev, dst_ptrs, scales, stream);
+    if (s != ST_OK) return s;
+  }
+  return ST_OK;
+}
+
+st_status st_stage_h2d(void *dst_dev, const void *src_host, uint64_t bytes, uint64_t chunk_bytes, void *stream,
+                       void *done_event) {
+  if (bytes && (!dst_dev || !src_host)) return set_error(ST_E_INVAL, "NULL pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint64_t step = chunk_bytes ? chunk_bytes : bytes;
+  for (uint64_t off = 0; off < bytes; off += step) {
+    uint64_t n = std::min(step, bytes - off);
+    cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t *>(dst_dev) + off, static_cast<const uint8_t *>(src_host) + off,
+                                    n, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess)
+      return set_error(ST_E_CUDA, "copy of %llu bytes at %llu: %s", (unsigned long long)n, (unsigned long long)off,
+                       cuda_msg(e).c_str());
+  }
+  if (done_event) {
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(done_event), st);
+    if (e != cudaSuccess) return set_error(ST_E_CUDA, "cudaEventRecord: %s", cuda_msg(e).c_str());
+  }
+  return ST_OK;
+}
+
+st_status st_load(const void *data_host, void *data_dev, const st_plan_t *p, void *const *dst_ptrs,
+                  const float *scales, void *copy_stream, void *compute_stream) {
+  if (!p) return set_error(ST_E_INVAL, "NULL plan");
+  st_status s = check_device_plan(p);
+  if (s != ST_OK) return s;
+  const uint64_t data = p->index->core->data_bytes;
+  if ((data && (!data_host || !data_dev)) || !dst_ptrs) return set_error(ST_E_INVAL, "NULL pointer");
+  cudaStream_t cs = static_cast<cudaStream_t>(copy_stream), ks = static_cast<cudaStream_t>(compute_stream);
+  // The copies overwrite data_dev: order them after work already on the compute stream.
+  cudaEvent_t start = p->events[p->n_chunks];
+  cudaError_t e = cudaEventRecord(start, ks);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, start, 0);
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "ordering the copy stream: %s", cuda_msg(e).c_str());
+  const uint64_t C = p->chunk_bytes ? p->chunk_bytes : (data ? data : 1);
+  for (uint32_t k = 0; k < p->n_chunks; ++k) {
+    uint64_t off = static_cast<uint64_t>(k) * C;
+    uint64_t n = off < data ? std::min(C, data - off) : 0;
+    if (n) {
+      e = cudaMemcpyAsync(static_cast<uint8_t *>(data_dev) + off, static_cast<const uint8_t *>(data_host) + off, n,
+                          cudaMemcpyHostToDevice, cs);
+      if (e != cudaSuccess)
+        return set_error(ST_E_CUDA, "copy of chunk %u (%llu bytes): %s", k, (unsigned long long)n, cuda_msg(e).c_str());
+    }
+    e = cudaEventRecord(p->events[k], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ks, p->events[k], 0);
+    if (e != cudaSuccess) return set_error(ST_E_CUDA, "chunk %u event: %s", k, cuda_msg(e).c_str());
+    s = launch_chunk(p, k, data_dev, dst_ptrs, scales, compute_stream);
+    if (s != ST_OK) return s;
+  }
+  return ST_OK;
+}
+
+st_status st_plan_check(const st_plan_t *p, void *stream, uint32_t *flags) {
+  if (!p || !flags) return set_error(ST_E_INVAL, "NULL argument");
+  st_status s = check_device_plan(p);
+  if (s != ST_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  uint32_t v = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&v, p->d_err, sizeof v, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && v) e = cudaMemset(p->d_err, 0, sizeof v);
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "reading the error word: %s", cuda_msg(e).c_str());
+  *flags = v;
+  if (v) return set_error(ST_E_DEVICE, "device flags 0x%x: a non-empty output had a NULL or misaligned destination", v);
+  return ST_OK;
+}
+
+}  // extern "C"

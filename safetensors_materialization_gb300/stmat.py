@@ -1,0 +1,385 @@
+"""Thin Python binding of libstmat (ctypes): the C ABI's names, with
+arguments marshalled from Python objects and torch tensors.
+
+Every step of the path (header parse, views, planning, staging copies and
+the materialize kernel) runs inside libstmat; PyTorch only provides device
+memory and streams.  There is no fallback: if libstmat.so is missing or a
+call fails, a StmatError is raised.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libstmat.so")
+
+DTYPES = ["BOOL", "U8", "I8", "I16", "U16", "I32", "U32", "I64", "U64", "F16", "BF16", "F32", "F64",
+          "F8_E4M3", "F8_E5M2", "KEEP"]
+STATUS = ["ST_OK", "ST_E_INVAL", "ST_E_TRUNCATED", "ST_E_HEADER_JSON", "ST_E_HEADER_TOO_LARGE",
+          "ST_E_DUP_KEY", "ST_E_DTYPE", "ST_E_SHAPE", "ST_E_OFFSETS", "ST_E_NOT_FOUND",
+          "ST_E_UNSUPPORTED_CAST", "ST_E_ALIGN", "ST_E_NOMEM", "ST_E_CUDA", "ST_E_DEVICE"]
+
+# Every symbol the C ABI exports (include/stmat.h).
+EXPORTS = [
+    "st_header_size", "st_index_build", "st_index_build_file", "st_index_free", "st_index_count",
+    "st_index_get", "st_index_find", "st_index_sizes", "st_index_numel", "st_index_metadata_count",
+    "st_index_metadata_get", "st_view_prefix", "st_view_filter", "st_view_rename", "st_plan",
+    "st_plan_free", "st_plan_count", "st_plan_output", "st_plan_arena", "st_plan_stats",
+    "st_plan_piece", "st_plan_worker", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
+    "st_last_error", "st_status_name", "st_dtype_size", "st_dtype_name", "st_version",
+]
+
+
+class StmatError(RuntimeError):
+    def __init__(self, code, msg=""):
+        self.code = code
+        self.status = STATUS[code] if 0 <= code < len(STATUS) else str(code)
+        super().__init__(f"{self.status}: {msg}")
+
+
+class TensorInfo(C.Structure):
+    _fields_ = [("name", C.c_char_p), ("dtype", C.c_int), ("ndim", C.c_int32),
+                ("shape", C.POINTER(C.c_int64)), ("numel", C.c_uint64), ("begin", C.c_uint64),
+                ("end", C.c_uint64)]
+
+
+class OutputInfo(C.Structure):
+    _fields_ = [("name", C.c_char_p), ("dtype", C.c_int), ("src_dtype", C.c_int), ("ndim", C.c_int32),
+                ("shape", C.POINTER(C.c_int64)), ("numel", C.c_uint64), ("bytes", C.c_uint64),
+                ("src_begin", C.c_uint64), ("scale_name", C.c_char_p)]
+
+
+class Selection(C.Structure):
+    _fields_ = [("names", C.POINTER(C.c_char_p)), ("n_names", C.c_size_t),
+                ("scale_names", C.POINTER(C.c_char_p)), ("scale_suffix_from", C.c_char_p),
+                ("scale_suffix_to", C.c_char_p), ("part", C.c_uint32), ("n_parts", C.c_uint32)]
+
+
+class PlanOptions(C.Structure):
+    _fields_ = [("workers", C.c_uint32), ("chunk_bytes", C.c_uint64), ("host_only", C.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libstmat (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise StmatError(1, f"{LIB_PATH} is missing; build it with "
+                                "safetensors_materialization_gb300.build.build()")
+        L = C.CDLL(LIB_PATH)
+        P, U64, U32, S, I = C.c_void_p, C.c_uint64, C.c_uint32, C.c_size_t, C.c_int
+        PP = C.POINTER(P)
+        sig = {
+            "st_header_size": [P, S, C.POINTER(U64)],
+            "st_index_build": [P, S, U64, PP],
+            "st_index_build_file": [P, U64, PP],
+            "st_index_count": [P, C.POINTER(S)],
+            "st_index_get": [P, S, C.POINTER(TensorInfo)],
+            "st_index_find": [P, C.c_char_p, C.POINTER(S)],
+            "st_index_sizes": [P, C.POINTER(U64), C.POINTER(U64)],
+            "st_index_numel": [P, C.POINTER(U64), C.POINTER(U64)],
+            "st_index_metadata_count": [P, C.POINTER(S)],
+            "st_index_metadata_get": [P, S, C.POINTER(C.c_char_p), C.POINTER(C.c_char_p)],
+            "st_view_prefix": [P, C.c_char_p, PP],
+            "st_view_filter": [P, C.POINTER(C.c_char_p), S, PP],
+            "st_view_rename": [P, C.POINTER(C.c_char_p), C.POINTER(C.c_char_p), S, PP],
+            "st_plan": [P, C.POINTER(Selection), I, C.POINTER(PlanOptions), PP],
+            "st_plan_count": [P, C.POINTER(S)],
+            "st_plan_output": [P, S, C.POINTER(OutputInfo)],
+            "st_plan_arena": [P, U64, C.POINTER(U64), C.POINTER(U64)],
+            "st_plan_stats": [P, C.POINTER(U32), C.POINTER(U32), C.POINTER(U64)],
+            "st_plan_piece": [P, U64, C.POINTER(U64), C.POINTER(U64), C.POINTER(U64), C.POINTER(U32),
+                              C.POINTER(U32), C.POINTER(U32)],
+            "st_plan_worker": [P, U32, U32, C.POINTER(U64), C.POINTER(U64)],
+            "st_materialize": [P, P, P, P, P],
+            "st_stage_h2d": [P, P, U64, U64, P, P],
+            "st_load": [P, P, P, P, P, P, P],
+            "st_plan_check": [P, P, C.POINTER(U32)],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = I
+        for name in ("st_index_free", "st_plan_free"):
+            getattr(L, name).argtypes = [P]
+            getattr(L, name).restype = None
+        L.st_last_error.restype = C.c_char_p
+        L.st_status_name.restype = C.c_char_p
+        L.st_status_name.argtypes = [I]
+        L.st_dtype_size.restype = S
+        L.st_dtype_size.argtypes = [I]
+        L.st_dtype_name.restype = C.c_char_p
+        L.st_dtype_name.argtypes = [I]
+        L.st_version.restype = U32
+        _lib = L
+    return _lib
+
+
+def _check(code):
+    if code != 0:
+        raise StmatError(code, lib().st_last_error().decode(errors="replace"))
+
+
+def _strs(names):
+    arr = (C.c_char_p * max(1, len(names)))()
+    for i, n in enumerate(names):
+        arr[i] = None if n is None else n.encode()
+    return arr
+
+
+def _addr(obj):
+    """Address of a numpy array, bytes object or torch tensor."""
+    if obj is None:
+        return None
+    if isinstance(obj, int):
+        return obj
+    if hasattr(obj, "data_ptr"):
+        return obj.data_ptr()
+    if isinstance(obj, np.ndarray):
+        return obj.ctypes.data
+    raise TypeError(f"cannot take the address of {type(obj)}")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return s if isinstance(s, int) else s.cuda_stream
+
+
+def header_size(first8: bytes) -> int:
+    n = C.c_uint64()
+    _check(lib().st_header_size(first8, len(first8), C.byref(n)))
+    return n.value
+
+
+class Index:
+    """A parsed header or a view (st_index_t)."""
+
+    def __init__(self, handle, keep=None):
+        self._h = C.c_void_p(handle)
+        self._keep = keep
+
+    @classmethod
+    def from_file(cls, image):
+        """Index of a whole file image (bytes or uint8 numpy array)."""
+        arr = np.frombuffer(image, dtype=np.uint8) if isinstance(image, (bytes, bytearray)) else image
+        out = C.c_void_p()
+        _check(lib().st_index_build_file(_addr(arr), arr.size, C.byref(out)))
+        return cls(out.value)
+
+    @classmethod
+    def from_header(cls, header, data_bytes):
+        """Index from the first 8 + N bytes and the data section size."""
+        arr = np.frombuffer(header, dtype=np.uint8) if isinstance(header, (bytes, bytearray)) else header
+        out = C.c_void_p()
+        _check(lib().st_index_build(_addr(arr), arr.size, data_bytes, C.byref(out)))
+        return cls(out.value)
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value and _lib is not None:
+            _lib.st_index_free(self._h)
+            self._h = C.c_void_p(None)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __len__(self):
+        n = C.c_size_t()
+        _check(lib().st_index_count(self._h, C.byref(n)))
+        return n.value
+
+    def entry(self, i):
+        info = TensorInfo()
+        _check(lib().st_index_get(self._h, i, C.byref(info)))
+        return {"name": info.name.decode(), "dtype": DTYPES[info.dtype],
+                "shape": [info.shape[d] for d in range(info.ndim)], "numel": info.numel,
+                "begin": info.begin, "end": info.end}
+
+    def entries(self):
+        return [self.entry(i) for i in range(len(self))]
+
+    def find(self, name):
+        i = C.c_size_t()
+        _check(lib().st_index_find(self._h, name.encode(), C.byref(i)))
+        return i.value
+
+    def sizes(self):
+        h, d = C.c_uint64(), C.c_uint64()
+        _check(lib().st_index_sizes(self._h, C.byref(h), C.byref(d)))
+        return h.value, d.value
+
+    def numel(self):
+        total = C.c_uint64()
+        counts = (C.c_uint64 * 15)()
+        _check(lib().st_index_numel(self._h, C.byref(total), counts))
+        return total.value, {DTYPES[d]: counts[d] for d in range(15) if counts[d]}
+
+    def metadata(self):
+        n = C.c_size_t()
+        _check(lib().st_index_metadata_count(self._h, C.byref(n)))
+        out = {}
+        for i in range(n.value):
+            k, v = C.c_char_p(), C.c_char_p()
+            _check(lib().st_index_metadata_get(self._h, i, C.byref(k), C.byref(v)))
+            out[k.value.decode()] = v.value.decode()
+        return out
+
+    def view_prefix(self, prefix):
+        out = C.c_void_p()
+        _check(lib().st_view_prefix(self._h, prefix.encode(), C.byref(out)))
+        return Index(out.value)
+
+    def view_filter(self, names):
+        out = C.c_void_p()
+        _check(lib().st_view_filter(self._h, _strs(names), len(names), C.byref(out)))
+        return Index(out.value)
+
+    def view_rename(self, rules):
+        out = C.c_void_p()
+        _check(lib().st_view_rename(self._h, _strs([a for a, _ in rules]), _strs([b for _, b in rules]),
+                                    len(rules), C.byref(out)))
+        return Index(out.value)
+
+    def plan(self, dst="BF16", names=None, scale_names=None, scale_suffix=None, part=0, n_parts=0,
+             workers=0, chunk_bytes=0, host_only=False):
+        """st_plan: outputs and device work for a selection."""
+        sel = Selection()
+        keep = []
+        if names is not None:
+            arr = _strs(names)
+            keep.append(arr)
+            sel.names, sel.n_names = C.cast(arr, C.POINTER(C.c_char_p)), len(names)
+        if scale_names is not None:
+            arr = _strs(scale_names)
+            keep.append(arr)
+            sel.scale_names = C.cast(arr, C.POINTER(C.c_char_p))
+        if scale_suffix:
+            sel.scale_suffix_from, sel.scale_suffix_to = scale_suffix[0].encode(), scale_suffix[1].encode()
+        sel.part, sel.n_parts = part, n_parts
+        opts = PlanOptions(workers, chunk_bytes, 1 if host_only else 0)
+        out = C.c_void_p()
+        _check(lib().st_plan(self._h, C.byref(sel), DTYPES.index(dst), C.byref(opts), C.byref(out)))
+        return Plan(out.value, self)
+
+
+class Plan:
+    """st_plan_t: the outputs of a selection and their device work."""
+
+    def __init__(self, handle, index):
+        self._h = C.c_void_p(handle)
+        self.index = index
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value and _lib is not None:
+            _lib.st_plan_free(self._h)
+            self._h = C.c_void_p(None)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __len__(self):
+        n = C.c_size_t()
+        _check(lib().st_plan_count(self._h, C.byref(n)))
+        return n.value
+
+    def output(self, i):
+        o = OutputInfo()
+        _check(lib().st_plan_output(self._h, i, C.byref(o)))
+        return {"name": o.name.decode(), "dtype": DTYPES[o.dtype], "src_dtype": DTYPES[o.src_dtype],
+                "shape": [o.shape[d] for d in range(o.ndim)], "numel": o.numel, "bytes": o.bytes,
+                "begin": o.src_begin, "scale": o.scale_name.decode() if o.scale_name else None}
+
+    def outputs(self):
+        return [self.output(i) for i in range(len(self))]
+
+    def arena(self, align=256):
+        n = len(self)
+        offs = (C.c_uint64 * max(1, n))()
+        total = C.c_uint64()
+        _check(lib().st_plan_arena(self._h, align, offs, C.byref(total)))
+        return [offs[i] for i in range(n)], total.value
+
+    def stats(self):
+        w, c, p = C.c_uint32(), C.c_uint32(), C.c_uint64()
+        _check(lib().st_plan_stats(self._h, C.byref(w), C.byref(c), C.byref(p)))
+        return {"workers": w.value, "chunks": c.value, "pieces": p.value}
+
+    def piece(self, k):
+        v = [C.c_uint64(), C.c_uint64(), C.c_uint64(), C.c_uint32(), C.c_uint32(), C.c_uint32()]
+        _check(lib().st_plan_piece(self._h, k, *[C.byref(x) for x in v]))
+        return dict(zip(["src", "dst", "scale", "count", "output", "cls"], [x.value for x in v]))
+
+    def worker(self, chunk, w):
+        a, b = C.c_uint64(), C.c_uint64()
+        _check(lib().st_plan_worker(self._h, chunk, w, C.byref(a), C.byref(b)))
+        return a.value, b.value
+
+    # ------------------------------------------------------------- device
+    def materialize(self, data, dst_ptrs, scales=None, stream=None):
+        """st_materialize.  data: device uint8 tensor (or address) of the data
+        section; dst_ptrs: device int64 tensor of output addresses."""
+        _check(lib().st_materialize(_addr(data), self._h, _addr(dst_ptrs), _addr(scales), _stream(stream)))
+
+    def load(self, data_host, data_dev, dst_ptrs, scales=None, copy_stream=None, compute_stream=None):
+        """st_load: staged copy of the data section overlapped with materialize."""
+        _check(lib().st_load(_addr(data_host), _addr(data_dev), self._h, _addr(dst_ptrs), _addr(scales),
+                             _stream(copy_stream), _stream(compute_stream)))
+
+    def check(self, stream=None):
+        flags = C.c_uint32()
+        code = lib().st_plan_check(self._h, _stream(stream), C.byref(flags))
+        if code not in (0, 14):
+            _check(code)
+        return flags.value
+
+
+def stage_h2d(dst_dev, src_host, nbytes, chunk_bytes=0, stream=None, done_event=None):
+    """st_stage_h2d: chunked host->device copies on `stream`."""
+    ev = None if done_event is None else done_event.cuda_event
+    _check(lib().st_stage_h2d(_addr(dst_dev), _addr(src_host), nbytes, chunk_bytes, _stream(stream), ev))
+
+
+# ----------------------------------------------------------- torch helpers
+
+def torch_dtype(name):
+    import torch
+    return {"BOOL": torch.bool, "U8": torch.uint8, "I8": torch.int8, "I16": torch.int16,
+            "U16": torch.uint16, "I32": torch.int32, "U32": torch.uint32, "I64": torch.int64,
+            "U64": torch.uint64, "F16": torch.float16, "BF16": torch.bfloat16, "F32": torch.float32,
+            "F64": torch.float64, "F8_E4M3": torch.float8_e4m3fn, "F8_E5M2": torch.float8_e5m2}[name]
+
+
+class Outputs:
+    """Destination buffers for a plan: one device arena carved into the
+    outputs (each 256-byte aligned) and the device array of their addresses."""
+
+    def __init__(self, plan: Plan, device="cuda", align=256):
+        import torch
+        self.plan = plan
+        self.infos = plan.outputs()
+        offs, total = plan.arena(align)
+        self.offsets = offs
+        self.arena = torch.empty(max(total, 1), dtype=torch.uint8, device=device)
+        base = self.arena.data_ptr()
+        self.ptrs = torch.tensor([base + o for o in offs] or [0], dtype=torch.int64, device=device)
+
+    def raw(self, i):
+        """Output i as uint8 bytes (a view into the arena)."""
+        return self.arena[self.offsets[i]:self.offsets[i] + self.infos[i]["bytes"]]
+
+    def tensor(self, i):
+        """Output i as a typed, shaped tensor (a view into the arena)."""
+        info = self.infos[i]
+        return self.raw(i).view(torch_dtype(info["dtype"])).view(info["shape"])
+
+    def tensors(self):
+        return {info["name"]: self.tensor(i) for i, info in enumerate(self.infos)}

@@ -1,0 +1,388 @@
+"""GPU parity: libstmat's CUDA path against the oracle, byte for byte (0 ULP).
+
+Every test calls the product through the C ABI (ctypes binding) and compares
+with the oracle on the same seeded bytes.  Small cases are compared in full;
+the full-size workloads are compared on windows of every tensor (head, tail
+and seeded random windows) and, at full size, on properties that hold for
+any size (a raw copy equals its source bytes).
+"""
+import json
+import struct
+
+import numpy as np
+import pytest
+
+from conftest import golden, small_file
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def to_device(image, offset=0, whole=True, data_start=None):
+    """Copies a file image (uint8 numpy) to the GPU.  whole=True keeps the
+    header in front (so the data section keeps the file's alignment) and adds
+    `offset` bytes before the image; returns (buffer, data pointer)."""
+    if whole:
+        buf = torch.empty(image.size + offset + 16, dtype=torch.uint8, device="cuda")
+        buf[offset:offset + image.size].copy_(torch.from_numpy(image))
+        return buf, buf.data_ptr() + offset + data_start
+    data = image[data_start:]
+    buf = torch.empty(max(1, data.size), dtype=torch.uint8, device="cuda")
+    if data.size:
+        buf[:data.size].copy_(torch.from_numpy(np.ascontiguousarray(data)))
+    return buf, buf.data_ptr()
+
+
+class Packed:
+    """Outputs packed back to back, each aligned only to its itemsize."""
+
+    def __init__(self, plan, shift=0):
+        self.infos = plan.outputs()
+        offs, at = [], 0
+        for o in self.infos:
+            isz = max(1, o["bytes"] // max(1, o["numel"]))
+            at = (at + isz - 1) // isz * isz
+            if (at // isz) % 2 == 0:
+                at += isz  # keep it off 2*itemsize alignment
+            offs.append(at)
+            at += o["bytes"]
+        self.offsets = offs
+        self.arena = torch.full((at + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+        self.ptrs = torch.tensor([self.arena.data_ptr() + o for o in offs] or [0], dtype=torch.int64,
+                                 device="cuda")
+
+    def raw(self, i):
+        return self.arena[self.offsets[i]:self.offsets[i] + self.infos[i]["bytes"]]
+
+
+def run(stmat, image, dst="BF16", view=None, scale_suffix=None, whole=True, offset=0, packed=False,
+        workers=0, scales=None):
+    ix = stmat.Index.from_file(image)
+    if view:
+        ix = view(ix)
+    plan = ix.plan(dst=dst, scale_suffix=scale_suffix, workers=workers)
+    hlen, dbytes = ix.sizes()
+    buf, data_ptr = to_device(image, offset, whole, 8 + hlen)
+    outs = Packed(plan) if packed else stmat.Outputs(plan)
+    plan.materialize(data_ptr, outs.ptrs, scales=scales)
+    torch.cuda.synchronize()
+    assert plan.check() == 0
+    return plan, outs, buf
+
+
+def oracle_all(oracle, image, dst="BF16", view=None, scale_suffix=None):
+    ix = oracle.parse(image)
+    if view:
+        ix = view(ix)
+    sel = ix.select(dst=dst, scale_suffix=scale_suffix)
+    data = image[8 + ix.header_len:]
+    return sel, [sel.materialize(i, data) for i in range(len(sel))]
+
+
+def assert_same(plan, outs, sel, expected):
+    assert [o["name"] for o in plan.outputs()] == [o["name"] for o in sel.outputs()]
+    for i, want in enumerate(expected):
+        got = outs.raw(i).cpu().numpy()
+        if not np.array_equal(got, want):
+            bad = np.nonzero(got != want)[0]
+            raise AssertionError(f"output {plan.output(i)['name']}: {bad.size} bytes differ, first at {bad[0]}: "
+                                 f"got {got[bad[0]:bad[0] + 8].tobytes().hex()} want {want[bad[0]:bad[0] + 8].tobytes().hex()}")
+
+
+def image_of(ents, data, pad=0):
+    h = json.dumps(ents).encode() + b" " * pad
+    return np.frombuffer(struct.pack("<Q", len(h)) + h + data, dtype=np.uint8).copy()
+
+
+# ------------------------------------------------------------------ golden
+
+@pytest.mark.parametrize("dst", ["BF16", "F16", "F32"])
+def test_golden_small_file(stmat, oracle, dst):
+    g, f = small_file()
+    img = np.frombuffer(f, dtype=np.uint8).copy()
+    plan, outs, _ = run(stmat, img, dst=dst, scale_suffix=(".weight", ".scale_weight"))
+    for i, o in enumerate(plan.outputs()):
+        assert outs.raw(i).cpu().numpy().tobytes().hex() == g["expect"][dst][o["name"]], o["name"]
+
+
+# -------------------------------------------------- exhaustive special values
+
+def special_image(seed=0):
+    """Every f16, bf16 and fp8 bit pattern, a structured f32 sweep, and fp8
+    tensors under special scales (2^k, random, subnormal-producing, overflowing,
+    zero, negative)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    parts, ents, off = [], {}, 0
+
+    def add(name, dt, arr):
+        nonlocal off
+        b = np.ascontiguousarray(arr).view(np.uint8).reshape(-1)
+        isz = {"F32": 4, "F16": 2, "BF16": 2, "F8_E4M3": 1, "F8_E5M2": 1}[dt]
+        ents[name] = {"dtype": dt, "shape": [b.size // isz], "data_offsets": [off, off + b.size]}
+        parts.append(b.tobytes())
+        off += b.size
+
+    all16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    add("f16_all", "F16", all16)
+    add("bf16_all", "BF16", all16)
+    hi = np.arange(1 << 16, dtype=np.uint32) << 16
+    lows = np.array([0, 1, 0x0FFF, 0x1000, 0x1001, 0x7FFF, 0x8000, 0x8001, 0xFFFF], dtype=np.uint32)
+    add("f32_grid", "F32", (hi[:, None] | lows[None, :]).reshape(-1))
+    add("f32_rand", "F32", rng.integers(0, 1 << 32, size=1 << 18, dtype=np.uint64).astype(np.uint32))
+    all8 = np.arange(256, dtype=np.uint8)
+    scales = [1.0, 0.5, 2.0 ** -7, 1024.0, 0.0371, float(np.float32(rng.uniform(1e-3, 1e-1))), 3.0e-39,
+              1.7e38, 0.0, -0.25]
+    for fmt in ("F8_E4M3", "F8_E5M2"):
+        add(f"{fmt}.raw.weight", fmt, all8)
+        for j, s in enumerate(scales):
+            add(f"{fmt}.s{j}.weight", fmt, np.tile(all8, 3))
+            add(f"{fmt}.s{j}.scale_weight", "F32", np.array([s], dtype=np.float32).view(np.uint32))
+            ents[f"{fmt}.s{j}.scale_weight"]["shape"] = []
+    return image_of(ents, b"".join(parts), pad=3)
+
+
+@pytest.mark.parametrize("dst", ["BF16", "F16", "F32"])
+@pytest.mark.parametrize("packed", [False, True])
+def test_every_bit_pattern(stmat, oracle, dst, packed):
+    img = special_image()
+    sfx = (".weight", ".scale_weight")
+    plan, outs, _ = run(stmat, img, dst=dst, scale_suffix=sfx, packed=packed)
+    sel, want = oracle_all(oracle, img, dst=dst, scale_suffix=sfx)
+    assert_same(plan, outs, sel, want)
+
+
+# ------------------------------------------------------- alignment sweep
+
+def sweep_image(residue_pad, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    dts = ["F32", "F16", "BF16", "F8_E4M3", "F8_E5M2", "I64", "BOOL", "U8", "I32"]
+    isz = {"F32": 4, "F16": 2, "BF16": 2, "F8_E4M3": 1, "F8_E5M2": 1, "I64": 8, "BOOL": 1, "U8": 1, "I32": 4}
+    ents, parts, off = {}, [], 0
+    lengths = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257,
+               511, 1000, 4095, 4096, 4097, 12345, 100003]
+    i = 0
+    for n in lengths:
+        for dt in dts:
+            raw = rng.integers(0, 256, size=n * isz[dt], dtype=np.uint8)
+            if dt == "BOOL":
+                raw = raw & 1
+            ents[f"t{i:04d}"] = {"dtype": dt, "shape": [n], "data_offsets": [off, off + raw.size]}
+            parts.append(raw.tobytes())
+            off += raw.size
+            i += 1
+            # a one-byte tensor between others shifts every later start by one
+            ents[f"t{i:04d}"] = {"dtype": "U8", "shape": [1], "data_offsets": [off, off + 1]}
+            parts.append(bytes([i & 255]))
+            off += 1
+            i += 1
+    return image_of(ents, b"".join(parts), pad=residue_pad)
+
+
+@pytest.mark.parametrize("residue", list(range(16)))
+def test_alignment_sweep(stmat, oracle, residue):
+    """Every class at every source misalignment (1-byte spacers shift the
+    starts; the device copy is offset by `residue`) into 256-byte-aligned and
+    into packed (itemsize-aligned) outputs."""
+    img = sweep_image(residue % 8, seed=residue)
+    for dst in ("BF16", "F16", "F32", "KEEP"):
+        sel, want = oracle_all(oracle, img, dst=dst)
+        for packed in (False, True):
+            plan, outs, _ = run(stmat, img, dst=dst, offset=residue, packed=packed,
+                                workers=[0, 7, 333][residue % 3])
+            assert_same(plan, outs, sel, want)
+
+
+def test_data_section_edges(stmat, oracle):
+    """Misaligned tensors that start at the first byte and end at the last
+    byte of an unaligned, exactly sized device data section."""
+    rng = np.random.Generator(np.random.PCG64(5))
+    for n0, n1 in [(1, 1), (33, 70), (1000, 4097), (17, 3)]:
+        a = rng.integers(0, 1 << 32, size=n0, dtype=np.uint64).astype(np.uint32)
+        b = rng.integers(0, 1 << 16, size=n1, dtype=np.uint64).astype(np.uint16)
+        ents = {"first": {"dtype": "F32", "shape": [n0], "data_offsets": [0, 4 * n0]},
+                "last": {"dtype": "F16", "shape": [n1], "data_offsets": [4 * n0, 4 * n0 + 2 * n1]}}
+        img = image_of(ents, a.tobytes() + b.tobytes())
+        sel, want = oracle_all(oracle, img, dst="BF16")
+        ix = stmat.Index.from_file(img)
+        plan = ix.plan(dst="BF16")
+        data = img[8 + ix.sizes()[0]:]
+        for shift in (1, 5, 9, 15):
+            buf = torch.zeros(data.size + 32, dtype=torch.uint8, device="cuda")
+            buf[shift:shift + data.size].copy_(torch.from_numpy(data.copy()))
+            outs = stmat.Outputs(plan)
+            plan.materialize(buf.data_ptr() + shift, outs.ptrs)
+            torch.cuda.synchronize()
+            assert plan.check() == 0
+            assert_same(plan, outs, sel, want)
+
+
+# ------------------------------------------------------------- workloads
+
+def window_compare(oracle_sel, plan, outs, data, rng, width=4096, windows=3):
+    """Compares every output on its first and last `width` elements and on
+    seeded random windows."""
+    for i, o in enumerate(plan.outputs()):
+        n = o["numel"]
+        if n == 0:
+            continue
+        isz = o["bytes"] // n
+        starts = {0, max(0, n - width)} | {int(x) for x in rng.integers(0, max(1, n - width), size=windows)}
+        got_all = outs.raw(i)
+        for s in sorted(starts):
+            k = min(width, n - s)
+            want = oracle_sel.materialize_range(i, data, s, k)
+            got = got_all[s * isz:(s + k) * isz].cpu().numpy()
+            assert np.array_equal(got, want), (o["name"], s)
+
+
+def workload_case(stmat, oracle, name, shard=0, dst_index=0, full=False):
+    from safetensors_materialization_gb300 import synth
+    w = synth.WORKLOADS[name]()
+    lay = w.files[shard]
+    img = synth.build_workload_file(w, shard)
+    view = None
+    if w.rename:
+        view = lambda ix: ix.view_rename(w.rename)  # noqa: E731
+    if w.prefix:
+        view = lambda ix: ix.view_prefix(w.prefix)  # noqa: E731
+    dst = w.dst[dst_index]
+    plan, outs, buf = run(stmat, img, dst=dst, view=view, scale_suffix=w.scale_suffix,
+                          whole=w.whole_file_on_device)
+    oix = oracle.parse(img)
+    if view:
+        oix = view(oix)
+    sel = oix.select(dst=dst, scale_suffix=w.scale_suffix)
+    assert [o["name"] for o in plan.outputs()] == [o["name"] for o in sel.outputs()]
+    data = img[lay.data_start:]
+    if full:
+        assert_same(plan, outs, sel, [sel.materialize(i, data) for i in range(len(sel))])
+    else:
+        window_compare(sel, plan, outs, data, np.random.Generator(np.random.PCG64(11)))
+    return plan, outs, buf, lay, img
+
+
+def test_tiny_workload_full(stmat, oracle):
+    workload_case(stmat, oracle, "tiny", full=True)
+
+
+def test_stress_workload_full(stmat, oracle):
+    """100k tensors, 7 dtypes, every source 1-15 bytes off 16-byte alignment."""
+    workload_case(stmat, oracle, "stress", full=True)
+
+
+def test_unet_workload(stmat, oracle):
+    plan, outs, buf, lay, img = workload_case(stmat, oracle, "unet")
+    # full size: F16 -> BF16 of N(0, 0.02) data (no NaN) equals torch's cast on every element
+    data = buf[:lay.data_bytes]
+    for i, o in enumerate(plan.outputs()):
+        src = data[o["begin"]:o["begin"] + o["numel"] * 2].view(torch.float16)
+        assert torch.equal(outs.raw(i).view(torch.int16), src.to(torch.bfloat16).view(torch.int16)), o["name"]
+
+
+def test_scaled_fp8_workload(stmat, oracle):
+    workload_case(stmat, oracle, "scaled_fp8")
+
+
+@pytest.mark.parametrize("shard", [0, 3])
+def test_llm_copy_is_byte_identical(stmat, oracle, shard):
+    """BF16 -> BF16 is a raw copy: at full size every output equals its source bytes."""
+    plan, outs, buf, lay, img = workload_case(stmat, oracle, "llm8b", shard=shard, dst_index=0)
+    for i, o in enumerate(plan.outputs()):
+        assert torch.equal(outs.raw(i), buf[o["begin"]:o["begin"] + o["bytes"]]), o["name"]
+
+
+def test_llm_cast_to_f16(stmat, oracle):
+    workload_case(stmat, oracle, "llm8b", shard=1, dst_index=1)
+
+
+# ------------------------------------------------------ pipeline and misc
+
+@pytest.mark.parametrize("chunk", [1 << 20, 48 << 20])
+def test_load_pipeline_matches_materialize(stmat, oracle, chunk):
+    """st_load (chunked pinned H2D copies overlapped with per-chunk kernels)
+    produces the oracle's bytes."""
+    from safetensors_materialization_gb300 import synth
+    w = synth.stress()
+    lay = w.files[0]
+    img = synth.build_workload_file(w, 0)
+    ix = stmat.Index.from_file(img)
+    plan = ix.plan(dst="BF16", chunk_bytes=chunk)
+    assert plan.stats()["chunks"] == (lay.data_bytes + chunk - 1) // chunk
+    host = torch.from_numpy(img[lay.data_start:].copy()).pin_memory()
+    dev = torch.empty(lay.data_bytes, dtype=torch.uint8, device="cuda")
+    outs = stmat.Outputs(plan)
+    copy = torch.cuda.Stream()
+    plan.load(host, dev, outs.ptrs, copy_stream=copy, compute_stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert plan.check() == 0
+    sel, want = oracle_all(oracle, img, dst="BF16")
+    assert_same(plan, outs, sel, want)
+    assert torch.equal(dev.cpu(), host)
+
+
+def test_stage_h2d(stmat):
+    src = torch.randint(0, 256, (10_000_019,), dtype=torch.uint8).pin_memory()
+    dst = torch.zeros_like(src, device="cuda")
+    ev = torch.cuda.Event()
+    stmat.stage_h2d(dst, src, src.numel(), chunk_bytes=1 << 20, done_event=ev)
+    ev.synchronize()
+    assert torch.equal(dst.cpu(), src)
+
+
+def test_scale_override(stmat, oracle):
+    img = special_image()
+    sfx = (".weight", ".scale_weight")
+    ix = stmat.Index.from_file(img)
+    plan = ix.plan(dst="BF16", scale_suffix=sfx)
+    hlen = ix.sizes()[0]
+    buf, data_ptr = to_device(img, 0, True, 8 + hlen)
+    outs = stmat.Outputs(plan)
+    scales = torch.full((len(plan),), 0.125, dtype=torch.float32, device="cuda")
+    plan.materialize(data_ptr, outs.ptrs, scales=scales)
+    torch.cuda.synchronize()
+    for i, o in enumerate(plan.outputs()):
+        if o["src_dtype"] in ("F8_E4M3", "F8_E5M2"):
+            raw = img[8 + hlen + o["begin"]:8 + hlen + o["begin"] + o["numel"]]
+            want = oracle.convert(o["src_dtype"], "BF16", raw, scale=0.125)
+            assert np.array_equal(outs.raw(i).cpu().numpy(), want), o["name"]
+
+
+def test_bad_destinations_are_flagged_and_skipped(stmat, oracle):
+    g, f = small_file()
+    img = np.frombuffer(f, dtype=np.uint8).copy()
+    ix = stmat.Index.from_file(img)
+    plan = ix.plan(dst="BF16")
+    buf, data_ptr = to_device(img, 0, True, 8 + ix.sizes()[0])
+    outs = stmat.Outputs(plan)
+    outs.arena.fill_(0xA5)
+    ptrs = outs.ptrs.clone()
+    ptrs[0] = 0                      # NULL destination for "a"
+    ptrs[1] = outs.ptrs[1] + 1       # odd address for the BF16 output "b"
+    plan.materialize(data_ptr, ptrs)
+    torch.cuda.synchronize()
+    assert plan.check() == 1
+    assert plan.check() == 0         # reading clears the flags
+    assert torch.all(outs.arena[:outs.offsets[2]] == 0xA5)   # nothing written for "a" or "b"
+    sel, want = oracle_all(oracle, img, dst="BF16")
+    for i in range(2, len(want)):
+        assert np.array_equal(outs.raw(i).cpu().numpy(), want[i])
+
+
+def test_empty_cases(stmat):
+    img = image_of({}, b"")
+    ix = stmat.Index.from_file(img)
+    plan = ix.plan(dst="BF16")
+    assert len(plan) == 0 and plan.stats()["pieces"] == 0
+    scratch = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    plan.materialize(scratch, torch.zeros(1, dtype=torch.int64, device="cuda"))  # no work, no launch
+    ents = {"z": {"dtype": "F32", "shape": [0], "data_offsets": [0, 0]},
+            "s": {"dtype": "F16", "shape": [], "data_offsets": [0, 2]}}
+    img = image_of(ents, b"\x00\x3c")
+    plan, outs, _ = run(stmat, img, dst="F32")
+    assert outs.raw(1).cpu().numpy().view(np.float32)[0] == 1.0

@@ -1,0 +1,127 @@
+"""CPU model of the materialize kernel's address arithmetic (no GPU).
+
+Restates, per piece, how the kernel splits a piece into a scalar head, a
+vector body of 16-byte source chunks and a scalar tail, and checks that for
+the plans the GPU tests and the benchmark run, every byte the kernel reads
+lies in the data section, every byte it writes lies in the piece's output,
+and head + body + tail cover the piece's elements exactly once.  Data bases
+are taken at every residue mod 16 and destinations at 256-byte and at
+itemsize-only alignment.  This must be kept in step with
+csrc/st_kernels.cu (run_piece).
+"""
+import numpy as np
+import pytest
+
+# class -> (source itemsize, output itemsize) in counted units
+CLS = {0: (1, 1), 1: (4, 2), 2: (4, 2), 3: (2, 2), 4: (2, 4), 5: (2, 2), 6: (2, 4),
+       7: (1, 2), 8: (1, 2), 9: (1, 4), 10: (1, 2), 11: (1, 2), 12: (1, 4)}
+
+
+def split(src, dst, n, si, so, lo, hi):
+    """Mirror of run_piece: returns (head, nch, vector source window, vector dst range)."""
+    K = 16 // si
+    OB = K * so
+    A = min(OB, 16)
+    head = ((A - (dst & (A - 1))) & (A - 1)) // so
+    head = min(head, n)
+    nch = (n - head) // K
+    sa = src + head * si
+    r = sa & 15
+    if r and nch:
+        if (sa & ~15) < lo:
+            head += K
+            nch -= 1
+            sa += 16
+        if nch and (sa & ~15) + 16 * nch + 16 > hi:
+            nch -= 1
+    sbase = sa & ~15
+    win = (sbase, sbase + 16 * nch + (16 if r else 0)) if nch else None
+    dbase = dst + head * so
+    return head, nch, K, win, (dbase, dbase + nch * OB) if nch else None, A
+
+
+def check_plan(plan, data_base, dst_align, data_bytes):
+    outs = plan.outputs()
+    st = plan.stats()
+    # output bases: consecutive, each aligned to dst_align (>= itemsize)
+    bases, at = [], 1 << 20
+    for o in outs:
+        isz = max(1, o["bytes"] // max(1, o["numel"]))
+        a = max(dst_align, isz)
+        at = (at + a - 1) // a * a
+        if dst_align < 16:
+            at += isz if (at // isz) % 2 == 0 else 0  # deliberately not 16-byte aligned
+        bases.append(at)
+        at += o["bytes"]
+    lo, hi = data_base, data_base + data_bytes
+    for k in range(st["pieces"]):
+        p = plan.piece(k)
+        si, so = CLS[p["cls"]]
+        n = p["count"]
+        src = data_base + p["src"]
+        out_base = bases[p["output"]]
+        assert out_base % so == 0
+        dst = out_base + p["dst"]
+        head, nch, K, win, drange, A = split(src, dst, n, si, so, lo, hi)
+        assert 0 <= head <= n and head + nch * K <= n
+        # scalar elements read [src + e si, +si) for e in head ∪ tail, all inside the piece's bytes
+        assert lo <= src and src + n * si <= hi
+        if win:
+            assert lo <= win[0] and win[1] <= hi, (k, win, lo, hi)
+            assert drange[0] % A == 0
+            assert out_base <= drange[0] and drange[1] <= out_base + outs[p["output"]]["bytes"]
+        assert dst + n * so <= out_base + outs[p["output"]]["bytes"]
+        if p["scale"] != (1 << 64) - 1:
+            assert lo <= data_base + p["scale"] and data_base + p["scale"] + 4 <= hi
+    # grid: blocks of 8 warps cover every worker; parts arrays have workers + 1 entries
+    blocks = (st["workers"] + 7) // 8
+    assert blocks * 8 >= st["workers"]
+    for c in range(st["chunks"]):
+        a, b = plan.worker(c, st["workers"] - 1)
+        assert b <= st["pieces"]
+
+
+def _plan(stmat, wl, workers, chunk=0, dst=None):
+    from safetensors_materialization_gb300 import synth
+    w = synth.WORKLOADS[wl]()
+    lay = w.files[0]
+    ix = stmat.Index.from_header(lay.header, lay.data_bytes)
+    if w.rename:
+        ix = ix.view_rename(w.rename)
+    if w.prefix:
+        ix = ix.view_prefix(w.prefix)
+    return ix.plan(dst=dst or w.dst[0], scale_suffix=w.scale_suffix, workers=workers, chunk_bytes=chunk,
+                   host_only=True), lay
+
+
+@pytest.mark.parametrize("wl,workers,chunk", [("tiny", 664, 0), ("stress", 9728, 0), ("stress", 777, 1 << 26)])
+@pytest.mark.parametrize("residue", [0, 1, 7, 8, 15])
+def test_workload_accesses_stay_in_bounds(stmat, wl, workers, chunk, residue):
+    plan, lay = _plan(stmat, wl, workers, chunk)
+    base = (1 << 32) + residue + (lay.data_start if residue == 7 else 0)
+    for dst_align in (256, 2):
+        check_plan(plan, base, dst_align, lay.data_bytes)
+
+
+@pytest.mark.parametrize("residue", [0, 3, 8, 13])
+def test_special_value_files_in_bounds(stmat, residue):
+    """Files like the GPU edge tests build: every class, tiny to multi-chunk
+    tensors, at the start and the end of the data section."""
+    import json
+    import struct
+    ents, off = {}, 0
+    rng = np.random.Generator(np.random.PCG64(residue))
+    dts = ["F32", "F16", "BF16", "F8_E4M3", "F8_E5M2", "I64", "BOOL", "U8"]
+    isz = {"F32": 4, "F16": 2, "BF16": 2, "F8_E4M3": 1, "F8_E5M2": 1, "I64": 8, "BOOL": 1, "U8": 1}
+    for i in range(120):
+        dt = dts[i % len(dts)]
+        n = int(rng.choice([1, 2, 3, 5, 15, 16, 17, 31, 33, 255, 257, 4097, 70001]))
+        ents[f"t{i:03d}"] = {"dtype": dt, "shape": [n], "data_offsets": [off, off + n * isz[dt]]}
+        off += n * isz[dt]
+    h = json.dumps(ents).encode()
+    ix = stmat.Index.from_header(struct.pack("<Q", len(h)) + h, off)
+    for dst in ("BF16", "F16", "F32", "KEEP"):
+        for workers in (1, 3, 64):
+            plan = ix.plan(dst=dst, workers=workers, host_only=True)
+            for dst_align in (256, 2, 1):
+                check_plan(plan, (1 << 32) + residue, dst_align, off)
