@@ -14,7 +14,8 @@ import os
 import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libstmat.so")
+# STMAT_LIB may point at another build of the library (e.g. a tuning variant).
+LIB_PATH = os.environ.get("STMAT_LIB") or os.path.join(HERE, "libstmat.so")
 
 DTYPES = ["BOOL", "U8", "I8", "I16", "U16", "I32", "U32", "I64", "U64", "F16", "BF16", "F32", "F64",
           "F8_E4M3", "F8_E5M2", "KEEP"]

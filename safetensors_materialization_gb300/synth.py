@@ -226,7 +226,7 @@ def scaled_fp8(seed=2, blocks=57):
             ents += [Entry(base + "weight", "F8_E4M3", shape), Entry(base + "scale_weight", "F32", [])]
     ents.sort(key=lambda e: e.name)
     lay = make_layout(ents, metadata={"format": "pt", "quantization": "scaled_fp8"})
-    return Workload("scaled_fp8_e4m3_57blk", [lay], [seed], ["BF16"],
+    return Workload(f"scaled_fp8_e4m3_{blocks}blk", [lay], [seed], ["BF16"],
                     scale_suffix=(".weight", ".scale_weight"))
 
 
@@ -298,7 +298,9 @@ def stress(seed=4, n=100_000):
     return Workload("stress_100k_misaligned", [lay], [seed], ["BF16"], whole_file_on_device=True)
 
 
-WORKLOADS = {"tiny": tiny, "unet": unet, "scaled_fp8": scaled_fp8, "llm8b": llm8b, "stress": stress}
+WORKLOADS = {"tiny": tiny, "unet": unet, "scaled_fp8": scaled_fp8, "llm8b": llm8b, "stress": stress,
+             # a 5-block slice of the scaled-fp8 checkpoint (1.04 GB source), for profiling
+             "scaled_fp8_5blk": lambda: scaled_fp8(blocks=5)}
 
 
 def build_workload_file(wl: Workload, k: int, out: np.ndarray | None = None):

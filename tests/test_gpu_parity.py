@@ -141,7 +141,9 @@ def special_image(seed=0):
     for fmt in ("F8_E4M3", "F8_E5M2"):
         add(f"{fmt}.raw.weight", fmt, all8)
         for j, s in enumerate(scales):
-            add(f"{fmt}.s{j}.weight", fmt, np.tile(all8, 3))
+            # 767 values: the second copy is shifted by one, so every pattern
+            # lands in both halves of an element pair
+            add(f"{fmt}.s{j}.weight", fmt, np.concatenate([all8, all8[1:], all8]))
             add(f"{fmt}.s{j}.scale_weight", "F32", np.array([s], dtype=np.float32).view(np.uint32))
             ents[f"{fmt}.s{j}.scale_weight"]["shape"] = []
     return image_of(ents, b"".join(parts), pad=3)

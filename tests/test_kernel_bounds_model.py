@@ -1,7 +1,8 @@
 """CPU model of the materialize kernel's address arithmetic (no GPU).
 
 Restates, per piece, how the kernel splits a piece into a scalar head, a
-vector body of 16-byte source chunks and a scalar tail, and checks that for
+vector body of SB-byte source steps (16, 8 or 4 bytes by class) and a
+scalar tail, and checks that for
 the plans the GPU tests and the benchmark run, every byte the kernel reads
 lies in the data section, every byte it writes lies in the piece's output,
 and head + body + tail cover the piece's elements exactly once.  Data bases
@@ -18,26 +19,28 @@ CLS = {0: (1, 1), 1: (4, 2), 2: (4, 2), 3: (2, 2), 4: (2, 4), 5: (2, 2), 6: (2, 
 
 
 def split(src, dst, n, si, so, lo, hi):
-    """Mirror of run_piece: returns (head, nch, vector source window, vector dst range)."""
-    K = 16 // si
-    OB = K * so
-    A = min(OB, 16)
+    """Mirror of run_piece: returns (head, steps, elements per step, source
+    window of the vector body, destination range of the body, its alignment)."""
+    SB = 16 * si // so if so > si else 16   # source bytes per lane step
+    KS = SB // si
+    OS = KS * so
+    A = OS
     head = ((A - (dst & (A - 1))) & (A - 1)) // so
     head = min(head, n)
-    nch = (n - head) // K
+    nst = (n - head) // KS
     sa = src + head * si
-    r = sa & 15
-    if r and nch:
-        if (sa & ~15) < lo:
-            head += K
-            nch -= 1
-            sa += 16
-        if nch and (sa & ~15) + 16 * nch + 16 > hi:
-            nch -= 1
-    sbase = sa & ~15
-    win = (sbase, sbase + 16 * nch + (16 if r else 0)) if nch else None
+    r = sa & (SB - 1)
+    if r and nst:
+        if (sa & ~(SB - 1)) < lo:
+            head += KS
+            nst -= 1
+            sa += SB
+        if nst and (sa & ~(SB - 1)) + SB * nst + SB > hi:
+            nst -= 1
+    sbase = sa & ~(SB - 1)
+    win = (sbase, sbase + SB * nst + (SB if r else 0)) if nst else None
     dbase = dst + head * so
-    return head, nch, K, win, (dbase, dbase + nch * OB) if nch else None, A
+    return head, nst, KS, win, (dbase, dbase + nst * OS) if nst else None, A
 
 
 def check_plan(plan, data_base, dst_align, data_bytes):
