@@ -39,6 +39,10 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="unet")
     ap.add_argument("--e2e-chunk-mb", type=int, default=128)
+    ap.add_argument("--workers", type=int, default=0, help="warps to balance over (0: from --blocks-per-sm)")
+    ap.add_argument("--blocks-per-sm", type=int, default=0, help="resident 8-warp blocks per SM (0: library default)")
+    ap.add_argument("--unit-bytes", type=int, default=0, help="traffic per interleaved unit (0: library default)")
+    ap.add_argument("--kernel", type=int, default=0, help="kernel build: 0 auto, 1 streaming, 2 latency")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -249,7 +253,8 @@ def run_ours(args, rank, world, local):
     host = torch.empty(lay.file_bytes, dtype=torch.uint8, pin_memory=True)
     synth.build_workload_file(w, 0, out=host.numpy())
     ix = view_of(w)(stmat.Index.from_file(host.numpy()))
-    plan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix)
+    plan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, workers=args.workers,
+                   blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel)
     dev = torch.empty(lay.file_bytes + 256, dtype=torch.uint8, device="cuda")
     if w.whole_file_on_device:
         dev[:lay.file_bytes].copy_(host)
@@ -273,7 +278,7 @@ def run_ours(args, rank, world, local):
     # ---- device-timed region: K launches, per-launch events on the launching stream
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(1.5)  # let nvidia-smi start sampling before the timed region
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -304,7 +309,8 @@ def run_ours(args, rank, world, local):
     # with per-chunk kernels (st_load), then a device->host read of the status word
     e2e = None
     if not args.no_e2e:
-        eplan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, chunk_bytes=args.e2e_chunk_mb << 20)
+        eplan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, chunk_bytes=args.e2e_chunk_mb << 20,
+                        blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel)
         copy = torch.cuda.Stream()
         hdata = host[lay.data_start:]
         ddata = dev[:lay.data_bytes]
@@ -345,7 +351,8 @@ def run_ours(args, rank, world, local):
                        "tensors": len(infos), "src_dtypes": sorted({o["src_dtype"] for o in infos}),
                        "dst_dtype": w.dst[0], "l2": "inputs exceed L2 (no flush): "
                        f"{(src_bytes + dst_bytes) / 1e9:.2f} GB per step vs 0.129 GB L2",
-                       "workers": st["workers"], "pieces": st["pieces"], "launches_per_step": launches_per_step,
+                       "workers": st["workers"], "pieces": st["pieces"], "kernel_build": st["kernel"],
+                       "launches_per_step": launches_per_step,
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),

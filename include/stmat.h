@@ -171,14 +171,22 @@ typedef struct st_selection {
  * F64 -> 16/32-bit floats is ST_E_UNSUPPORTED_CAST. */
 
 typedef struct st_plan_options {
-  uint32_t workers;     /* warps to balance over; 0 = every resident warp of the current device */
-  uint64_t chunk_bytes; /* 0 = one launch over the whole data section; otherwise the data
-                           section is split in chunks of this size for st_load's pipeline */
-  int32_t host_only;    /* nonzero: build the plan without touching the GPU (requires workers) */
+  uint32_t workers;       /* warps to balance over; 0 = blocks_per_sm resident 8-warp blocks
+                             on every SM of the current device */
+  uint64_t chunk_bytes;   /* 0 = one launch over the whole data section; otherwise the data
+                             section is split in chunks of this size for st_load's pipeline */
+  int32_t host_only;      /* nonzero: build the plan without touching the GPU (requires workers) */
+  uint32_t blocks_per_sm; /* 0 = 3 for the streaming build, the most that fit for the latency build */
+  uint64_t unit_bytes;    /* traffic per interleaved unit; 0 = 32768 */
+  uint32_t kernel;        /* 0 = choose: the latency build when outputs average under 64 KiB of
+                             traffic (many small tensors), else the streaming build; 1 = streaming
+                             build (deep unroll); 2 = latency build (high occupancy) */
 } st_plan_options;
 
-/* Builds the plan: outputs, then pieces (output element ranges) balanced by
- * bytes across `workers` warps per chunk.  Unless host_only, allocates the
+/* Builds the plan: outputs, then pieces (output element ranges).  Each chunk
+ * is cut, in source order, into units of about unit_bytes of traffic (source
+ * plus destination bytes), and unit j is given to warp j mod workers, so that
+ * all warps sweep the data section together.  Unless host_only, allocates the
  * plan's device tables on the current device (cudaMalloc) and uploads them
  * synchronously; call it outside stream capture.  opts may be NULL. */
 st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst_dtype,
@@ -202,8 +210,10 @@ st_status st_plan_output(const st_plan_t *plan, size_t i, st_output_info *info);
 /* Offsets of every output in one buffer, each aligned to `align` (a power of
  * two >= 16); offsets has st_plan_count entries.  `total` is the size. */
 st_status st_plan_arena(const st_plan_t *plan, uint64_t align, uint64_t *offsets, uint64_t *total);
-/* Piece/worker layout (for tests and tuning). */
-st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chunks, uint64_t *pieces);
+/* Piece/worker layout and kernel build (1 streaming, 2 latency), for tests and
+ * tuning; any pointer may be NULL. */
+st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chunks, uint64_t *pieces,
+                        uint32_t *kernel);
 /* Piece k as {src, dst, scale, count, output, class} (host copy). */
 st_status st_plan_piece(const st_plan_t *plan, uint64_t k, uint64_t *src, uint64_t *dst,
                         uint64_t *scale, uint32_t *count, uint32_t *output, uint32_t *cls);

@@ -83,12 +83,16 @@ ST_HD inline int cls_in_size(uint32_t c) {
   }
 }
 
-// Kernels (st_kernels.cu).
-// Resident 256-thread blocks per SM for the materialize kernel, and SM count
-// of the current device.
-st_status kernel_occupancy(int *sms, int *blocks_per_sm);
+// Kernel builds (st_kernels.cu): deep unroll for large tensors, or higher
+// occupancy for many small tensors.
+constexpr uint32_t kKernelStream = 1;
+constexpr uint32_t kKernelLatency = 2;
+
+// Resident 256-thread blocks per SM for a kernel build, and the SM count of
+// the current device.
+st_status kernel_occupancy(uint32_t variant, int *sms, int *blocks_per_sm);
 // Launches the materialize kernel over `a.workers` warps.
-st_status launch_materialize(const LaunchArgs &a, void *stream);
+st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream);
 
 // Error reporting shared by the host files.
 st_status set_error(st_status s, const char *fmt, ...);

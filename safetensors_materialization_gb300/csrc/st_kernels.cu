@@ -175,26 +175,23 @@ struct CopyBytes {
   }
 };
 
-// Lane steps per batch for 16-, 8- and 4-byte source steps (compile-time
-// tuning knobs; the defaults keep about 64 source bytes in flight per lane).
-#ifndef ST_UNROLL_SB16
-#define ST_UNROLL_SB16 4
-#endif
-#ifndef ST_UNROLL_SB8
-#define ST_UNROLL_SB8 8
-#endif
-#ifndef ST_UNROLL_SB4
-#define ST_UNROLL_SB4 16
-#endif
-// Minimum resident blocks per SM requested from the register allocator
-// (0: let ptxas choose).
-#ifndef ST_MIN_BLOCKS
-#define ST_MIN_BLOCKS 0
-#endif
+// Two builds of the kernel share all code but the unroll depth (lane steps
+// per batch for 16-, 8- and 4-byte source steps) and the register budget:
+//  - StreamCfg: about 64 source bytes in flight per lane, <= 64 registers;
+//    for checkpoints of large tensors, run at 3 blocks per SM;
+//  - LatencyCfg: half the depth, <= 40 registers (6 blocks per SM); for
+//    many small tensors, where per-piece latency dominates and more resident
+//    warps hide it.
+struct StreamCfg {
+  static constexpr int kU16 = 4, kU8 = 8, kU4 = 16;
+};
+struct LatencyCfg {
+  static constexpr int kU16 = 2, kU8 = 4, kU4 = 8;
+};
 
-template <class CV>
+template <class Cfg, class CV>
 struct Unroll {
-  static constexpr int value = CV::SB == 16 ? ST_UNROLL_SB16 : CV::SB == 8 ? ST_UNROLL_SB8 : ST_UNROLL_SB4;
+  static constexpr int value = CV::SB == 16 ? Cfg::kU16 : CV::SB == 8 ? Cfg::kU8 : Cfg::kU4;
 };
 
 // ------------------------------------------------------------- data moves
@@ -274,13 +271,14 @@ __device__ __forceinline__ void next_words(const uint32_t (&a)[N], uint32_t (&b)
 // Vector body over lane steps [0, nst): step c's SB bytes start at byte r of
 // the SB-aligned word sbase + SB c (r == 0 when not kMis).  Every lane runs
 // the same number of iterations (shuffles need the whole warp).
-template <class CV, bool kMis>
+template <class Cfg, class CV, bool kMis>
 __device__ __forceinline__ void body(const uint8_t *sbase, uint32_t r, uint8_t *dbase, uint64_t nst, float scale,
                                      uint32_t lane) {
-  constexpr int U = Unroll<CV>::value;
+  constexpr int U = Unroll<Cfg, CV>::value;
   constexpr int N = CV::SB / 4;
-  uint64_t base = 0;
-  for (; base + 32 * U <= nst; base += 32 * U) {
+  const uint64_t nb = nst / (32 * U);  // full batches
+  for (uint64_t i = 0; i < nb; ++i) {
+    const uint64_t base = i * 32 * U;
     uint32_t a[U][N];
 #pragma unroll
     for (int u = 0; u < U; ++u) ldw<N>(sbase + (base + 32 * u + lane) * CV::SB, a[u]);
@@ -292,7 +290,7 @@ __device__ __forceinline__ void body(const uint8_t *sbase, uint32_t r, uint8_t *
       do_step<CV, kMis>(dbase, c, a[u], kMis ? b : a[u], r, scale);
     }
   }
-  for (; base < nst; base += 32) {
+  for (uint64_t base = nb * 32 * U; base < nst; base += 32) {
     const uint64_t c = base + lane;
     const bool valid = c < nst;
     uint32_t a[N];
@@ -322,7 +320,7 @@ __device__ __forceinline__ void scalar_range(const uint8_t *src, uint8_t *dst, u
   }
 }
 
-template <class CV>
+template <class Cfg, class CV>
 __device__ __forceinline__ void run_piece(const uint8_t *data, uint64_t data_bytes, const uint8_t *src, uint8_t *dst,
                                           uint64_t n, float scale, uint32_t lane) {
   constexpr int KS = CV::KS, SB = CV::SB;
@@ -347,8 +345,8 @@ __device__ __forceinline__ void run_piece(const uint8_t *data, uint64_t data_byt
   if (nst) {
     const uint8_t *sbase = reinterpret_cast<const uint8_t *>(sa & ~uintptr_t(SB - 1));
     uint8_t *dbase = dst + head * CV::SO;
-    if (r) body<CV, true>(sbase, r, dbase, nst, scale, lane);
-    else body<CV, false>(sbase, 0, dbase, nst, scale, lane);
+    if (r) body<Cfg, CV, true>(sbase, r, dbase, nst, scale, lane);
+    else body<Cfg, CV, false>(sbase, 0, dbase, nst, scale, lane);
   }
   if (tail < n) scalar_range<CV>(src, dst, tail, n, scale, lane);
 }
@@ -379,13 +377,8 @@ struct Staged {
   float scale[32];
 };
 
-#if ST_MIN_BLOCKS > 0
-#define ST_LAUNCH_BOUNDS __launch_bounds__(kThreads, ST_MIN_BLOCKS)
-#else
-#define ST_LAUNCH_BOUNDS __launch_bounds__(kThreads)
-#endif
-
-__global__ void ST_LAUNCH_BOUNDS materialize_kernel(const LaunchArgs a) {
+template <class Cfg>
+__device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
   __shared__ Staged stage[kWarpsPerBlock];
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t wib = threadIdx.x >> 5;
@@ -425,19 +418,19 @@ __global__ void ST_LAUNCH_BOUNDS materialize_kernel(const LaunchArgs a) {
       const uint8_t *src = a.data + pc.src;
       const uint64_t cnt = pc.count;
       switch (cls) {
-        case CLS_COPY: run_piece<CopyBytes>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_F32_BF16: run_piece<Conv<S_F32, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_F32_F16: run_piece<Conv<S_F32, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_F16_BF16: run_piece<Conv<S_F16, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_F16_F32: run_piece<Conv<S_F16, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_BF16_F16: run_piece<Conv<S_BF16, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_BF16_F32: run_piece<Conv<S_BF16, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E4M3_BF16: run_piece<Conv<S_E4M3, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E4M3_F16: run_piece<Conv<S_E4M3, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E4M3_F32: run_piece<Conv<S_E4M3, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E5M2_BF16: run_piece<Conv<S_E5M2, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E5M2_F16: run_piece<Conv<S_E5M2, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E5M2_F32: run_piece<Conv<S_E5M2, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_COPY: run_piece<Cfg, CopyBytes>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_F32_BF16: run_piece<Cfg, Conv<S_F32, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_F32_F16: run_piece<Cfg, Conv<S_F32, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_F16_BF16: run_piece<Cfg, Conv<S_F16, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_F16_F32: run_piece<Cfg, Conv<S_F16, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_BF16_F16: run_piece<Cfg, Conv<S_BF16, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_BF16_F32: run_piece<Cfg, Conv<S_BF16, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_E4M3_BF16: run_piece<Cfg, Conv<S_E4M3, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_E4M3_F16: run_piece<Cfg, Conv<S_E4M3, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_E4M3_F32: run_piece<Cfg, Conv<S_E4M3, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_E5M2_BF16: run_piece<Cfg, Conv<S_E5M2, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_E5M2_F16: run_piece<Cfg, Conv<S_E5M2, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_E5M2_F32: run_piece<Cfg, Conv<S_E5M2, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
         default:
           if (lane == 0) atomicOr(a.err, kErrBadDst);
       }
@@ -445,23 +438,34 @@ __global__ void ST_LAUNCH_BOUNDS materialize_kernel(const LaunchArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(kThreads) materialize_stream(const LaunchArgs a) { materialize_body<StreamCfg>(a); }
+
+__global__ void __launch_bounds__(kThreads, 6) materialize_latency(const LaunchArgs a) {
+  materialize_body<LatencyCfg>(a);
+}
+
 std::string cuda_msg(cudaError_t e) { return std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e); }
 
 }  // namespace
 
-st_status kernel_occupancy(int *sms, int *blocks_per_sm) {
+st_status kernel_occupancy(uint32_t variant, int *sms, int *blocks_per_sm) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_kernel, kThreads, 0);
+  if (e == cudaSuccess)
+    e = variant == kKernelLatency
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_latency, kThreads, 0)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_stream, kThreads, 0);
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "querying the device: %s", cuda_msg(e).c_str());
   if (*blocks_per_sm < 1) *blocks_per_sm = 1;
   return ST_OK;
 }
 
-st_status launch_materialize(const LaunchArgs &a, void *stream) {
+st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream) {
   const uint32_t blocks = (a.workers + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  materialize_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (variant == kKernelLatency) materialize_latency<<<blocks, kThreads, 0, st>>>(a);
+  else materialize_stream<<<blocks, kThreads, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "materialize launch (%u blocks): %s", blocks, cuda_msg(e).c_str());
   return ST_OK;

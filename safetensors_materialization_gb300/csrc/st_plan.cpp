@@ -33,10 +33,15 @@
 namespace stmat {
 namespace {
 
-constexpr uint64_t kSplitUnits = 64;        // pieces of one output start at multiples of this
+constexpr uint64_t kSplitBytes = 2048;      // pieces of one output start at multiples of this many
+                                            // source bytes: one full batch of lane steps
 constexpr uint64_t kPieceCost = 1024;       // fixed cost of a piece, in bytes of traffic
 constexpr uint64_t kMinWorkerCost = 4096;   // no more warps than total cost / this
 constexpr uint64_t kMaxPieceUnits = 1ull << 30;
+constexpr uint64_t kDefaultUnitBytes = 32768;  // cost of one interleaved unit
+constexpr uint32_t kStreamBlocksPerSm = 3;     // streaming build: fewer, deeper warps
+constexpr uint64_t kSmallOutputBytes = 65536;  // mean traffic per output below which the
+                                               // latency build is chosen
 
 bool is_fp8(int d) { return d == ST_F8_E4M3 || d == ST_F8_E5M2; }
 bool is_float(int d) {
@@ -89,7 +94,9 @@ struct st_plan_s {
   std::shared_ptr<const IndexData> index;
   std::vector<Output> outs;
   uint32_t workers = 1;
+  uint32_t kernel = kKernelStream;
   uint64_t chunk_bytes = 0;
+  uint64_t unit_bytes = kDefaultUnitBytes;
   uint32_t n_chunks = 1;
   std::vector<Piece> pieces;
   std::vector<uint32_t> parts;  // n_chunks * (workers + 1)
@@ -221,6 +228,69 @@ struct Segment {
   uint64_t u0, u1;
 };
 
+// Cuts `segs` (in source order) into n consecutive units of about equal cost
+// (`total` = the segments' cost): appends the units' pieces to *units and the
+// n + 1 unit boundaries to *ub.  Cuts inside an output fall on multiples of
+// kSplitBytes source bytes, and each cut adds one piece's fixed cost.
+void cut_units(const st_plan_s &p, const std::vector<Segment> &segs, uint64_t n, double total,
+               std::vector<Piece> *units, std::vector<uint32_t> *ub) {
+  const Core &core = *p.index->core;
+  units->clear();
+  ub->assign(n + 1, 0);
+  const double share = (total + double(n - 1) * kPieceCost) / n;
+  uint64_t w = 0;
+  double used = 0;  // cost assigned so far (units < w and unit w's part)
+  auto emit = [&](const Segment &s, uint64_t a, uint64_t b) {
+    const Output &o = p.outs[s.out];
+    const Tensor &t = core.tensors[o.entry];
+    const uint64_t si = cls_in_size(o.cls), so = cls_out_size(o.cls);
+    for (uint64_t x = a; x < b; x += kMaxPieceUnits) {
+      uint64_t y = std::min(b, x + kMaxPieceUnits);
+      Piece pc;
+      pc.src = t.begin + x * si;
+      pc.dst = x * so;
+      pc.scale = o.scale >= 0 ? core.tensors[o.scale].begin : kNoScale;
+      pc.count = static_cast<uint32_t>(y - x);
+      pc.out_cls = (s.out << kClsBits) | o.cls;
+      units->push_back(pc);
+    }
+  };
+  auto next_unit = [&]() {
+    ++w;
+    (*ub)[w] = static_cast<uint32_t>(units->size());
+  };
+  for (const Segment &s : segs) {
+    const Output &o = p.outs[s.out];
+    const double per = cls_in_size(o.cls) + cls_out_size(o.cls);
+    const uint64_t granule = kSplitBytes / cls_in_size(o.cls);
+    uint64_t u = s.u0;
+    while (u < s.u1) {
+      double rest = kPieceCost + double(s.u1 - u) * per;
+      double room = (w + 1) * share - used;
+      if (w + 1 == n || rest <= room + 0.5 * kPieceCost) {
+        emit(s, u, s.u1);
+        used += rest;
+        u = s.u1;
+        if (w + 1 < n && used >= (w + 1) * share) next_unit();
+        break;
+      }
+      // Fill the rest of unit w with a prefix that ends on a split boundary.
+      double take = std::floor((room - kPieceCost) / per);
+      uint64_t cut = take > 0 ? u + static_cast<uint64_t>(take) : u;
+      cut -= cut % granule;
+      if (cut > u) {
+        emit(s, u, cut);
+        used += kPieceCost + double(cut - u) * per;
+        u = cut;
+      }
+      // Boundaries are absolute, so the slack this cut left rolls over to
+      // the next unit instead of piling up on the last one.
+      next_unit();
+    }
+  }
+  while (w < n) next_unit();
+}
+
 // Builds pieces and per-chunk worker partitions.
 void build_pieces(st_plan_s *p) {
   const Core &core = *p->index->core;
@@ -258,6 +328,8 @@ void build_pieces(st_plan_s *p) {
   const uint32_t W = p->workers;
   p->pieces.clear();
   p->parts.assign(static_cast<size_t>(p->n_chunks) * (W + 1), 0);
+  std::vector<Piece> units;
+  std::vector<uint32_t> ub;
   for (uint32_t k = 0; k < p->n_chunks; ++k) {
     auto &segs = per_chunk[k];
     std::stable_sort(segs.begin(), segs.end(), [&](const Segment &a, const Segment &b) {
@@ -270,60 +342,21 @@ void build_pieces(st_plan_s *p) {
       const Output &o = p->outs[s.out];
       total += kPieceCost + double(s.u1 - s.u0) * (cls_in_size(o.cls) + cls_out_size(o.cls));
     }
-    // A boundary that falls inside a segment splits it and adds one piece.
-    const double share = (total + double(W - 1) * kPieceCost) / W;
+    // The chunk is cut, in source order, into N = rounds * W units of equal
+    // cost; unit j goes to warp j mod W.  All warps then work through
+    // neighbouring units at the same time, so the GPU's accesses at any moment
+    // fall in one compact window of the data section (better DRAM row
+    // locality than W independent streams), and each warp's share stays
+    // within one unit of the mean.
+    const uint64_t rounds = std::max<uint64_t>(1, static_cast<uint64_t>(std::llround(total / (double(W) * p->unit_bytes))));
+    const uint64_t N = rounds * W;
+    cut_units(*p, segs, N, total, &units, &ub);
     uint32_t *parts = &p->parts[static_cast<size_t>(k) * (W + 1)];
-    uint32_t w = 0;
-    double used = 0;  // cost assigned so far (workers < w and worker w's part)
-    parts[0] = static_cast<uint32_t>(p->pieces.size());
-    auto emit = [&](const Segment &s, uint64_t a, uint64_t b) {
-      const Output &o = p->outs[s.out];
-      const Tensor &t = core.tensors[o.entry];
-      const uint64_t si = cls_in_size(o.cls), so = cls_out_size(o.cls);
-      for (uint64_t x = a; x < b; x += kMaxPieceUnits) {
-        uint64_t y = std::min(b, x + kMaxPieceUnits);
-        Piece pc;
-        pc.src = t.begin + x * si;
-        pc.dst = x * so;
-        pc.scale = o.scale >= 0 ? core.tensors[o.scale].begin : kNoScale;
-        pc.count = static_cast<uint32_t>(y - x);
-        pc.out_cls = (s.out << kClsBits) | o.cls;
-        p->pieces.push_back(pc);
-      }
-    };
-    auto next_worker = [&]() {
-      ++w;
+    for (uint32_t w = 0; w < W; ++w) {
       parts[w] = static_cast<uint32_t>(p->pieces.size());
-    };
-    for (const Segment &s : segs) {
-      const Output &o = p->outs[s.out];
-      const double per = cls_in_size(o.cls) + cls_out_size(o.cls);
-      uint64_t u = s.u0;
-      while (u < s.u1) {
-        double rest = kPieceCost + double(s.u1 - u) * per;
-        double room = (w + 1) * share - used;
-        if (w + 1 == W || rest <= room + 0.5 * kPieceCost) {
-          emit(s, u, s.u1);
-          used += rest;
-          u = s.u1;
-          if (w + 1 < W && used >= (w + 1) * share) next_worker();
-          break;
-        }
-        // Fill the rest of worker w with a prefix that ends on a split boundary.
-        double take = std::floor((room - kPieceCost) / per);
-        uint64_t cut = take > 0 ? u + static_cast<uint64_t>(take) : u;
-        cut -= cut % kSplitUnits;
-        if (cut > u) {
-          emit(s, u, cut);
-          used += kPieceCost + double(cut - u) * per;
-          u = cut;
-        }
-        // Boundaries are absolute, so the slack this cut left rolls over to
-        // the next worker instead of piling up on the last one.
-        next_worker();
-      }
+      for (uint64_t j = w; j < N; j += W) p->pieces.insert(p->pieces.end(), units.begin() + ub[j], units.begin() + ub[j + 1]);
     }
-    while (w < W) next_worker();
+    parts[W] = static_cast<uint32_t>(p->pieces.size());
   }
 }
 
@@ -343,16 +376,33 @@ st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst
     const bool host_only = opts && opts->host_only;
     uint32_t workers = opts ? opts->workers : 0;
     p->chunk_bytes = opts ? opts->chunk_bytes : 0;
+    if (opts && opts->unit_bytes) p->unit_bytes = opts->unit_bytes;
+    uint64_t cost = 0, traffic = 0, nonempty = 0;
+    for (const Output &o : p->outs) {
+      const uint64_t t = o.units * (cls_in_size(o.cls) + cls_out_size(o.cls));
+      cost += kPieceCost + t;
+      traffic += t;
+      nonempty += t > 0;
+    }
+    // Many small tensors: the latency build at full occupancy; else streaming.
+    if (opts && opts->kernel) {
+      if (opts->kernel != kKernelStream && opts->kernel != kKernelLatency)
+        return set_error(ST_E_INVAL, "options.kernel must be 0, 1 or 2");
+      p->kernel = opts->kernel;
+    } else {
+      p->kernel = nonempty && traffic / nonempty < kSmallOutputBytes ? kKernelLatency : kKernelStream;
+    }
     int sms = 0, blocks = 0;
     if (!host_only || workers == 0) {
       if (host_only) return set_error(ST_E_INVAL, "a host-only plan needs options.workers");
-      s = kernel_occupancy(&sms, &blocks);
+      s = kernel_occupancy(p->kernel, &sms, &blocks);
       if (s != ST_OK) return s;
-      if (workers == 0) workers = static_cast<uint32_t>(sms) * static_cast<uint32_t>(blocks) * kWarpsPerBlock;
+      uint32_t bps = static_cast<uint32_t>(blocks);
+      if (opts && opts->blocks_per_sm) bps = std::min(bps, opts->blocks_per_sm);
+      else if (p->kernel == kKernelStream) bps = std::min(bps, kStreamBlocksPerSm);
+      if (workers == 0) workers = static_cast<uint32_t>(sms) * bps * kWarpsPerBlock;
     }
     // No more warps than the work can use.
-    uint64_t cost = 0;
-    for (const Output &o : p->outs) cost += kPieceCost + o.units * (cls_in_size(o.cls) + cls_out_size(o.cls));
     uint64_t cap = std::max<uint64_t>(1, cost / kMinWorkerCost);
     p->workers = static_cast<uint32_t>(std::min<uint64_t>(workers, cap));
     build_pieces(p.get());
@@ -420,8 +470,10 @@ st_status st_plan_arena(const st_plan_t *p, uint64_t align, uint64_t *offsets, u
   return ST_OK;
 }
 
-st_status st_plan_stats(const st_plan_t *p, uint32_t *workers, uint32_t *chunks, uint64_t *pieces) {
+st_status st_plan_stats(const st_plan_t *p, uint32_t *workers, uint32_t *chunks, uint64_t *pieces,
+                        uint32_t *kernel) {
   if (!p) return set_error(ST_E_INVAL, "NULL plan");
+  if (kernel) *kernel = p->kernel;
   if (workers) *workers = p->workers;
   if (chunks) *chunks = p->n_chunks;
   if (pieces) *pieces = p->pieces.size();
@@ -478,7 +530,7 @@ st_status launch_chunk(const st_plan_t *p, uint32_t k, const void *data_dev, voi
   a.dst = dst;
   a.scales = scales;
   a.err = p->d_err;
-  return launch_materialize(a, stream);
+  return launch_materialize(a, p->kernel, stream);
 }
 
 }  // namespace

@@ -60,7 +60,8 @@ class Selection(C.Structure):
 
 
 class PlanOptions(C.Structure):
-    _fields_ = [("workers", C.c_uint32), ("chunk_bytes", C.c_uint64), ("host_only", C.c_int32)]
+    _fields_ = [("workers", C.c_uint32), ("chunk_bytes", C.c_uint64), ("host_only", C.c_int32),
+                ("blocks_per_sm", C.c_uint32), ("unit_bytes", C.c_uint64), ("kernel", C.c_uint32)]
 
 
 _lib = None
@@ -94,7 +95,7 @@ def lib():
             "st_plan_count": [P, C.POINTER(S)],
             "st_plan_output": [P, S, C.POINTER(OutputInfo)],
             "st_plan_arena": [P, U64, C.POINTER(U64), C.POINTER(U64)],
-            "st_plan_stats": [P, C.POINTER(U32), C.POINTER(U32), C.POINTER(U64)],
+            "st_plan_stats": [P, C.POINTER(U32), C.POINTER(U32), C.POINTER(U64), C.POINTER(U32)],
             "st_plan_piece": [P, U64, C.POINTER(U64), C.POINTER(U64), C.POINTER(U64), C.POINTER(U32),
                               C.POINTER(U32), C.POINTER(U32)],
             "st_plan_worker": [P, U32, U32, C.POINTER(U64), C.POINTER(U64)],
@@ -250,7 +251,7 @@ class Index:
         return Index(out.value)
 
     def plan(self, dst="BF16", names=None, scale_names=None, scale_suffix=None, part=0, n_parts=0,
-             workers=0, chunk_bytes=0, host_only=False):
+             workers=0, chunk_bytes=0, host_only=False, blocks_per_sm=0, unit_bytes=0, kernel=0):
         """st_plan: outputs and device work for a selection."""
         sel = Selection()
         keep = []
@@ -265,7 +266,7 @@ class Index:
         if scale_suffix:
             sel.scale_suffix_from, sel.scale_suffix_to = scale_suffix[0].encode(), scale_suffix[1].encode()
         sel.part, sel.n_parts = part, n_parts
-        opts = PlanOptions(workers, chunk_bytes, 1 if host_only else 0)
+        opts = PlanOptions(workers, chunk_bytes, 1 if host_only else 0, blocks_per_sm, unit_bytes, kernel)
         out = C.c_void_p()
         _check(lib().st_plan(self._h, C.byref(sel), DTYPES.index(dst), C.byref(opts), C.byref(out)))
         return Plan(out.value, self)
@@ -310,9 +311,10 @@ class Plan:
         return [offs[i] for i in range(n)], total.value
 
     def stats(self):
-        w, c, p = C.c_uint32(), C.c_uint32(), C.c_uint64()
-        _check(lib().st_plan_stats(self._h, C.byref(w), C.byref(c), C.byref(p)))
-        return {"workers": w.value, "chunks": c.value, "pieces": p.value}
+        w, c, p, k = C.c_uint32(), C.c_uint32(), C.c_uint64(), C.c_uint32()
+        _check(lib().st_plan_stats(self._h, C.byref(w), C.byref(c), C.byref(p), C.byref(k)))
+        return {"workers": w.value, "chunks": c.value, "pieces": p.value,
+                "kernel": {1: "stream", 2: "latency"}.get(k.value, str(k.value))}
 
     def piece(self, k):
         v = [C.c_uint64(), C.c_uint64(), C.c_uint64(), C.c_uint32(), C.c_uint32(), C.c_uint32()]

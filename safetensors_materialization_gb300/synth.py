@@ -188,12 +188,13 @@ def tiny(seed=0):
     return Workload("tiny_16_mixed", [lay], [seed], ["BF16"], prefix="model.")
 
 
-def unet(seed=1):
+def unet(seed=1, n1280=38):
     """UNet-shaped fp16 checkpoint (716 tensors, 1.334 G params) under
-    'model.diffusion_model.'; rename view to 'unet.' and BF16."""
+    'model.diffusion_model.'; rename view to 'unet.' and BF16.  n1280 sets the
+    number of 1280-channel resblocks (38 in the full checkpoint)."""
     p = "model.diffusion_model."
     ents = []
-    for C, n in ((320, 6), (640, 6), (1280, 38)):
+    for C, n in ((320, 6), (640, 6), (1280, n1280)):
         for i in range(n):
             b = f"{p}res_{C}_{i:02d}."
             ents += [Entry(b + "conv1.weight", "F16", [C, C, 3, 3]), Entry(b + "conv1.bias", "F16", [C]),
@@ -211,7 +212,8 @@ def unet(seed=1):
                  Entry(f"{p}transition_{j}.bias", "F16", [co])]
     ents.sort(key=lambda e: e.name)
     lay = make_layout(ents, metadata={"format": "pt"})
-    return Workload("unet_fp16_716", [lay], [seed], ["BF16"], rename=[(p, "unet.")])
+    name = "unet_fp16_716" if n1280 == 38 else f"unet_fp16_{len(ents)}"
+    return Workload(name, [lay], [seed], ["BF16"], rename=[(p, "unet.")])
 
 
 def scaled_fp8(seed=2, blocks=57):
@@ -300,7 +302,9 @@ def stress(seed=4, n=100_000):
 
 WORKLOADS = {"tiny": tiny, "unet": unet, "scaled_fp8": scaled_fp8, "llm8b": llm8b, "stress": stress,
              # a 5-block slice of the scaled-fp8 checkpoint (1.04 GB source), for profiling
-             "scaled_fp8_5blk": lambda: scaled_fp8(blocks=5)}
+             "scaled_fp8_5blk": lambda: scaled_fp8(blocks=5),
+             # a UNet with 8 of the 38 1280-channel resblocks (0.83 GB source), for profiling
+             "unet_small": lambda: unet(n1280=8)}
 
 
 def build_workload_file(wl: Workload, k: int, out: np.ndarray | None = None):

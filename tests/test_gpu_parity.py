@@ -62,11 +62,11 @@ class Packed:
 
 
 def run(stmat, image, dst="BF16", view=None, scale_suffix=None, whole=True, offset=0, packed=False,
-        workers=0, scales=None):
+        workers=0, scales=None, kernel=0):
     ix = stmat.Index.from_file(image)
     if view:
         ix = view(ix)
-    plan = ix.plan(dst=dst, scale_suffix=scale_suffix, workers=workers)
+    plan = ix.plan(dst=dst, scale_suffix=scale_suffix, workers=workers, kernel=kernel)
     hlen, dbytes = ix.sizes()
     buf, data_ptr = to_device(image, offset, whole, 8 + hlen)
     outs = Packed(plan) if packed else stmat.Outputs(plan)
@@ -151,10 +151,12 @@ def special_image(seed=0):
 
 @pytest.mark.parametrize("dst", ["BF16", "F16", "F32"])
 @pytest.mark.parametrize("packed", [False, True])
-def test_every_bit_pattern(stmat, oracle, dst, packed):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_every_bit_pattern(stmat, oracle, dst, packed, kernel):
     img = special_image()
     sfx = (".weight", ".scale_weight")
-    plan, outs, _ = run(stmat, img, dst=dst, scale_suffix=sfx, packed=packed)
+    plan, outs, _ = run(stmat, img, dst=dst, scale_suffix=sfx, packed=packed, kernel=kernel)
+    assert plan.stats()["kernel"] == {1: "stream", 2: "latency"}[kernel]
     sel, want = oracle_all(oracle, img, dst=dst, scale_suffix=sfx)
     assert_same(plan, outs, sel, want)
 
@@ -195,9 +197,10 @@ def test_alignment_sweep(stmat, oracle, residue):
     for dst in ("BF16", "F16", "F32", "KEEP"):
         sel, want = oracle_all(oracle, img, dst=dst)
         for packed in (False, True):
-            plan, outs, _ = run(stmat, img, dst=dst, offset=residue, packed=packed,
-                                workers=[0, 7, 333][residue % 3])
-            assert_same(plan, outs, sel, want)
+            for kernel in (1, 2):
+                plan, outs, _ = run(stmat, img, dst=dst, offset=residue, packed=packed,
+                                    workers=[0, 7, 333][residue % 3], kernel=kernel)
+                assert_same(plan, outs, sel, want)
 
 
 def test_data_section_edges(stmat, oracle):
