@@ -257,6 +257,36 @@ st_status st_stage_h2d(void *dst_dev, const void *src_host, uint64_t bytes, uint
 st_status st_load(const void *data_host, void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
                   const float *scales, void *copy_stream, void *compute_stream);
 
+/* Allocation-free st_materialize.  No counterpart on the pages: it exists for
+ * callers that cannot allocate device memory, for example code running while a
+ * CUDA stream capture forbids cudaMalloc, or processes whose device memory is
+ * entirely held by another allocator (a framework's caching pool, a serving
+ * engine's preallocated arena) so that cudaMalloc fails even though memory is
+ * free inside that pool.  Such a caller builds the plan with host_only set
+ * (st_plan then touches no GPU memory) and calls this instead of
+ * st_materialize; arguments are as for st_materialize.
+ *   - Scratch: the plan's piece table, warp ranges and error word are copied
+ *     (cudaMemcpyAsync from the plan's host memory, cudaMemsetAsync for the
+ *     error word) into one static device array of 4 MiB built into the
+ *     library.  Every GPU that loads the library holds those 4 MiB until the
+ *     process exits.  A plan that needs more (32 bytes per piece plus 4 per
+ *     warp per chunk, each part rounded up to 256 bytes) is rejected with
+ *     ST_E_INVAL before anything is queued; plan with a larger unit_bytes or
+ *     fewer workers to shrink it.
+ *   - Set-up: the first call on a device, with that device current, looks up
+ *     the array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - Sharing: every call, on every stream, uses the same array, and it keeps
+ *     the last call's contents; the error word is cleared by each call.  Calls
+ *     whose work overlaps on the GPU (different streams, or threads) race on
+ *     the array and corrupt each other: order them on one stream.
+ *   - No cudaMalloc, cudaFree or other allocating CUDA or library routine is
+ *     called.  A NULL or misaligned destination is skipped as in
+ *     st_materialize but not reported (the flag stays in the array).
+ * Returns without synchronizing. */
+st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
+                                 const float *scales, void *stream);
+
 /* Waits for `stream`, then reads and clears the plan's device error flags:
  * bit 0 = a non-empty output had a NULL or misaligned destination.
  * Returns ST_E_DEVICE when any flag was set. */

@@ -94,6 +94,11 @@ st_status kernel_occupancy(uint32_t variant, int *sms, int *blocks_per_sm);
 // Launches the materialize kernel over `a.workers` warps.
 st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream);
 
+// Size of the device array behind st_materialize_noalloc, and its device
+// address on the current device (looked up on first use per device).
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+st_status static_scratch(void **addr);
+
 // Error reporting shared by the host files.
 st_status set_error(st_status s, const char *fmt, ...);
 

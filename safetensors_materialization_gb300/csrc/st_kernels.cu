@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 #include <string>
 
 #include "st_internal.h"
@@ -468,6 +469,40 @@ st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream
   else materialize_stream<<<blocks, kThreads, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "materialize launch (%u blocks): %s", blocks, cuda_msg(e).c_str());
+  return ST_OK;
+}
+
+// ------------------------------------------------ allocation-free scratch
+//
+// Scratch for st_materialize_noalloc: the plan's piece table, warp ranges and
+// error word are copied here instead of into memory the library allocates.
+// The array is part of the module image, so every device that loads the
+// library holds these bytes until the process exits.  In host code the name
+// g_static_scratch is only a host-side stand-in, never a device address: the
+// device address comes from cudaGetSymbolAddress, looked up once per device
+// with that device current.
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 256;
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices] = {};
+}  // namespace
+
+st_status static_scratch(void **addr) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "cudaGetDevice: %s", cuda_msg(e).c_str());
+  if (dev < 0 || dev >= kMaxDevices) return set_error(ST_E_INVAL, "device %d is beyond the %d supported", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return set_error(ST_E_CUDA, "looking up the static scratch on device %d: %s", dev, cuda_msg(e).c_str());
+    g_static_addr[dev] = p;
+  }
+  *addr = g_static_addr[dev];
   return ST_OK;
 }
 

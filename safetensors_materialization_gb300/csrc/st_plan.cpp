@@ -603,6 +603,49 @@ st_status st_load(const void *data_host, void *data_dev, const st_plan_t *p, voi
   return ST_OK;
 }
 
+st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *p, void *const *dst_ptrs,
+                                 const float *scales, void *stream) {
+  if (!p) return set_error(ST_E_INVAL, "NULL plan");
+  if (p->pieces.empty()) return ST_OK;
+  if (!data_dev || !dst_ptrs) return set_error(ST_E_INVAL, "NULL data or destination array");
+  // Layout inside the static array: pieces | warp ranges | error word.
+  const size_t pieces_bytes = p->pieces.size() * sizeof(Piece);
+  const size_t parts_off = (pieces_bytes + 255) & ~size_t(255);
+  const size_t parts_bytes = p->parts.size() * sizeof(uint32_t);
+  const size_t err_off = (parts_off + parts_bytes + 255) & ~size_t(255);
+  const size_t need = err_off + sizeof(uint32_t);
+  if (need > kStaticScratchBytes)
+    return set_error(ST_E_INVAL,
+                     "the plan needs %zu bytes of static scratch (%zu pieces, %u warps, %u chunks) but the library "
+                     "holds %zu; plan with a larger unit_bytes or fewer workers",
+                     need, p->pieces.size(), p->workers, p->n_chunks, kStaticScratchBytes);
+  void *scratch = nullptr;
+  st_status s = static_scratch(&scratch);
+  if (s != ST_OK) return s;
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(base, p->pieces.data(), pieces_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(base + parts_off, p->parts.data(), parts_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(base + err_off, 0, sizeof(uint32_t), st);  // left over from the last call
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "filling the static scratch: %s", cuda_msg(e).c_str());
+  for (uint32_t k = 0; k < p->n_chunks; ++k) {
+    const uint32_t *parts = &p->parts[static_cast<size_t>(k) * (p->workers + 1)];
+    if (parts[0] == parts[p->workers]) continue;
+    LaunchArgs a;
+    a.data = static_cast<const uint8_t *>(data_dev);
+    a.data_bytes = p->index->core->data_bytes;
+    a.pieces = reinterpret_cast<const Piece *>(base);
+    a.parts = reinterpret_cast<const uint32_t *>(base + parts_off) + static_cast<size_t>(k) * (p->workers + 1);
+    a.workers = p->workers;
+    a.dst = dst_ptrs;
+    a.scales = scales;
+    a.err = reinterpret_cast<uint32_t *>(base + err_off);
+    s = launch_materialize(a, p->kernel, stream);
+    if (s != ST_OK) return s;
+  }
+  return ST_OK;
+}
+
 st_status st_plan_check(const st_plan_t *p, void *stream, uint32_t *flags) {
   if (!p || !flags) return set_error(ST_E_INVAL, "NULL argument");
   st_status s = check_device_plan(p);

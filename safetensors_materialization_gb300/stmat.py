@@ -30,6 +30,7 @@ EXPORTS = [
     "st_index_metadata_get", "st_view_prefix", "st_view_filter", "st_view_rename", "st_plan",
     "st_plan_free", "st_plan_count", "st_plan_output", "st_plan_arena", "st_plan_stats",
     "st_plan_piece", "st_plan_worker", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
+    "st_materialize_noalloc",
     "st_last_error", "st_status_name", "st_dtype_size", "st_dtype_name", "st_version",
 ]
 
@@ -100,6 +101,7 @@ def lib():
                               C.POINTER(U32), C.POINTER(U32)],
             "st_plan_worker": [P, U32, U32, C.POINTER(U64), C.POINTER(U64)],
             "st_materialize": [P, P, P, P, P],
+            "st_materialize_noalloc": [P, P, P, P, P],
             "st_stage_h2d": [P, P, U64, U64, P, P],
             "st_load": [P, P, P, P, P, P, P],
             "st_plan_check": [P, P, C.POINTER(U32)],
@@ -331,6 +333,12 @@ class Plan:
         """st_materialize.  data: device uint8 tensor (or address) of the data
         section; dst_ptrs: device int64 tensor of output addresses."""
         _check(lib().st_materialize(_addr(data), self._h, _addr(dst_ptrs), _addr(scales), _stream(stream)))
+
+    def materialize_noalloc(self, data, dst_ptrs, scales=None, stream=None):
+        """st_materialize_noalloc: as materialize(), with the plan's tables in
+        the library's static device scratch instead of allocated memory."""
+        _check(lib().st_materialize_noalloc(_addr(data), self._h, _addr(dst_ptrs), _addr(scales),
+                                            _stream(stream)))
 
     def load(self, data_host, data_dev, dst_ptrs, scales=None, copy_stream=None, compute_stream=None):
         """st_load: staged copy of the data section overlapped with materialize."""
