@@ -1,0 +1,78 @@
+"""Multi-rank path on CPU (gloo, world size 2): each rank plans its own part
+of a checkpoint with st_selection.part/n_parts (host-only plans, no GPU), the
+parts are exchanged over the process group, and their union must be every
+output exactly once, in order, with the same bytes as the oracle's parts.
+The step-time reduction bench.py uses (max over ranks) is checked too.
+"""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    try:
+        import sys
+        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+        sys.path.insert(0, root)
+        from safetensors_materialization_gb300 import stmat, synth
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        lay = synth.unet().files[0]
+        ix = stmat.Index.from_header(lay.header, lay.data_bytes).view_rename([("model.diffusion_model.", "unet.")])
+        plan = ix.plan(dst="BF16", part=rank, n_parts=world, workers=1024, host_only=True)
+        mine = [(o["name"], o["bytes"]) for o in plan.outputs()]
+        parts = [None] * world
+        dist.all_gather_object(parts, mine)
+        t = torch.tensor([1.5 + rank])        # a stand-in step time per rank
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        q.put((rank, parts, float(t.item())))
+        dist.destroy_process_group()
+    except Exception as e:  # noqa: BLE001 - reported to the parent
+        q.put((rank, repr(e), None))
+
+
+def test_two_ranks_partition_outputs(stmat, oracle):
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=300) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    results.sort()
+    for rank, parts, tmax in results:
+        assert not isinstance(parts, str), parts
+        assert tmax == 2.5                      # max over ranks
+    parts = results[0][1]
+    assert results[1][1] == parts               # every rank sees the same split
+    from safetensors_materialization_gb300 import synth
+    import numpy as np
+    lay = synth.unet().files[0]
+    full = stmat.Index.from_header(lay.header, lay.data_bytes).view_rename(
+        [("model.diffusion_model.", "unet.")]).plan(dst="BF16", workers=1024, host_only=True)
+    everything = [(o["name"], o["bytes"]) for o in full.outputs()]
+    assert parts[0] + parts[1] == everything    # disjoint, contiguous, complete
+    total = sum(b for _, b in everything)
+    biggest = max(b for _, b in everything)
+    for p in parts:
+        assert abs(sum(b for _, b in p) - total / world) <= biggest
+    # the oracle's parts are the same
+    img = np.concatenate([np.frombuffer(lay.header, dtype=np.uint8), np.zeros(lay.data_bytes, np.uint8)])
+    oix = oracle.parse(img).view_rename([("model.diffusion_model.", "unet.")])
+    for r in range(world):
+        assert [(o["name"], o["bytes"]) for o in oix.select(dst="BF16", part=r, nparts=world).outputs()] == parts[r]
