@@ -43,6 +43,7 @@ def parse_args():
     ap.add_argument("--blocks-per-sm", type=int, default=0, help="resident 8-warp blocks per SM (0: library default)")
     ap.add_argument("--unit-bytes", type=int, default=0, help="traffic per interleaved unit (0: library default)")
     ap.add_argument("--kernel", type=int, default=0, help="kernel build: 0 auto, 1 streaming, 2 latency")
+    ap.add_argument("--order", type=int, default=0, help="unit order: 0 class-major, 1 source")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -254,7 +255,8 @@ def run_ours(args, rank, world, local):
     synth.build_workload_file(w, 0, out=host.numpy())
     ix = view_of(w)(stmat.Index.from_file(host.numpy()))
     plan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, workers=args.workers,
-                   blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel)
+                   blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel,
+                   order=args.order)
     dev = torch.empty(lay.file_bytes + 256, dtype=torch.uint8, device="cuda")
     if w.whole_file_on_device:
         dev[:lay.file_bytes].copy_(host)
@@ -310,7 +312,8 @@ def run_ours(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         eplan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, chunk_bytes=args.e2e_chunk_mb << 20,
-                        blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel)
+                        blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel,
+                   order=args.order)
         copy = torch.cuda.Stream()
         hdata = host[lay.data_start:]
         ddata = dev[:lay.data_bytes]

@@ -181,12 +181,14 @@ typedef struct st_plan_options {
   uint32_t kernel;        /* 0 = choose: the latency build when outputs average under 64 KiB of
                              traffic (many small tensors), else the streaming build; 1 = streaming
                              build (deep unroll); 2 = latency build (high occupancy) */
+  uint32_t order;         /* unit order within a chunk: 0 = grouped by conversion class, then
+                             source order (all warps run one class at a time); 1 = source order */
 } st_plan_options;
 
 /* Builds the plan: outputs, then pieces (output element ranges).  Each chunk
- * is cut, in source order, into units of about unit_bytes of traffic (source
- * plus destination bytes), and unit j is given to warp j mod workers, so that
- * all warps sweep the data section together.  Unless host_only, allocates the
+ * is cut, in class-major source order, into units of about unit_bytes of
+ * traffic (source plus destination bytes), and unit j is given to warp
+ * j mod workers, so that all warps sweep the data section together.  Unless host_only, allocates the
  * plan's device tables on the current device (cudaMalloc) and uploads them
  * synchronously; call it outside stream capture.  opts may be NULL. */
 st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst_dtype,

@@ -186,8 +186,21 @@ struct CopyBytes {
 struct StreamCfg {
   static constexpr int kU16 = 4, kU8 = 8, kU4 = 16;
 };
+// Compile-time tuning knobs for the latency build (defaults measured best).
+#ifndef ST_LAT_U16
+#define ST_LAT_U16 2
+#endif
+#ifndef ST_LAT_U8
+#define ST_LAT_U8 4
+#endif
+#ifndef ST_LAT_U4
+#define ST_LAT_U4 8
+#endif
+#ifndef ST_LAT_MIN_BLOCKS
+#define ST_LAT_MIN_BLOCKS 6
+#endif
 struct LatencyCfg {
-  static constexpr int kU16 = 2, kU8 = 4, kU4 = 8;
+  static constexpr int kU16 = ST_LAT_U16, kU8 = ST_LAT_U8, kU4 = ST_LAT_U4;
 };
 
 template <class Cfg, class CV>
@@ -272,26 +285,47 @@ __device__ __forceinline__ void next_words(const uint32_t (&a)[N], uint32_t (&b)
 // Vector body over lane steps [0, nst): step c's SB bytes start at byte r of
 // the SB-aligned word sbase + SB c (r == 0 when not kMis).  Every lane runs
 // the same number of iterations (shuffles need the whole warp).
+// One batch of U lane steps: issue every load, then convert and store.
+template <class CV, int U>
+__device__ __forceinline__ void load_batch(const uint8_t *sbase, uint64_t base, uint32_t lane,
+                                           uint32_t (&a)[U][CV::SB / 4]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) ldw<CV::SB / 4>(sbase + (base + 32 * u + lane) * CV::SB, a[u]);
+}
+
+template <class CV, bool kMis, int U>
+__device__ __forceinline__ void process_batch(const uint8_t *sbase, uint32_t r, uint8_t *dbase, uint64_t base,
+                                              float scale, uint32_t lane, const uint32_t (&a)[U][CV::SB / 4]) {
+  constexpr int N = CV::SB / 4;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint64_t c = base + 32 * u + lane;
+    if constexpr (kMis) {
+      uint32_t b[N];
+      next_words<N>(a[u], b, lane == 31, sbase + (c + 1) * CV::SB);
+      do_step<CV, true>(dbase, c, a[u], b, r, scale);
+    } else {
+      do_step<CV, false>(dbase, c, a[u], a[u], r, scale);
+    }
+  }
+}
+
+// Vector body over lane steps [0, nst): step c's SB bytes start at byte r of
+// the SB-aligned word sbase + SB c (r == 0 when not kMis).  Every lane runs
+// the same number of iterations (shuffles need the whole warp).
 template <class Cfg, class CV, bool kMis>
 __device__ __forceinline__ void body(const uint8_t *sbase, uint32_t r, uint8_t *dbase, uint64_t nst, float scale,
                                      uint32_t lane) {
   constexpr int U = Unroll<Cfg, CV>::value;
   constexpr int N = CV::SB / 4;
-  const uint64_t nb = nst / (32 * U);  // full batches
+  constexpr uint64_t B = 32 * U;
+  const uint64_t nb = nst / B;  // full batches
   for (uint64_t i = 0; i < nb; ++i) {
-    const uint64_t base = i * 32 * U;
-    uint32_t a[U][N];
-#pragma unroll
-    for (int u = 0; u < U; ++u) ldw<N>(sbase + (base + 32 * u + lane) * CV::SB, a[u]);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint64_t c = base + 32 * u + lane;
-      uint32_t b[N];
-      if constexpr (kMis) next_words<N>(a[u], b, lane == 31, sbase + (c + 1) * CV::SB);
-      do_step<CV, kMis>(dbase, c, a[u], kMis ? b : a[u], r, scale);
-    }
+    uint32_t x[U][N];
+    load_batch<CV, U>(sbase, i * B, lane, x);
+    process_batch<CV, kMis, U>(sbase, r, dbase, i * B, scale, lane, x);
   }
-  for (uint64_t base = nb * 32 * U; base < nst; base += 32) {
+  for (uint64_t base = nb * B; base < nst; base += 32) {
     const uint64_t c = base + lane;
     const bool valid = c < nst;
     uint32_t a[N];
@@ -304,11 +338,14 @@ __device__ __forceinline__ void body(const uint8_t *sbase, uint32_t r, uint8_t *
   }
 }
 
-// Elements [a, b) one per lane, with byte loads (any source alignment).
+// Elements [0, head) and [tail, n) one per lane, with byte loads (any source
+// alignment); one loop serves both ends so each class has one copy of it.
 template <class CV>
-__device__ __forceinline__ void scalar_range(const uint8_t *src, uint8_t *dst, uint64_t a, uint64_t b, float scale,
-                                             uint32_t lane) {
-  for (uint64_t e = a + lane; e < b; e += 32) {
+__device__ __forceinline__ void scalar_ends(const uint8_t *src, uint8_t *dst, uint64_t head, uint64_t tail,
+                                            uint64_t n, float scale, uint32_t lane) {
+  const uint64_t count = head + (n - tail);
+  for (uint64_t i = lane; i < count; i += 32) {
+    const uint64_t e = i < head ? i : tail + (i - head);
     const uint8_t *p = src + e * CV::SI;
     uint32_t bits = 0;
 #pragma unroll
@@ -342,14 +379,13 @@ __device__ __forceinline__ void run_piece(const uint8_t *data, uint64_t data_byt
     if (nst && (sa & ~uintptr_t(SB - 1)) + SB * nst + SB > hi) --nst;
   }
   const uint64_t tail = head + nst * KS;
-  if (head) scalar_range<CV>(src, dst, 0, head, scale, lane);
+  if (head || tail < n) scalar_ends<CV>(src, dst, head, tail, n, scale, lane);
   if (nst) {
     const uint8_t *sbase = reinterpret_cast<const uint8_t *>(sa & ~uintptr_t(SB - 1));
     uint8_t *dbase = dst + head * CV::SO;
     if (r) body<Cfg, CV, true>(sbase, r, dbase, nst, scale, lane);
     else body<Cfg, CV, false>(sbase, 0, dbase, nst, scale, lane);
   }
-  if (tail < n) scalar_range<CV>(src, dst, tail, n, scale, lane);
 }
 
 // Binary32 from 4 little-endian bytes at any alignment.
@@ -441,7 +477,7 @@ __device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
 
 __global__ void __launch_bounds__(kThreads) materialize_stream(const LaunchArgs a) { materialize_body<StreamCfg>(a); }
 
-__global__ void __launch_bounds__(kThreads, 6) materialize_latency(const LaunchArgs a) {
+__global__ void __launch_bounds__(kThreads, ST_LAT_MIN_BLOCKS) materialize_latency(const LaunchArgs a) {
   materialize_body<LatencyCfg>(a);
 }
 

@@ -62,7 +62,8 @@ class Selection(C.Structure):
 
 class PlanOptions(C.Structure):
     _fields_ = [("workers", C.c_uint32), ("chunk_bytes", C.c_uint64), ("host_only", C.c_int32),
-                ("blocks_per_sm", C.c_uint32), ("unit_bytes", C.c_uint64), ("kernel", C.c_uint32)]
+                ("blocks_per_sm", C.c_uint32), ("unit_bytes", C.c_uint64), ("kernel", C.c_uint32),
+                ("order", C.c_uint32)]
 
 
 _lib = None
@@ -253,7 +254,7 @@ class Index:
         return Index(out.value)
 
     def plan(self, dst="BF16", names=None, scale_names=None, scale_suffix=None, part=0, n_parts=0,
-             workers=0, chunk_bytes=0, host_only=False, blocks_per_sm=0, unit_bytes=0, kernel=0):
+             workers=0, chunk_bytes=0, host_only=False, blocks_per_sm=0, unit_bytes=0, kernel=0, order=0):
         """st_plan: outputs and device work for a selection."""
         sel = Selection()
         keep = []
@@ -268,7 +269,7 @@ class Index:
         if scale_suffix:
             sel.scale_suffix_from, sel.scale_suffix_to = scale_suffix[0].encode(), scale_suffix[1].encode()
         sel.part, sel.n_parts = part, n_parts
-        opts = PlanOptions(workers, chunk_bytes, 1 if host_only else 0, blocks_per_sm, unit_bytes, kernel)
+        opts = PlanOptions(workers, chunk_bytes, 1 if host_only else 0, blocks_per_sm, unit_bytes, kernel, order)
         out = C.c_void_p()
         _check(lib().st_plan(self._h, C.byref(sel), DTYPES.index(dst), C.byref(opts), C.byref(out)))
         return Plan(out.value, self)
