@@ -149,6 +149,14 @@ def build_workload(name):
     return w
 
 
+def selection_of(w, ix):
+    """names/slices arguments of a workload's selection (sliced loads)."""
+    if not w.slices:
+        return {}
+    names = [e["name"] for e in ix.entries()]
+    return {"names": names, "slices": [w.slices.get(n) for n in names]}
+
+
 def view_of(w):
     if w.rename:
         return lambda ix: ix.view_rename(w.rename)
@@ -169,7 +177,7 @@ def oracle_sample(w, seconds, reps=1):
     # only the sampled tensors' bytes are generated
     img = synth.build_workload_file(w, 0)
     ix = view_of(w)(O.parse(img))
-    sel = ix.select(dst=w.dst[0], scale_suffix=w.scale_suffix)
+    sel = ix.select(dst=w.dst[0], scale_suffix=w.scale_suffix, **selection_of(w, ix))
     data = img[lay.data_start:]
     outs = sel.outputs()
     # calibrate on the first output, then pick a prefix of outputs
@@ -203,7 +211,8 @@ def run_reference(args, rank, world):
     from safetensors_materialization_gb300 import synth
     lay = w.files[0]
     img = synth.build_workload_file(w, 0)
-    sel = view_of(w)(O.parse(img)).select(dst=w.dst[0], scale_suffix=w.scale_suffix)
+    oix = view_of(w)(O.parse(img))
+    sel = oix.select(dst=w.dst[0], scale_suffix=w.scale_suffix, **selection_of(w, oix))
     data = img[lay.data_start:]
     outs = sel.outputs()
     t0 = time.perf_counter()
@@ -254,9 +263,10 @@ def run_ours(args, rank, world, local):
     host = torch.empty(lay.file_bytes, dtype=torch.uint8, pin_memory=True)
     synth.build_workload_file(w, 0, out=host.numpy())
     ix = view_of(w)(stmat.Index.from_file(host.numpy()))
+    sel = selection_of(w, ix)
     plan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, workers=args.workers,
                    blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel,
-                   order=args.order)
+                   order=args.order, **sel)
     dev = torch.empty(lay.file_bytes + 256, dtype=torch.uint8, device="cuda")
     if w.whole_file_on_device:
         dev[:lay.file_bytes].copy_(host)
@@ -313,7 +323,7 @@ def run_ours(args, rank, world, local):
     if not args.no_e2e:
         eplan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, chunk_bytes=args.e2e_chunk_mb << 20,
                         blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel,
-                   order=args.order)
+                        order=args.order, **sel)
         copy = torch.cuda.Stream()
         hdata = host[lay.data_start:]
         ddata = dev[:lay.data_bytes]

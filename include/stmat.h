@@ -146,6 +146,19 @@ st_status st_view_rename(const st_index_t *parent, const char *const *from, cons
 
 /* ------------------------------------------------------------------ plan */
 
+/* A range along one dimension ("TensorFrame ... supports slicing metadata"):
+ * the output keeps indices [start, stop) of dimension `dim` and all of the
+ * others, row-major, so its shape is the tensor's with shape[dim] =
+ * stop - start.  dim < 0: the whole tensor.  0 <= dim < ndim and
+ * 0 <= start <= stop <= shape[dim], else ST_E_INVAL.  Slicing the outer
+ * dimension gives one contiguous source range; slicing an inner one gives
+ * one run per outer index (a strided gather, e.g. a row-parallel
+ * tensor-parallel shard). */
+typedef struct st_slice {
+  int32_t dim;
+  int64_t start, stop;
+} st_slice;
+
 typedef struct st_selection {
   /* Names to materialize, in output order; NULL selects every tensor of the
    * index in index order. */
@@ -163,6 +176,9 @@ typedef struct st_selection {
    * c_i bytes before it, T in total) belongs to part
    * floor(n_parts * (2 c_i + b_i) / (2 T)). */
   uint32_t part, n_parts;
+  /* Optional, n_names entries (requires names): a slice per selected name.
+   * Parts (above) weigh outputs by their sliced bytes. */
+  const st_slice *slices;
 } st_selection;
 /* A scale must be a one-element F32 tensor and may scale only an fp8 tensor
  * (ST_E_INVAL otherwise); scale tensors are consumed, not output.  Output
@@ -200,11 +216,13 @@ typedef struct st_output_info {
   st_dtype dtype;         /* output dtype */
   st_dtype src_dtype;
   int32_t ndim;
-  const int64_t *shape;
-  uint64_t numel;
+  const int64_t *shape;   /* the output's shape (sliced when a slice was given) */
+  uint64_t numel;         /* elements of the output */
   uint64_t bytes;         /* numel * itemsize(dtype) */
-  uint64_t src_begin;     /* data-section offset of the source bytes */
+  uint64_t src_begin;     /* data-section offset of the source tensor */
   const char *scale_name; /* scale tensor, or NULL */
+  int32_t slice_dim;      /* the slice, or -1 */
+  int64_t slice_start, slice_stop;
 } st_output_info;
 
 st_status st_plan_count(const st_plan_t *plan, size_t *count);
@@ -216,9 +234,12 @@ st_status st_plan_arena(const st_plan_t *plan, uint64_t align, uint64_t *offsets
  * tuning; any pointer may be NULL. */
 st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chunks, uint64_t *pieces,
                         uint32_t *kernel);
-/* Piece k as {src, dst, scale, count, output, class} (host copy). */
+/* Piece k (host copy): `rows` runs of `count` counted units; run r reads
+ * from data-section offset src + r * pitch and writes output bytes from
+ * dst + r * count * out_itemsize; scale offset (or ~0), output, class. */
 st_status st_plan_piece(const st_plan_t *plan, uint64_t k, uint64_t *src, uint64_t *dst,
-                        uint64_t *scale, uint32_t *count, uint32_t *output, uint32_t *cls);
+                        uint64_t *scale, uint32_t *count, uint32_t *output, uint32_t *cls,
+                        uint32_t *rows, uint64_t *pitch);
 /* Pieces of worker w in chunk c: [first, last). */
 st_status st_plan_worker(const st_plan_t *plan, uint32_t chunk, uint32_t w, uint64_t *first,
                          uint64_t *last);

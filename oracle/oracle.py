@@ -47,7 +47,9 @@ def lib():
             "or_out_dtype": (I, [I, I]),
             "or_convert": (I, [I, I, C.c_char_p, U64, I, C.c_float, P]),
             "or_select": (I, [P, C.POINTER(C.c_char_p), U64, C.POINTER(C.c_char_p), C.c_char_p,
-                              C.c_char_p, I, U64, U64, C.POINTER(P)]),
+                              C.c_char_p, I, U64, U64, C.POINTER(I64), C.POINTER(P)]),
+            "or_plan_numel": (U64, [P, U64]), "or_plan_ndim": (I, [P, P, U64]),
+            "or_plan_dim": (I64, [P, P, U64, I]),
             "or_plan_free": (None, [P]), "or_plan_count": (U64, [P]),
             "or_plan_name": (C.c_char_p, [P, U64]), "or_plan_entry": (U64, [P, U64]),
             "or_plan_dtype": (I, [P, U64]), "or_plan_scale": (I64, [P, U64]),
@@ -149,14 +151,21 @@ class OIndex:
         return OIndex(out.value, keep=self)
 
     def select(self, names=None, dst="BF16", scale_names=None, scale_suffix=None,
-               part=0, nparts=1):
+               part=0, nparts=1, slices=None):
+        """slices: per name None or (dim, start, stop)."""
         out = C.c_void_p()
         nm = _strs(names) if names is not None else None
         sn = _strs(scale_names) if scale_names is not None else None
         fr, to = (scale_suffix if scale_suffix else (None, None))
+        sl = None
+        if slices is not None:
+            flat = []
+            for x in slices:
+                flat += list(x) if x is not None else [-1, 0, 0]
+            sl = (C.c_int64 * max(1, len(flat)))(*flat)
         _check(lib().or_select(self._h, nm, len(names) if names is not None else 0, sn,
                                fr.encode() if fr else None, to.encode() if to else None,
-                               DTYPES.index(dst), part, nparts, C.byref(out)))
+                               DTYPES.index(dst), part, nparts, sl, C.byref(out)))
         return OPlan(out.value, self)
 
 
@@ -184,8 +193,9 @@ class OPlan:
             "entry": L.or_plan_entry(self._h, i),
             "dtype": DTYPES[L.or_plan_dtype(self._h, i)],
             "src_dtype": e["dtype"],
-            "shape": e["shape"],
-            "numel": e["numel"],
+            "shape": [L.or_plan_dim(self.index.handle, self._h, i, d)
+                      for d in range(L.or_plan_ndim(self.index.handle, self._h, i))],
+            "numel": L.or_plan_numel(self._h, i),
             "begin": e["begin"],
             "scale": None if sc < 0 else self.index.entry(sc)["name"],
             "bytes": L.or_plan_bytes(self.index.handle, self._h, i),

@@ -860,7 +860,19 @@ typedef struct {
   uint64_t entry;   /* index entry */
   int out_dtype;
   int64_t scale;    /* index entry of the f32 scale, or -1 */
+  int sdim;         /* sliced dimension, or -1 */
+  int64_t start, stop;
+  uint64_t numel;   /* elements of the output (after slicing) */
 } or_output;
+
+/* Products of the dimensions before and after `dim`. */
+static void outer_inner(const or_entry *e, int dim, uint64_t *outer, uint64_t *inner) {
+  int d;
+  *outer = 1;
+  *inner = 1;
+  for (d = 0; d < dim; d++) *outer *= (uint64_t)e->shape[d];
+  for (d = dim + 1; d < e->ndim; d++) *inner *= (uint64_t)e->shape[d];
+}
 
 typedef struct or_plan {
   or_output *o;
@@ -880,8 +892,11 @@ static int ends_with(const char *s, const char *suf) {
   return a >= b && strcmp(s + a - b, suf) == 0;
 }
 
-/* names == NULL selects every entry in index order.  scale_names (when not
-   NULL) gives each selected name its scale tensor (NULL for none).  Otherwise,
+/* names == NULL selects every entry in index order.  slices (when not NULL,
+   with names) holds three numbers per name: dim, start, stop; the output is
+   then the tensor's [start, stop) range along dim (dim < 0: the whole
+   tensor), each [0, ndim), 0 <= start <= stop <= shape[dim].  scale_names
+   (when not NULL) gives each selected name its scale tensor (NULL for none).  Otherwise,
    when both suffixes are given, an fp8 tensor "<stem><from>" is paired with
    "<stem><to>" if that tensor exists.  A scale must be a one-element F32
    tensor and may only scale an fp8 tensor.  Tensors used as scales are
@@ -889,7 +904,7 @@ static int ends_with(const char *s, const char *suf) {
    `nparts` (balanced by output bytes, contiguous in output order). */
 int or_select(const or_index *ix, const char *const *names, uint64_t n_names,
               const char *const *scale_names, const char *from, const char *to, int req,
-              uint64_t part, uint64_t nparts, or_plan **out) {
+              uint64_t part, uint64_t nparts, const int64_t *slices, or_plan **out) {
   uint64_t n = names ? n_names : ix->n, i, j, k;
   int64_t *ent = NULL, *sc = NULL;
   char *consumed = NULL;
@@ -908,6 +923,13 @@ int or_select(const or_index *ix, const char *const *names, uint64_t n_names,
     for (j = 0; j < i; j++)
       if (ent[j] == ent[i]) { st = OR_E_DUP_KEY; goto done; }
     sc[i] = -1;
+  }
+  if (slices && !names) { st = OR_E_INVAL; goto done; }
+  for (i = 0; slices && i < n; i++) {
+    const or_entry *e = &ix->e[ent[i]];
+    int64_t dim = slices[3 * i], a = slices[3 * i + 1], b = slices[3 * i + 2];
+    if (dim < 0) continue;
+    if (dim >= e->ndim || a < 0 || a > b || b > e->shape[dim]) { st = OR_E_INVAL; goto done; }
   }
   for (i = 0; i < n; i++) {
     const or_entry *e = &ix->e[ent[i]];
@@ -946,6 +968,17 @@ int or_select(const or_index *ix, const char *const *names, uint64_t n_names,
     p->o[p->n].entry = (uint64_t)ent[i];
     p->o[p->n].out_dtype = od;
     p->o[p->n].scale = sc[i];
+    p->o[p->n].sdim = -1;
+    p->o[p->n].numel = e->numel;
+    if (slices && slices[3 * i] >= 0) {
+      uint64_t outer, inner;
+      int dim = (int)slices[3 * i];
+      outer_inner(e, dim, &outer, &inner);
+      p->o[p->n].sdim = dim;
+      p->o[p->n].start = slices[3 * i + 1];
+      p->o[p->n].stop = slices[3 * i + 2];
+      p->o[p->n].numel = outer * (uint64_t)(slices[3 * i + 2] - slices[3 * i + 1]) * inner;
+    }
     p->n++;
   }
   if (nparts > 1) {
@@ -953,9 +986,9 @@ int or_select(const or_index *ix, const char *const *names, uint64_t n_names,
        floor(nparts * (c_i + b_i / 2) / T), computed as
        floor(nparts * (2 c_i + b_i) / (2 T)); with T == 0 all go to part 0. */
     unsigned __int128 T = 0, c = 0;
-    for (i = 0; i < p->n; i++) T += (unsigned __int128)ix->e[p->o[i].entry].numel * kSize[p->o[i].out_dtype];
+    for (i = 0; i < p->n; i++) T += (unsigned __int128)p->o[i].numel * kSize[p->o[i].out_dtype];
     for (i = 0, k = 0; i < p->n; i++) {
-      unsigned __int128 b = (unsigned __int128)ix->e[p->o[i].entry].numel * kSize[p->o[i].out_dtype];
+      unsigned __int128 b = (unsigned __int128)p->o[i].numel * kSize[p->o[i].out_dtype];
       uint64_t owner = 0;
       if (T > 0) {
         unsigned __int128 q = ((2 * c + b) * nparts) / (2 * T);
@@ -983,9 +1016,53 @@ uint64_t or_plan_entry(const or_plan *p, uint64_t i) { return p->o[i].entry; }
 int or_plan_dtype(const or_plan *p, uint64_t i) { return p->o[i].out_dtype; }
 int64_t or_plan_scale(const or_plan *p, uint64_t i) { return p->o[i].scale; }
 
+/* Elements and shape of output i (the sliced shape when sliced). */
+uint64_t or_plan_numel(const or_plan *p, uint64_t i) { return p->o[i].numel; }
+int or_plan_ndim(const or_index *ix, const or_plan *p, uint64_t i) { return ix->e[p->o[i].entry].ndim; }
+int64_t or_plan_dim(const or_index *ix, const or_plan *p, uint64_t i, int d) {
+  const or_output *o = &p->o[i];
+  if (d == o->sdim) return o->stop - o->start;
+  return ix->e[o->entry].shape[d];
+}
+
 /* Bytes of output i. */
 uint64_t or_plan_bytes(const or_index *ix, const or_plan *p, uint64_t i) {
-  return ix->e[p->o[i].entry].numel * (uint64_t)kSize[p->o[i].out_dtype];
+  (void)ix;
+  return p->o[i].numel * (uint64_t)kSize[p->o[i].out_dtype];
+}
+
+/* Converts output elements [first, first + count) of output o (source
+   element index of output element e: the row e / run of the slice, then the
+   column e % run, run = (stop - start) * inner elements per row). */
+static int convert_window(const or_index *ix, const or_output *o, const uint8_t *data, uint64_t first,
+                          uint64_t count, uint8_t *dst) {
+  const or_entry *e = &ix->e[o->entry];
+  const int si = kSize[e->dtype], so = kSize[o->out_dtype];
+  float scale = 1.0f;
+  uint64_t done = 0;
+  if (o->scale >= 0) {
+    const or_entry *s = &ix->e[o->scale];
+    uint32_t u = (uint32_t)load_le(data + s->begin, 4);
+    memcpy(&scale, &u, 4);
+  }
+  if (o->sdim < 0)
+    return or_convert(e->dtype, o->out_dtype, data + e->begin + first * (uint64_t)si, count, o->scale >= 0, scale,
+                      dst);
+  {
+    uint64_t outer, inner, run, D = (uint64_t)e->shape[o->sdim];
+    outer_inner(e, o->sdim, &outer, &inner);
+    run = (uint64_t)(o->stop - o->start) * inner;
+    while (done < count) {
+      uint64_t oe = first + done, row = oe / run, col = oe % run;
+      uint64_t k = run - col < count - done ? run - col : count - done;
+      uint64_t src_elem = (row * D + (uint64_t)o->start) * inner + col;
+      int st = or_convert(e->dtype, o->out_dtype, data + e->begin + src_elem * si, k, o->scale >= 0, scale,
+                          dst + done * so);
+      if (st != OR_OK) return st;
+      done += k;
+    }
+  }
+  return OR_OK;
 }
 
 /* Materializes output i from the data section `data` (data_bytes long) into
@@ -993,29 +1070,14 @@ uint64_t or_plan_bytes(const or_index *ix, const or_plan *p, uint64_t i) {
 int or_materialize(const or_index *ix, const or_plan *p, uint64_t i, const uint8_t *data,
                    uint64_t data_bytes, uint8_t *dst) {
   const or_output *o = &p->o[i];
-  const or_entry *e = &ix->e[o->entry];
-  float scale = 1.0f;
-  if (e->end > data_bytes) return OR_E_OFFSETS;
-  if (o->scale >= 0) {
-    const or_entry *s = &ix->e[o->scale];
-    uint32_t u = (uint32_t)load_le(data + s->begin, 4);
-    memcpy(&scale, &u, 4);
-  }
-  return or_convert(e->dtype, o->out_dtype, data + e->begin, e->numel, o->scale >= 0, scale, dst);
+  if (ix->e[o->entry].end > data_bytes) return OR_E_OFFSETS;
+  return convert_window(ix, o, data, 0, o->numel, dst);
 }
 
 /* Materializes a window [first, first + count) of output i's elements. */
 int or_materialize_range(const or_index *ix, const or_plan *p, uint64_t i, const uint8_t *data,
                          uint64_t first, uint64_t count, uint8_t *dst) {
   const or_output *o = &p->o[i];
-  const or_entry *e = &ix->e[o->entry];
-  float scale = 1.0f;
-  if (first > e->numel || count > e->numel - first) return OR_E_INVAL;
-  if (o->scale >= 0) {
-    const or_entry *s = &ix->e[o->scale];
-    uint32_t u = (uint32_t)load_le(data + s->begin, 4);
-    memcpy(&scale, &u, 4);
-  }
-  return or_convert(e->dtype, o->out_dtype, data + e->begin + first * (uint64_t)kSize[e->dtype], count,
-                    o->scale >= 0, scale, dst);
+  if (first > o->numel || count > o->numel - first) return OR_E_INVAL;
+  return convert_window(ix, o, data, first, count, dst);
 }

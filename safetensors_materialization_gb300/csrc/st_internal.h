@@ -33,15 +33,20 @@ enum Cls : uint32_t {
   CLS_COUNT
 };
 
-// One contiguous element range of one output: the unit a warp processes.
+// `rows` runs of `count` elements of one output: the unit a warp processes.
+// Run r reads from data + src + r * pitch and writes to the output at
+// dst + r * count * out_itemsize (one run unless an inner dimension is sliced).
 struct alignas(16) Piece {
-  uint64_t src;      // data-section byte offset of the range's first element
+  uint64_t src;      // data-section byte offset of the first run's first element
   uint64_t dst;      // byte offset of that element inside its output buffer
   uint64_t scale;    // data-section byte offset of the binary32 scale, or kNoScale
-  uint32_t count;    // elements (bytes for CLS_COPY)
+  uint32_t count;    // elements per run (bytes for CLS_COPY)
   uint32_t out_cls;  // output index << kClsBits | class
+  uint32_t rows;     // runs
+  uint32_t pad;
+  uint64_t pitch;    // source bytes between runs
 };
-static_assert(sizeof(Piece) == 32, "piece layout");
+static_assert(sizeof(Piece) == 48, "piece layout");
 
 constexpr uint64_t kNoScale = ~0ull;
 constexpr uint32_t kClsBits = 5;

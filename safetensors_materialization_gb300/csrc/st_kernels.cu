@@ -398,13 +398,32 @@ __device__ __forceinline__ Piece load_piece(const Piece *p) {
   const uint4 *q = reinterpret_cast<const uint4 *>(p);
   const uint4 x = ld16(reinterpret_cast<const uint8_t *>(q));
   const uint4 y = ld16(reinterpret_cast<const uint8_t *>(q + 1));
+  const uint4 z = ld16(reinterpret_cast<const uint8_t *>(q + 2));
   Piece pc;
   pc.src = (static_cast<uint64_t>(x.y) << 32) | x.x;
   pc.dst = (static_cast<uint64_t>(x.w) << 32) | x.z;
   pc.scale = (static_cast<uint64_t>(y.y) << 32) | y.x;
   pc.count = y.z;
   pc.out_cls = y.w;
+  pc.rows = z.x;
+  pc.pad = z.y;
+  pc.pitch = (static_cast<uint64_t>(z.w) << 32) | z.z;
   return pc;
+}
+
+// The runs of a piece, one after the other (one run unless an inner
+// dimension of the output is sliced).
+template <class Cfg, class CV>
+__device__ __forceinline__ void run_rows(const LaunchArgs &a, const volatile Piece *sp, uint8_t *dst, float scale,
+                                         uint32_t lane) {
+  // The piece's fields are re-read from its staged copy in shared memory for
+  // every run (volatile), so no descriptor state stays live in registers
+  // across run_piece.
+  for (uint32_t r = 0; r < sp->rows; ++r) {
+    const uint64_t cnt = sp->count;
+    run_piece<Cfg, CV>(a.data, a.data_bytes, a.data + sp->src + r * sp->pitch, dst + r * cnt * CV::SO, cnt, scale,
+                       lane);
+  }
 }
 
 // Per-warp staging of up to 32 pieces: descriptor, destination and scale.
@@ -442,8 +461,7 @@ __device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
     }
     __syncwarp();
     for (uint32_t i = 0; i < n; ++i) {
-      const Piece pc = st.piece[i];
-      const uint32_t cls = pc.out_cls & ((1u << kClsBits) - 1);
+      const uint32_t cls = st.piece[i].out_cls & ((1u << kClsBits) - 1);
       uint8_t *dst = st.dst[i];
       const float scale = st.scale[i];
       const int so = cls_out_size(cls);
@@ -451,23 +469,21 @@ __device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
         if (lane == 0) atomicOr(a.err, kErrBadDst);
         continue;
       }
-      dst += pc.dst;
-      const uint8_t *src = a.data + pc.src;
-      const uint64_t cnt = pc.count;
+      dst += st.piece[i].dst;
       switch (cls) {
-        case CLS_COPY: run_piece<Cfg, CopyBytes>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_F32_BF16: run_piece<Cfg, Conv<S_F32, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_F32_F16: run_piece<Cfg, Conv<S_F32, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_F16_BF16: run_piece<Cfg, Conv<S_F16, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_F16_F32: run_piece<Cfg, Conv<S_F16, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_BF16_F16: run_piece<Cfg, Conv<S_BF16, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_BF16_F32: run_piece<Cfg, Conv<S_BF16, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E4M3_BF16: run_piece<Cfg, Conv<S_E4M3, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E4M3_F16: run_piece<Cfg, Conv<S_E4M3, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E4M3_F32: run_piece<Cfg, Conv<S_E4M3, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E5M2_BF16: run_piece<Cfg, Conv<S_E5M2, D_BF16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E5M2_F16: run_piece<Cfg, Conv<S_E5M2, D_F16>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
-        case CLS_E5M2_F32: run_piece<Cfg, Conv<S_E5M2, D_F32>>(a.data, a.data_bytes, src, dst, cnt, scale, lane); break;
+        case CLS_COPY: run_rows<Cfg, CopyBytes>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_F32_BF16: run_rows<Cfg, Conv<S_F32, D_BF16>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_F32_F16: run_rows<Cfg, Conv<S_F32, D_F16>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_F16_BF16: run_rows<Cfg, Conv<S_F16, D_BF16>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_F16_F32: run_rows<Cfg, Conv<S_F16, D_F32>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_BF16_F16: run_rows<Cfg, Conv<S_BF16, D_F16>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_BF16_F32: run_rows<Cfg, Conv<S_BF16, D_F32>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_E4M3_BF16: run_rows<Cfg, Conv<S_E4M3, D_BF16>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_E4M3_F16: run_rows<Cfg, Conv<S_E4M3, D_F16>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_E4M3_F32: run_rows<Cfg, Conv<S_E4M3, D_F32>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_E5M2_BF16: run_rows<Cfg, Conv<S_E5M2, D_BF16>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_E5M2_F16: run_rows<Cfg, Conv<S_E5M2, D_F16>>(a, &st.piece[i], dst, scale, lane); break;
+        case CLS_E5M2_F32: run_rows<Cfg, Conv<S_E5M2, D_F32>>(a, &st.piece[i], dst, scale, lane); break;
         default:
           if (lane == 0) atomicOr(a.err, kErrBadDst);
       }

@@ -83,7 +83,19 @@ struct Output {
   int out_dtype;
   int64_t scale = -1;  // core tensor of the scale
   uint32_t cls;
+  uint64_t numel;      // output elements (after slicing)
   uint64_t units;      // counted units (elements, or bytes for copies)
+  std::vector<int64_t> shape;  // output shape
+  int32_t sdim = -1;   // slice
+  int64_t start = 0, stop = 0;
+  // Source geometry in counted units: `runs` runs of `run` units; run r
+  // starts at data-section byte src0 + r * pitch.  One run unless an inner
+  // dimension is sliced.
+  uint64_t runs = 1, run = 0, src0 = 0, pitch = 0;
+  // Data-section byte of output unit u.
+  uint64_t unit_src(uint64_t u) const {
+    return runs == 1 ? src0 + u * cls_in_size(cls) : src0 + (u / run) * pitch + (u % run) * cls_in_size(cls);
+  }
 };
 
 }  // namespace stmat
@@ -149,6 +161,17 @@ st_status select_outputs(const IndexData &ix, const st_selection *sel, int req, 
     if (taken[pos[i]]) return set_error(ST_E_DUP_KEY, "\"%s\" selected twice", ix.names[pos[i]]);
     taken[pos[i]] = 1;
   }
+  const st_slice *slices = sel ? sel->slices : nullptr;
+  if (slices && all) return set_error(ST_E_INVAL, "slices need names");
+  for (size_t i = 0; slices && i < n; ++i) {
+    const Tensor &t = core.tensors[ix.ent[pos[i]]];
+    const st_slice &sl = slices[i];
+    if (sl.dim < 0) continue;
+    if (sl.dim >= static_cast<int32_t>(t.shape.size()) || sl.start < 0 || sl.start > sl.stop ||
+        sl.stop > t.shape[sl.dim])
+      return set_error(ST_E_INVAL, "slice (dim %d, %lld..%lld) does not fit \"%s\"", sl.dim,
+                       static_cast<long long>(sl.start), static_cast<long long>(sl.stop), ix.names[pos[i]]);
+  }
   // Scale pairing.
   std::vector<int64_t> scale(n, -1);  // position of the scale in the view
   std::vector<char> consumed(ix.ent.size(), 0);
@@ -199,17 +222,39 @@ st_status select_outputs(const IndexData &ix, const st_selection *sel, int req, 
     int c = class_of(t.dtype, od, o.scale >= 0);
     if (c < 0) return set_error(ST_E_UNSUPPORTED_CAST, "no conversion for \"%s\"", o.name.c_str());
     o.cls = static_cast<uint32_t>(c);
-    o.units = c == CLS_COPY ? t.numel * dtype_size(t.dtype) : t.numel;
+    const uint64_t isz = dtype_size(t.dtype), upe = c == CLS_COPY ? isz : 1;  // units per element
+    o.shape = t.shape;
+    o.numel = t.numel;
+    o.src0 = t.begin;
+    if (slices && slices[i].dim >= 0) {
+      const st_slice &sl = slices[i];
+      uint64_t outer = 1, inner = 1;
+      for (int32_t d = 0; d < sl.dim; ++d) outer *= static_cast<uint64_t>(t.shape[d]);
+      for (size_t d = sl.dim + 1; d < t.shape.size(); ++d) inner *= static_cast<uint64_t>(t.shape[d]);
+      const uint64_t D = static_cast<uint64_t>(t.shape[sl.dim]), w = static_cast<uint64_t>(sl.stop - sl.start);
+      o.sdim = sl.dim;
+      o.start = sl.start;
+      o.stop = sl.stop;
+      o.shape[sl.dim] = sl.stop - sl.start;
+      o.numel = outer * w * inner;
+      o.src0 = t.begin + static_cast<uint64_t>(sl.start) * inner * isz;
+      if (outer > 1 && w < D && w * inner > 0) {
+        o.runs = outer;
+        o.run = w * inner * upe;
+        o.pitch = D * inner * isz;
+      }
+    }
+    o.units = o.numel * upe;
+    if (o.runs == 1) o.run = o.units;
     outs->push_back(std::move(o));
   }
   if (n_parts > 1) {
     // Output i goes to part floor(n_parts * (2 c_i + b_i) / (2 T)).
     unsigned __int128 T = 0, c = 0;
-    for (const Output &o : *outs)
-      T += static_cast<unsigned __int128>(core.tensors[o.entry].numel) * dtype_size(o.out_dtype);
+    for (const Output &o : *outs) T += static_cast<unsigned __int128>(o.numel) * dtype_size(o.out_dtype);
     std::vector<Output> kept;
     for (Output &o : *outs) {
-      unsigned __int128 b = static_cast<unsigned __int128>(core.tensors[o.entry].numel) * dtype_size(o.out_dtype);
+      unsigned __int128 b = static_cast<unsigned __int128>(o.numel) * dtype_size(o.out_dtype);
       uint64_t owner = 0;
       if (T > 0) {
         unsigned __int128 q = ((2 * c + b) * n_parts) / (2 * T);
@@ -241,20 +286,52 @@ void cut_units(const st_plan_s &p, const std::vector<Segment> &segs, uint64_t n,
   const double share = (total + double(n - 1) * kPieceCost) / n;
   uint64_t w = 0;
   double used = 0;  // cost assigned so far (units < w and unit w's part)
+  // Output units [a, b) as pieces: one contiguous piece per kMaxPieceUnits,
+  // or, across the runs of a sliced output, a partial first run, one
+  // multi-row piece for the whole runs, and a partial last run.
   auto emit = [&](const Segment &s, uint64_t a, uint64_t b) {
     const Output &o = p.outs[s.out];
-    const Tensor &t = core.tensors[o.entry];
-    const uint64_t si = cls_in_size(o.cls), so = cls_out_size(o.cls);
-    for (uint64_t x = a; x < b; x += kMaxPieceUnits) {
-      uint64_t y = std::min(b, x + kMaxPieceUnits);
+    const uint64_t so = cls_out_size(o.cls);
+    const uint64_t scale = o.scale >= 0 ? core.tensors[o.scale].begin : kNoScale;
+    auto push = [&](uint64_t u, uint64_t count, uint64_t rows) {
       Piece pc;
-      pc.src = t.begin + x * si;
-      pc.dst = x * so;
-      pc.scale = o.scale >= 0 ? core.tensors[o.scale].begin : kNoScale;
-      pc.count = static_cast<uint32_t>(y - x);
+      pc.src = o.unit_src(u);
+      pc.dst = u * so;
+      pc.scale = scale;
+      pc.count = static_cast<uint32_t>(count);
       pc.out_cls = (s.out << kClsBits) | o.cls;
+      pc.rows = static_cast<uint32_t>(rows);
+      pc.pad = 0;
+      pc.pitch = o.pitch;
       units->push_back(pc);
+    };
+    auto contiguous = [&](uint64_t x, uint64_t y) {  // [x, y) inside one run
+      for (; x < y; x += kMaxPieceUnits) push(x, std::min(y, x + kMaxPieceUnits) - x, 1);
+    };
+    if (o.runs == 1) {
+      contiguous(a, b);
+      return;
     }
+    const uint64_t L = o.run;
+    if (a % L) {
+      const uint64_t e = std::min(b, (a / L + 1) * L);
+      contiguous(a, e);
+      a = e;
+    }
+    if (b - a >= L && L <= kMaxPieceUnits) {
+      uint64_t rows = (b - a) / L;
+      while (rows) {
+        const uint64_t k = std::min<uint64_t>(rows, 0xFFFFFFFFu);
+        push(a, L, k);
+        a += k * L;
+        rows -= k;
+      }
+    }
+    while (b - a >= L) {  // runs too long for one piece each
+      contiguous(a, a + L);
+      a += L;
+    }
+    if (a < b) contiguous(a, b);
   };
   auto next_unit = [&]() {
     ++w;
@@ -263,7 +340,11 @@ void cut_units(const st_plan_s &p, const std::vector<Segment> &segs, uint64_t n,
   for (const Segment &s : segs) {
     const Output &o = p.outs[s.out];
     const double per = cls_in_size(o.cls) + cls_out_size(o.cls);
-    const uint64_t granule = kSplitBytes / cls_in_size(o.cls);
+    // Cuts fall on 2 KiB of source, or between runs when the runs of a sliced
+    // output are short enough to keep whole.
+    const uint64_t granule = o.runs > 1 && double(o.run) * per <= double(p.unit_bytes)
+                                 ? o.run
+                                 : kSplitBytes / cls_in_size(o.cls);
     uint64_t u = s.u0;
     while (u < s.u1) {
       double rest = kPieceCost + double(s.u1 - u) * per;
@@ -303,23 +384,35 @@ void build_pieces(st_plan_s *p) {
   std::vector<uint32_t> order(p->outs.size());
   for (uint32_t i = 0; i < order.size(); ++i) order[i] = i;
   std::stable_sort(order.begin(), order.end(), [&](uint32_t a, uint32_t b) {
-    return core.tensors[p->outs[a].entry].begin < core.tensors[p->outs[b].entry].begin;
+    return p->outs[a].src0 < p->outs[b].src0;
   });
   for (uint32_t oi : order) {
     const Output &o = p->outs[oi];
     if (o.units == 0) continue;
-    const Tensor &t = core.tensors[o.entry];
     const uint64_t si = cls_in_size(o.cls);
     if (!C) {
       per_chunk[0].push_back({oi, 0, o.units});
       continue;
     }
     uint64_t scale_chunk = o.scale >= 0 ? (core.tensors[o.scale].end - 1) / C : 0;
+    if (o.runs > 1) {
+      // Whole runs go to the chunk holding their last byte.
+      uint64_t r0 = 0, k0 = 0;
+      for (uint64_t r = 0; r <= o.runs; ++r) {
+        const uint64_t k = r < o.runs ? std::max(scale_chunk, (o.src0 + r * o.pitch + o.run * si - 1) / C) : ~0ull;
+        if (r > 0 && k != k0) {
+          per_chunk[k0].push_back({oi, r0 * o.run, r * o.run});
+          r0 = r;
+        }
+        k0 = k;
+      }
+      continue;
+    }
     uint64_t u = 0;
-    for (uint64_t k = t.begin / C; u < o.units; ++k) {
+    for (uint64_t k = o.src0 / C; u < o.units; ++k) {
       // units whose last byte lies before the end of chunk k
       uint64_t end = (k + 1) * C;
-      uint64_t ue = end <= t.begin ? 0 : std::min<uint64_t>(o.units, (end - t.begin) / si);
+      uint64_t ue = end <= o.src0 ? 0 : std::min<uint64_t>(o.units, (end - o.src0) / si);
       if (ue > u) {
         per_chunk[std::max<uint64_t>(k, scale_chunk)].push_back({oi, u, ue});
         u = ue;
@@ -342,8 +435,7 @@ void build_pieces(st_plan_s *p) {
     std::stable_sort(segs.begin(), segs.end(), [&](const Segment &a, const Segment &b) {
       const Output &oa = p->outs[a.out], &ob = p->outs[b.out];
       if (by_class && oa.cls != ob.cls) return oa.cls < ob.cls;
-      return core.tensors[oa.entry].begin + a.u0 * cls_in_size(oa.cls) <
-             core.tensors[ob.entry].begin + b.u0 * cls_in_size(ob.cls);
+      return oa.unit_src(a.u0) < ob.unit_src(b.u0);
     });
     double total = 0;
     for (const Segment &s : segs) {
@@ -457,12 +549,15 @@ st_status st_plan_output(const st_plan_t *p, size_t i, st_output_info *info) {
   info->name = o.name.c_str();
   info->dtype = static_cast<st_dtype>(o.out_dtype);
   info->src_dtype = static_cast<st_dtype>(t.dtype);
-  info->ndim = static_cast<int32_t>(t.shape.size());
-  info->shape = t.shape.data();
-  info->numel = t.numel;
-  info->bytes = t.numel * dtype_size(o.out_dtype);
+  info->ndim = static_cast<int32_t>(o.shape.size());
+  info->shape = o.shape.data();
+  info->numel = o.numel;
+  info->bytes = o.numel * dtype_size(o.out_dtype);
   info->src_begin = t.begin;
   info->scale_name = o.scale >= 0 ? p->index->core->tensors[o.scale].name.c_str() : nullptr;
+  info->slice_dim = o.sdim;
+  info->slice_start = o.start;
+  info->slice_stop = o.stop;
   return ST_OK;
 }
 
@@ -474,7 +569,7 @@ st_status st_plan_arena(const st_plan_t *p, uint64_t align, uint64_t *offsets, u
   for (size_t i = 0; i < p->outs.size(); ++i) {
     at = (at + align - 1) & ~(align - 1);
     offsets[i] = at;
-    at += p->index->core->tensors[p->outs[i].entry].numel * dtype_size(p->outs[i].out_dtype);
+    at += p->outs[i].numel * dtype_size(p->outs[i].out_dtype);
   }
   *total = at;
   return ST_OK;
@@ -491,8 +586,9 @@ st_status st_plan_stats(const st_plan_t *p, uint32_t *workers, uint32_t *chunks,
 }
 
 st_status st_plan_piece(const st_plan_t *p, uint64_t k, uint64_t *src, uint64_t *dst, uint64_t *scale,
-                        uint32_t *count, uint32_t *output, uint32_t *cls) {
-  if (!p || !src || !dst || !scale || !count || !output || !cls) return set_error(ST_E_INVAL, "NULL argument");
+                        uint32_t *count, uint32_t *output, uint32_t *cls, uint32_t *rows, uint64_t *pitch) {
+  if (!p || !src || !dst || !scale || !count || !output || !cls || !rows || !pitch)
+    return set_error(ST_E_INVAL, "NULL argument");
   if (k >= p->pieces.size()) return set_error(ST_E_INVAL, "piece %llu out of range", (unsigned long long)k);
   const Piece &pc = p->pieces[k];
   *src = pc.src;
@@ -501,6 +597,8 @@ st_status st_plan_piece(const st_plan_t *p, uint64_t k, uint64_t *src, uint64_t 
   *count = pc.count;
   *output = pc.out_cls >> kClsBits;
   *cls = pc.out_cls & ((1u << kClsBits) - 1);
+  *rows = pc.rows;
+  *pitch = pc.pitch;
   return ST_OK;
 }
 

@@ -51,13 +51,19 @@ class TensorInfo(C.Structure):
 class OutputInfo(C.Structure):
     _fields_ = [("name", C.c_char_p), ("dtype", C.c_int), ("src_dtype", C.c_int), ("ndim", C.c_int32),
                 ("shape", C.POINTER(C.c_int64)), ("numel", C.c_uint64), ("bytes", C.c_uint64),
-                ("src_begin", C.c_uint64), ("scale_name", C.c_char_p)]
+                ("src_begin", C.c_uint64), ("scale_name", C.c_char_p), ("slice_dim", C.c_int32),
+                ("slice_start", C.c_int64), ("slice_stop", C.c_int64)]
+
+
+class Slice(C.Structure):
+    _fields_ = [("dim", C.c_int32), ("start", C.c_int64), ("stop", C.c_int64)]
 
 
 class Selection(C.Structure):
     _fields_ = [("names", C.POINTER(C.c_char_p)), ("n_names", C.c_size_t),
                 ("scale_names", C.POINTER(C.c_char_p)), ("scale_suffix_from", C.c_char_p),
-                ("scale_suffix_to", C.c_char_p), ("part", C.c_uint32), ("n_parts", C.c_uint32)]
+                ("scale_suffix_to", C.c_char_p), ("part", C.c_uint32), ("n_parts", C.c_uint32),
+                ("slices", C.POINTER(Slice))]
 
 
 class PlanOptions(C.Structure):
@@ -99,7 +105,7 @@ def lib():
             "st_plan_arena": [P, U64, C.POINTER(U64), C.POINTER(U64)],
             "st_plan_stats": [P, C.POINTER(U32), C.POINTER(U32), C.POINTER(U64), C.POINTER(U32)],
             "st_plan_piece": [P, U64, C.POINTER(U64), C.POINTER(U64), C.POINTER(U64), C.POINTER(U32),
-                              C.POINTER(U32), C.POINTER(U32)],
+                              C.POINTER(U32), C.POINTER(U32), C.POINTER(U32), C.POINTER(U64)],
             "st_plan_worker": [P, U32, U32, C.POINTER(U64), C.POINTER(U64)],
             "st_materialize": [P, P, P, P, P],
             "st_materialize_noalloc": [P, P, P, P, P],
@@ -254,7 +260,8 @@ class Index:
         return Index(out.value)
 
     def plan(self, dst="BF16", names=None, scale_names=None, scale_suffix=None, part=0, n_parts=0,
-             workers=0, chunk_bytes=0, host_only=False, blocks_per_sm=0, unit_bytes=0, kernel=0, order=0):
+             workers=0, chunk_bytes=0, host_only=False, blocks_per_sm=0, unit_bytes=0, kernel=0, order=0,
+             slices=None):
         """st_plan: outputs and device work for a selection."""
         sel = Selection()
         keep = []
@@ -269,6 +276,12 @@ class Index:
         if scale_suffix:
             sel.scale_suffix_from, sel.scale_suffix_to = scale_suffix[0].encode(), scale_suffix[1].encode()
         sel.part, sel.n_parts = part, n_parts
+        if slices is not None:
+            arr = (Slice * max(1, len(slices)))()
+            for i, x in enumerate(slices):
+                arr[i] = Slice(*(x if x is not None else (-1, 0, 0)))
+            keep.append(arr)
+            sel.slices = C.cast(arr, C.POINTER(Slice))
         opts = PlanOptions(workers, chunk_bytes, 1 if host_only else 0, blocks_per_sm, unit_bytes, kernel, order)
         out = C.c_void_p()
         _check(lib().st_plan(self._h, C.byref(sel), DTYPES.index(dst), C.byref(opts), C.byref(out)))
@@ -301,7 +314,8 @@ class Plan:
         _check(lib().st_plan_output(self._h, i, C.byref(o)))
         return {"name": o.name.decode(), "dtype": DTYPES[o.dtype], "src_dtype": DTYPES[o.src_dtype],
                 "shape": [o.shape[d] for d in range(o.ndim)], "numel": o.numel, "bytes": o.bytes,
-                "begin": o.src_begin, "scale": o.scale_name.decode() if o.scale_name else None}
+                "begin": o.src_begin, "scale": o.scale_name.decode() if o.scale_name else None,
+                "slice": None if o.slice_dim < 0 else (o.slice_dim, o.slice_start, o.slice_stop)}
 
     def outputs(self):
         return [self.output(i) for i in range(len(self))]
@@ -320,9 +334,10 @@ class Plan:
                 "kernel": {1: "stream", 2: "latency"}.get(k.value, str(k.value))}
 
     def piece(self, k):
-        v = [C.c_uint64(), C.c_uint64(), C.c_uint64(), C.c_uint32(), C.c_uint32(), C.c_uint32()]
+        v = [C.c_uint64(), C.c_uint64(), C.c_uint64(), C.c_uint32(), C.c_uint32(), C.c_uint32(), C.c_uint32(),
+             C.c_uint64()]
         _check(lib().st_plan_piece(self._h, k, *[C.byref(x) for x in v]))
-        return dict(zip(["src", "dst", "scale", "count", "output", "cls"], [x.value for x in v]))
+        return dict(zip(["src", "dst", "scale", "count", "output", "cls", "rows", "pitch"], [x.value for x in v]))
 
     def worker(self, chunk, w):
         a, b = C.c_uint64(), C.c_uint64()

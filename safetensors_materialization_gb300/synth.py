@@ -174,6 +174,7 @@ class Workload:
     rename: list = field(default_factory=list)   # rename view rules
     scale_suffix: tuple | None = None            # (weight suffix, scale suffix)
     whole_file_on_device: bool = False           # stage the header too (keeps its misalignment)
+    slices: dict | None = None                   # name -> (dim, start, stop) for sliced loads
 
 
 def tiny(seed=0):
@@ -300,11 +301,40 @@ def stress(seed=4, n=100_000):
     return Workload("stress_100k_misaligned", [lay], [seed], ["BF16"], whole_file_on_device=True)
 
 
+def tp_slices(entries, tp, rank):
+    """Megatron-style tensor-parallel shard `rank` of `tp` for Llama names:
+    column-parallel projections (q/k/v, gate/up) and the vocab-parallel
+    embedding and head split dim 0; row-parallel ones (o, down) split dim 1
+    (a strided gather); norms stay whole."""
+    out = {}
+    for e in entries:
+        n = e.name
+        if any(k in n for k in ("q_proj", "k_proj", "v_proj", "gate_proj", "up_proj", "embed_tokens", "lm_head")):
+            d = 0
+        elif any(k in n for k in ("o_proj", "down_proj")):
+            d = 1
+        else:
+            continue
+        size = e.shape[d] // tp
+        out[n] = (d, rank * size, (rank + 1) * size)
+    return out
+
+
+def llm8b_tp4(seed=3):
+    """Shard file 0 of the 8B LLM checkpoint loaded as tensor-parallel rank 0
+    of 4: BF16 copies of the rank's slices."""
+    w = llm8b(seed)
+    lay = w.files[0]
+    return Workload("llm8b_shard0_tp4_rank0", [lay], [w.seeds[0]], ["BF16"],
+                    slices=tp_slices(lay.entries, 4, 0))
+
+
 WORKLOADS = {"tiny": tiny, "unet": unet, "scaled_fp8": scaled_fp8, "llm8b": llm8b, "stress": stress,
              # a 5-block slice of the scaled-fp8 checkpoint (1.04 GB source), for profiling
              "scaled_fp8_5blk": lambda: scaled_fp8(blocks=5),
              # a UNet with 8 of the 38 1280-channel resblocks (0.83 GB source), for profiling
-             "unet_small": lambda: unet(n1280=8)}
+             "unet_small": lambda: unet(n1280=8),
+             "llm8b_tp4": llm8b_tp4}
 
 
 def build_workload_file(wl: Workload, k: int, out: np.ndarray | None = None):

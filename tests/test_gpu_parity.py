@@ -391,3 +391,81 @@ def test_empty_cases(stmat):
     img = image_of(ents, b"\x00\x3c")
     plan, outs, _ = run(stmat, img, dst="F32")
     assert outs.raw(1).cpu().numpy().view(np.float32)[0] == 1.0
+
+
+# ---------------------------------------------------------------- slicing
+
+def sliced_image(seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shapes = [[64, 300], [9, 40, 33], [3, 5, 7, 11], [512, 96], [2, 7000], [12], [33, 17]]
+    dts = ["F32", "F16", "F8_E4M3", "BF16", "I64", "F8_E5M2", "BOOL"]
+    isz = {"F32": 4, "F16": 2, "BF16": 2, "F8_E4M3": 1, "F8_E5M2": 1, "I64": 8, "BOOL": 1}
+    ents, parts, off = {}, [], 0
+    for i, (shp, dt) in enumerate(zip(shapes, dts)):
+        n = int(np.prod(shp))
+        raw = rng.integers(0, 256, size=n * isz[dt], dtype=np.uint8)
+        if dt == "BOOL":
+            raw &= 1
+        ents[f"s{i}"] = {"dtype": dt, "shape": shp, "data_offsets": [off, off + raw.size]}
+        parts.append(raw.tobytes())
+        off += raw.size
+    return image_of(ents, b"".join(parts), pad=5), shapes, rng
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_sliced_outputs(stmat, oracle, kernel):
+    """Slices on every dimension (contiguous and strided runs) at misaligned
+    sources, into aligned and packed outputs."""
+    img, shapes, rng = sliced_image(21 + kernel)
+    names = [f"s{i}" for i in range(len(shapes))]
+    ix = stmat.Index.from_file(img)
+    hlen = ix.sizes()[0]
+    oix = oracle.parse(img)
+    data = img[8 + hlen:]
+    for trial in range(8):
+        slices = []
+        for shp in shapes:
+            d = int(rng.integers(0, len(shp)))
+            a = int(rng.integers(0, shp[d]))
+            slices.append((d, a, int(rng.integers(a, shp[d] + 1))))
+        dst = ["BF16", "F16", "F32", "KEEP"][trial % 4]
+        sel = oix.select(dst=dst, names=names, slices=slices)
+        want = [sel.materialize(i, data) for i in range(len(sel))]
+        plan = ix.plan(dst=dst, names=names, slices=slices, kernel=kernel, unit_bytes=[2048, 32768][trial % 2])
+        buf, data_ptr = to_device(img, trial % 16, True, 8 + hlen)
+        outs = Packed(plan) if trial % 3 == 0 else stmat.Outputs(plan)
+        plan.materialize(data_ptr, outs.ptrs)
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        assert [o["shape"] for o in plan.outputs()] == [o["shape"] for o in sel.outputs()]
+        assert_same(plan, outs, sel, want)
+
+
+def test_tensor_parallel_shard_load(stmat, oracle):
+    """Rank 0 of 4 tensor-parallel ranks of an LLM shard file at full size:
+    every sliced output equals torch's slice of the source tensor (a byte
+    copy), and windows equal the oracle."""
+    from safetensors_materialization_gb300 import synth
+    w = synth.llm8b_tp4()
+    lay = w.files[0]
+    img = synth.build_workload_file(w, 0)
+    ix = stmat.Index.from_file(img)
+    names = [e["name"] for e in ix.entries()]
+    slices = [w.slices.get(n) for n in names]
+    plan = ix.plan(dst="BF16", names=names, slices=slices)
+    buf, data_ptr = to_device(img, 0, False, lay.data_start)
+    outs = stmat.Outputs(plan)
+    plan.materialize(data_ptr, outs.ptrs)
+    torch.cuda.synchronize()
+    assert plan.check() == 0
+    ents = {e["name"]: e for e in ix.entries()}
+    for i, o in enumerate(plan.outputs()):
+        e = ents[o["name"]]
+        src = buf[e["begin"]:e["end"]].view(torch.bfloat16).view(e["shape"])
+        if o["slice"]:
+            d, a, b = o["slice"]
+            src = src.narrow(d, a, b - a)
+        assert torch.equal(outs.tensor(i).view(torch.int16), src.contiguous().view(torch.int16)), o["name"]
+    oix = oracle.parse(img)
+    sel = oix.select(dst="BF16", names=names, slices=slices)
+    window_compare(sel, plan, outs, img[lay.data_start:], np.random.Generator(np.random.PCG64(5)), windows=2)

@@ -302,3 +302,77 @@ def test_worker_balance(stmat):
         mean = sum(loads) / len(loads)
         biggest_unsplit = 1024 + 4096 * 12
         assert max(loads) <= mean + biggest_unsplit + 2048, (wl, max(loads), mean)
+
+
+# ------------------------------------------------------------- slicing
+
+def sliced_layout(seed):
+    import json
+    import struct
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shapes = [[64, 300], [9, 40, 33], [3, 5, 7, 11], [4096, 96], [2, 700], [12]]
+    dts = ["F32", "F16", "F8_E4M3", "BF16", "I64", "F8_E5M2"]
+    isz = {"F32": 4, "F16": 2, "BF16": 2, "F8_E4M3": 1, "F8_E5M2": 1, "I64": 8}
+    ents, off = {}, 0
+    for i, (shp, dt) in enumerate(zip(shapes, dts)):
+        n = int(np.prod(shp))
+        ents[f"s{i}"] = {"dtype": dt, "shape": shp, "data_offsets": [off, off + n * isz[dt]]}
+        off += n * isz[dt]
+    h = json.dumps(ents).encode()
+    return struct.pack("<Q", len(h)) + h, off, shapes, rng
+
+
+def test_slicing_outputs_match_oracle(stmat, oracle):
+    header, data_bytes, shapes, rng = sliced_layout(1)
+    L = stmat.Index.from_header(header, data_bytes)
+    O = oracle.parse(np.concatenate([np.frombuffer(header, dtype=np.uint8), np.zeros(data_bytes, np.uint8)]))
+    names = [f"s{i}" for i in range(len(shapes))]
+    for trial in range(20):
+        slices = []
+        for shp in shapes:
+            if rng.integers(0, 4) == 0:
+                slices.append(None)
+                continue
+            d = int(rng.integers(0, len(shp)))
+            a = int(rng.integers(0, shp[d]))
+            slices.append((d, a, int(rng.integers(a, shp[d] + 1))))
+        for dst in ("BF16", "KEEP"):
+            for nparts, part in ((1, 0), (2, 1)):
+                a_ = L.plan(dst=dst, names=names, slices=slices, workers=16, host_only=True, n_parts=nparts,
+                            part=part)
+                b_ = O.select(dst=dst, names=names, slices=slices, nparts=nparts, part=part)
+                assert outputs_key(a_.outputs()) == outputs_key(b_.outputs())
+    for bad in [(2, 0, 1), (0, 5, 4), (1, 0, 301), (-1, 0, 0)]:
+        sl = [bad] + [None] * (len(shapes) - 1)
+        sa = status_of(lambda: L.plan(dst="BF16", names=names, slices=sl, workers=4, host_only=True))
+        so = status_of(lambda: O.select(dst="BF16", names=names, slices=sl))
+        assert sa == so
+    assert status_of(lambda: L.plan(dst="BF16", slices=[(0, 0, 1)] * 6, workers=4, host_only=True)) == "INVAL"
+
+
+@pytest.mark.parametrize("chunk", [0, 20000])
+def test_sliced_pieces_cover_each_output_once(stmat, chunk):
+    header, data_bytes, shapes, rng = sliced_layout(2)
+    ix = stmat.Index.from_header(header, data_bytes)
+    names = [f"s{i}" for i in range(len(shapes))]
+    slices = [(1, 7, 250), (1, 3, 30), (2, 2, 5), (1, 16, 48), (1, 100, 101), (0, 2, 9)]
+    plan = ix.plan(dst="BF16", names=names, slices=slices, workers=37, host_only=True, chunk_bytes=chunk,
+                   unit_bytes=2048)
+    outs = plan.outputs()
+    st = plan.stats()
+    covered = [set() for _ in outs]
+    multi = 0
+    for k in range(st["pieces"]):
+        p = plan.piece(k)
+        si, so = CLS_SIZES[p["cls"]]
+        multi += p["rows"] > 1
+        for r in range(p["rows"]):
+            u0 = p["dst"] // so + r * p["count"]
+            for u in range(u0, u0 + p["count"]):
+                assert u not in covered[p["output"]]
+                covered[p["output"]].add(u)
+    for i, o in enumerate(outs):
+        isz = {"I64": 8, "F32": 4, "F16": 2, "BF16": 2, "F8_E4M3": 1, "F8_E5M2": 1}[o["src_dtype"]]
+        units = o["numel"] * (1 if o["dtype"] != o["src_dtype"] else isz)   # copies count bytes
+        assert len(covered[i]) == units, o["name"]
+    assert multi > 0

@@ -59,12 +59,26 @@ def check_plan(plan, data_base, dst_align, data_bytes):
     lo, hi = data_base, data_base + data_bytes
     for k in range(st["pieces"]):
         p = plan.piece(k)
+        for r in range(p["rows"]):
+            check_run(p, r, bases, outs, data_base, lo, hi)
+    # grid: blocks of 8 warps cover every worker; parts arrays have workers + 1 entries
+    blocks = (st["workers"] + 7) // 8
+    assert blocks * 8 >= st["workers"]
+    for c in range(st["chunks"]):
+        a, b = plan.worker(c, st["workers"] - 1)
+        assert b <= st["pieces"]
+
+
+def check_run(p, r, bases, outs, data_base, lo, hi):
+    """Run r of piece p (the kernel's run_rows: source + r * pitch, output +
+    r * count * itemsize) against the data section and its output."""
+    if True:
         si, so = CLS[p["cls"]]
         n = p["count"]
-        src = data_base + p["src"]
+        src = data_base + p["src"] + r * p["pitch"]
         out_base = bases[p["output"]]
         assert out_base % so == 0
-        dst = out_base + p["dst"]
+        dst = out_base + p["dst"] + r * n * so
         head, nch, K, win, drange, A = split(src, dst, n, si, so, lo, hi)
         assert 0 <= head <= n and head + nch * K <= n
         # scalar elements read [src + e si, +si) for e in head ∪ tail, all inside the piece's bytes
@@ -76,12 +90,6 @@ def check_plan(plan, data_base, dst_align, data_bytes):
         assert dst + n * so <= out_base + outs[p["output"]]["bytes"]
         if p["scale"] != (1 << 64) - 1:
             assert lo <= data_base + p["scale"] and data_base + p["scale"] + 4 <= hi
-    # grid: blocks of 8 warps cover every worker; parts arrays have workers + 1 entries
-    blocks = (st["workers"] + 7) // 8
-    assert blocks * 8 >= st["workers"]
-    for c in range(st["chunks"]):
-        a, b = plan.worker(c, st["workers"] - 1)
-        assert b <= st["pieces"]
 
 
 def _plan(stmat, wl, workers, chunk=0, dst=None):
@@ -128,3 +136,35 @@ def test_special_value_files_in_bounds(stmat, residue):
             plan = ix.plan(dst=dst, workers=workers, host_only=True)
             for dst_align in (256, 2, 1):
                 check_plan(plan, (1 << 32) + residue, dst_align, off)
+
+
+@pytest.mark.parametrize("residue", [0, 5, 8])
+def test_sliced_plans_in_bounds(stmat, residue):
+    """Slices on every dimension (multi-run pieces with a source pitch)."""
+    import json
+    import struct
+    rng = np.random.Generator(np.random.PCG64(10 + residue))
+    shapes = [[64, 300], [9, 40, 33], [3, 5, 7, 11], [4096, 96], [2, 70000]]
+    dts = ["F32", "F16", "F8_E4M3", "BF16", "I64"]
+    isz = {"F32": 4, "F16": 2, "BF16": 2, "F8_E4M3": 1, "I64": 8}
+    ents, off = {}, 0
+    for i, (shp, dt) in enumerate(zip(shapes, dts)):
+        n = int(np.prod(shp))
+        ents[f"s{i}"] = {"dtype": dt, "shape": shp, "data_offsets": [off, off + n * isz[dt]]}
+        off += n * isz[dt]
+    h = json.dumps(ents).encode()
+    ix = stmat.Index.from_header(struct.pack("<Q", len(h)) + h, off)
+    names = [f"s{i}" for i in range(len(shapes))]
+    for trial in range(6):
+        slices = []
+        for shp in shapes:
+            d = int(rng.integers(0, len(shp)))
+            a = int(rng.integers(0, shp[d]))
+            b = int(rng.integers(a, shp[d] + 1))
+            slices.append((d, a, b))
+        for dst in ("BF16", "F32", "KEEP"):
+            for workers in (1, 5, 128):
+                plan = ix.plan(dst=dst, names=names, slices=slices, workers=workers, host_only=True,
+                               unit_bytes=[4096, 32768][trial % 2])
+                for dst_align in (256, 2):
+                    check_plan(plan, (1 << 32) + residue, dst_align, off)
