@@ -8,7 +8,7 @@ default workload is the UNet-shaped checkpoint: 716 F16 tensors (2.668 GB),
 rename view 'model.diffusion_model.' -> 'unet.', materialized to BF16.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload unet|tiny|scaled_fp8|llm8b|stress]
+                  [--workload unet|tiny|scaled_fp8|llm8b|llm8b_f16|stress|...]
 
 Prints one JSON line (rank 0).  Under torchrun each rank materializes its own
 replica (no data-path collective; weak scaling), timings are max-reduced.
@@ -157,6 +157,26 @@ def selection_of(w, ix):
     return {"names": names, "slices": [w.slices.get(n) for n in names]}
 
 
+def host_image(w, stmat, torch):
+    """(root index, pinned host tensor, offset of the data section in it).
+    One shard: the whole file image.  Several: one arena holding every shard's
+    data section at the bases st_index_concat gives, under one joined index,
+    so that one plan and one launch cover all shards."""
+    from safetensors_materialization_gb300 import synth
+    if len(w.files) == 1:
+        lay = w.files[0]
+        host = torch.empty(lay.file_bytes, dtype=torch.uint8, pin_memory=True)
+        synth.build_workload_file(w, 0, out=host.numpy())
+        return stmat.Index.from_file(host.numpy()), host, lay.data_start
+    parts = [stmat.Index.from_header(lay.header, lay.data_bytes) for lay in w.files]
+    ix, bases = stmat.Index.concat(parts)
+    host = torch.empty(ix.sizes()[1], dtype=torch.uint8, pin_memory=True)
+    arena = host.numpy()
+    for k, lay in enumerate(w.files):
+        synth.build_workload_data(w, k, arena[bases[k]:bases[k] + lay.data_bytes])
+    return ix, host, 0
+
+
 def view_of(w):
     if w.rename:
         return lambda ix: ix.view_rename(w.rename)
@@ -196,7 +216,8 @@ def oracle_sample(w, seconds, reps=1):
             sel.materialize(i, data)
         times.append(time.perf_counter() - t0)
     dt = min(times)
-    desc = f"first {k} of {len(outs)} outputs ({acc / 1e6:.1f} MB dst) of {w.name}, single thread"
+    where = w.name if len(w.files) == 1 else f"shard 0 of {w.name}"
+    desc = f"first {k} of {len(outs)} outputs ({acc / 1e6:.1f} MB dst) of {where}, single thread"
     return acc / dt / 1e9, desc, acc, dt
 
 
@@ -231,7 +252,8 @@ def run_reference(args, rank, world):
             sel.materialize(i, data)
     dt = (time.perf_counter() - t0) / max(1, args.steps)
     value = acc / dt / 1e9
-    sample = f"first {k} of {len(outs)} outputs ({acc / 1e6:.1f} MB dst) of {w.name} per step"
+    where = w.name if len(w.files) == 1 else f"shard 0 of {w.name}"
+    sample = f"first {k} of {len(outs)} outputs ({acc / 1e6:.1f} MB dst) of {where} per step"
     line = {
         "impl": "reference", "metric": "materialized GB/s (dst bytes)", "value": round(value, 4),
         "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -258,21 +280,20 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     w = build_workload(args.workload)
-    lay = w.files[0]
-    # file image in pinned host memory (the e2e source); data section on the device
-    host = torch.empty(lay.file_bytes, dtype=torch.uint8, pin_memory=True)
-    synth.build_workload_file(w, 0, out=host.numpy())
-    ix = view_of(w)(stmat.Index.from_file(host.numpy()))
+    # source bytes in pinned host memory (the e2e source); data section on the device
+    root, host, data_start = host_image(w, stmat, torch)
+    ix = view_of(w)(root)
+    data_bytes = root.sizes()[1]
     sel = selection_of(w, ix)
     plan = ix.plan(dst=w.dst[0], scale_suffix=w.scale_suffix, workers=args.workers,
                    blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel,
                    order=args.order, **sel)
-    dev = torch.empty(lay.file_bytes + 256, dtype=torch.uint8, device="cuda")
+    dev = torch.empty(host.numel() + 256, dtype=torch.uint8, device="cuda")
     if w.whole_file_on_device:
-        dev[:lay.file_bytes].copy_(host)
-        data_ptr = dev.data_ptr() + lay.data_start
+        dev[:host.numel()].copy_(host)
+        data_ptr = dev.data_ptr() + data_start
     else:
-        dev[:lay.data_bytes].copy_(host[lay.data_start:])
+        dev[:data_bytes].copy_(host[data_start:data_start + data_bytes])
         data_ptr = dev.data_ptr()
     outs = stmat.Outputs(plan)
     infos = plan.outputs()
@@ -325,8 +346,8 @@ def run_ours(args, rank, world, local):
                         blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes, kernel=args.kernel,
                         order=args.order, **sel)
         copy = torch.cuda.Stream()
-        hdata = host[lay.data_start:]
-        ddata = dev[:lay.data_bytes]
+        hdata = host[data_start:data_start + data_bytes]
+        ddata = dev[:data_bytes]
         for _ in range(2):
             eplan.load(hdata, ddata, outs.ptrs, copy_stream=copy, compute_stream=stream)
             eplan.check(stream)
@@ -343,7 +364,7 @@ def run_ours(args, rank, world, local):
             t = torch.tensor([es], device="cuda")
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             es = float(t.item())
-        e2e = {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "h2d_bytes_per_step": lay.data_bytes,
+        e2e = {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "h2d_bytes_per_step": data_bytes,
                "d2h_bytes_per_step": 4, "ms_per_step": round(es * 1e3, 3),
                "chunk_bytes": args.e2e_chunk_mb << 20, "chunks": eplan.stats()["chunks"]}
 
@@ -364,6 +385,7 @@ def run_ours(args, rank, world, local):
                        "tensors": len(infos), "src_dtypes": sorted({o["src_dtype"] for o in infos}),
                        "dst_dtype": w.dst[0], "l2": "inputs exceed L2 (no flush): "
                        f"{(src_bytes + dst_bytes) / 1e9:.2f} GB per step vs 0.129 GB L2",
+                       "shard_files": len(w.files),
                        "workers": st["workers"], "pieces": st["pieces"], "kernel_build": st["kernel"],
                        "launches_per_step": launches_per_step,
                        "parallelism": f"replicas x{world}"},

@@ -117,7 +117,7 @@ st_status st_index_count(const st_index_t *index, size_t *count);
 st_status st_index_get(const st_index_t *index, size_t i, st_tensor_info *info);
 /* Position of `name` in this index/view; ST_E_NOT_FOUND if absent. */
 st_status st_index_find(const st_index_t *index, const char *name, size_t *i);
-/* N and data_bytes of the underlying file. */
+/* N and data_bytes of the underlying file (a joined index: 0 and the arena size). */
 st_status st_index_sizes(const st_index_t *index, uint64_t *header_len, uint64_t *data_bytes);
 /* Sum of numel, and per-dtype element counts (counts[15], may be NULL):
  * metadata-only parameter count and dominant dtype ("Pipeline refactors":
@@ -143,6 +143,26 @@ st_status st_view_filter(const st_index_t *parent, const char *const *names, siz
  * entries mapping to one name -> ST_E_DUP_KEY (state_dict_prefix_replace). */
 st_status st_view_rename(const st_index_t *parent, const char *const *from, const char *const *to,
                          size_t n, st_index_t **out);
+
+/* One index over several shard files ("Disk tier safetensors streaming
+ * design audit (ComfyUI)", "Strategy summary (implemented)": a
+ * checkpoint split over shard files is loaded through one streaming
+ * mapping), so that one plan and one launch cover every shard.
+ *   parts   n >= 1 indexes or views, one per shard, in arena order.
+ *   align   power of two: shard k's data section is placed in one arena at
+ *           bases[k] = the end of shard k-1's rounded up to `align`
+ *           (bases[0] = 0); the bytes between shards are never read.
+ *   bases   caller array of n entries, written on success.  The caller
+ *           places shard k's data section at arena + bases[k] and passes the
+ *           arena as data_dev / data_host.
+ * The joined index lists part 0's entries, then part 1's, ..., each in its
+ * part's order under its part's names, with offsets shifted by the part's
+ * base; data_bytes = bases[n-1] + data_bytes of part n-1; header_len = 0;
+ * metadata keeps each key's first occurrence in part order.  Names must be
+ * unique across parts (ST_E_DUP_KEY); ST_E_INVAL on NULL or a bad align.
+ * The parts may be freed afterwards. */
+st_status st_index_concat(const st_index_t *const *parts, size_t n, uint64_t align, uint64_t *bases,
+                          st_index_t **out);
 
 /* ------------------------------------------------------------------ plan */
 
@@ -292,7 +312,7 @@ st_status st_load(const void *data_host, void *data_dev, const st_plan_t *plan, 
  *     (cudaMemcpyAsync from the plan's host memory, cudaMemsetAsync for the
  *     error word) into one static device array of 4 MiB built into the
  *     library.  Every GPU that loads the library holds those 4 MiB until the
- *     process exits.  A plan that needs more (32 bytes per piece plus 4 per
+ *     process exits.  A plan that needs more (48 bytes per piece plus 4 per
  *     warp per chunk, each part rounded up to 256 bytes) is rejected with
  *     ST_E_INVAL before anything is queued; plan with a larger unit_bytes or
  *     fewer workers to shrink it.

@@ -34,6 +34,7 @@ def lib():
         P, U64, I64, I = C.c_void_p, C.c_uint64, C.c_int64, C.c_int
         sig = {
             "or_parse": (I, [C.c_char_p, U64, C.POINTER(P)]),
+            "or_parse_header": (I, [C.c_char_p, U64, U64, C.POINTER(P)]),
             "or_index_free": (None, [P]),
             "or_count": (U64, [P]), "or_header_len": (U64, [P]), "or_data_bytes": (U64, [P]),
             "or_name": (C.c_char_p, [P, U64]), "or_dtype": (I, [P, U64]), "or_ndim": (I, [P, U64]),
@@ -44,6 +45,7 @@ def lib():
             "or_view_prefix": (I, [P, C.c_char_p, C.POINTER(P)]),
             "or_view_filter": (I, [P, C.POINTER(C.c_char_p), U64, C.POINTER(P)]),
             "or_view_rename": (I, [P, C.POINTER(C.c_char_p), C.POINTER(C.c_char_p), U64, C.POINTER(P)]),
+            "or_concat": (I, [C.POINTER(P), U64, U64, C.POINTER(U64), C.POINTER(P)]),
             "or_out_dtype": (I, [I, I]),
             "or_convert": (I, [I, I, C.c_char_p, U64, I, C.c_float, P]),
             "or_select": (I, [P, C.POINTER(C.c_char_p), U64, C.POINTER(C.c_char_p), C.c_char_p,
@@ -229,6 +231,24 @@ def parse(file_bytes):
         else np.ascontiguousarray(file_bytes, dtype=np.uint8)
     out = C.c_void_p()
     _check(lib().or_parse(C.cast(arr.ctypes.data, C.c_char_p), arr.size, C.byref(out)))
+    return OIndex(out.value)
+
+
+def concat(parts, align=256):
+    """Joined index over shard indexes; returns (index, bases)."""
+    n = len(parts)
+    hs = (C.c_void_p * max(1, n))(*[p.handle.value for p in parts])
+    bases = (C.c_uint64 * max(1, n))()
+    out = C.c_void_p()
+    _check(lib().or_concat(hs, n, align, bases, C.byref(out)))
+    return OIndex(out.value, keep=list(parts)), [int(b) for b in bases[:n]]
+
+
+def parse_header(header, data_bytes):
+    """Index from the first 8 + N bytes of a file and its data section size."""
+    arr = np.frombuffer(bytes(header), dtype=np.uint8)
+    out = C.c_void_p()
+    _check(lib().or_parse_header(C.cast(arr.ctypes.data, C.c_char_p), arr.size, data_bytes, C.byref(out)))
     return OIndex(out.value)
 
 

@@ -533,20 +533,20 @@ static char *mark_repeats(char **keys, uint64_t n) {
   return rep;
 }
 
-/* Parses a whole file image (header length, JSON header, data section). */
-int or_parse(const uint8_t *file, uint64_t file_len, or_index **out) {
-  uint64_t N, data_bytes, i, expect;
+/* Parses the first 8 + N bytes of a file (`len` of them given) whose data
+   section is `data_bytes` long. */
+int or_parse_header(const uint8_t *file, uint64_t len, uint64_t data_bytes, or_index **out) {
+  uint64_t N, i, expect;
   jreader r;
   jval root;
   or_index *ix;
   char *repeated;
   int st = OR_OK;
   *out = NULL;
-  if (file_len < 8) return OR_E_TRUNCATED;
+  if (len < 8) return OR_E_TRUNCATED;
   N = read_u64le(file);
   if (N > OR_MAX_HEADER) return OR_E_HEADER_TOO_LARGE;
-  if (N > file_len - 8) return OR_E_TRUNCATED;
-  data_bytes = file_len - 8 - N;
+  if (N > len - 8) return OR_E_TRUNCATED;
   r.p = file + 8;
   r.end = file + 8 + N;
   r.depth = 0;
@@ -587,6 +587,17 @@ int or_parse(const uint8_t *file, uint64_t file_len, or_index **out) {
   if (expect != data_bytes) { or_index_free(ix); return OR_E_OFFSETS; }
   *out = ix;
   return OR_OK;
+}
+
+/* Parses a whole file image (header length, JSON header, data section). */
+int or_parse(const uint8_t *file, uint64_t file_len, or_index **out) {
+  uint64_t N;
+  *out = NULL;
+  if (file_len < 8) return OR_E_TRUNCATED;
+  N = read_u64le(file);
+  if (N > OR_MAX_HEADER) return OR_E_HEADER_TOO_LARGE;
+  if (N > file_len - 8) return OR_E_TRUNCATED;
+  return or_parse_header(file, 8 + N, file_len - 8 - N, out);
 }
 
 /* --- accessors (for ctypes) --- */
@@ -698,6 +709,57 @@ int or_view_rename(const or_index *parent, const char *const *from, const char *
     free(buf);
     if (st != OR_OK) { or_index_free(v); return st; }
   }
+  for (i = 0; i < v->n; i++)
+    for (j = 0; j < i; j++)
+      if (strcmp(v->e[i].name, v->e[j].name) == 0) { or_index_free(v); return OR_E_DUP_KEY; }
+  *out = v;
+  return OR_OK;
+}
+
+/* Joined index over shard files ("Strategy summary (implemented)": one
+   streaming mapping over a checkpoint split in shards).  Reading: shard k's
+   data section sits in one arena at bases[k], the previous shard's end
+   rounded up to a multiple of `align`; the joined index lists every part's
+   entries in part order with offsets shifted by the part's base; a name in
+   two parts is an error; metadata keeps a key's first occurrence. */
+int or_concat(const or_index *const *parts, uint64_t n, uint64_t align, uint64_t *bases, or_index **out) {
+  uint64_t k, i, j, total = 0, metas = 0, end = 0;
+  or_index *v;
+  if (n == 0 || align == 0 || (align & (align - 1)) != 0) return OR_E_INVAL;
+  for (k = 0; k < n; k++) {
+    total += parts[k]->n;
+    metas += parts[k]->nmeta;
+  }
+  v = (or_index *)calloc(1, sizeof(or_index));
+  if (!v) return OR_E_NOMEM;
+  v->e = (or_entry *)calloc(total ? total : 1, sizeof(or_entry));
+  v->meta_keys = (char **)calloc(metas ? metas : 1, sizeof(char *));
+  v->meta_vals = (char **)calloc(metas ? metas : 1, sizeof(char *));
+  if (!v->e || !v->meta_keys || !v->meta_vals) { or_index_free(v); return OR_E_NOMEM; }
+  for (k = 0; k < n; k++) {
+    const or_index *p = parts[k];
+    uint64_t base = end;
+    while (base % align != 0) base++;
+    bases[k] = base;
+    end = base + p->data_bytes;
+    for (i = 0; i < p->n; i++) {
+      if (view_add(v, &p->e[i], p->e[i].name) != OR_OK) { or_index_free(v); return OR_E_NOMEM; }
+      v->e[v->n - 1].begin += base;
+      v->e[v->n - 1].end += base;
+    }
+    for (i = 0; i < p->nmeta; i++) {
+      int seen = 0;
+      for (j = 0; j < v->nmeta; j++)
+        if (strcmp(v->meta_keys[j], p->meta_keys[i]) == 0) seen = 1;
+      if (seen) continue;
+      v->meta_keys[v->nmeta] = dupstr(p->meta_keys[i]);
+      v->meta_vals[v->nmeta] = dupstr(p->meta_vals[i]);
+      v->nmeta++;
+      if (!v->meta_keys[v->nmeta - 1] || !v->meta_vals[v->nmeta - 1]) { or_index_free(v); return OR_E_NOMEM; }
+    }
+  }
+  v->data_bytes = end;
+  v->header_len = 0;
   for (i = 0; i < v->n; i++)
     for (j = 0; j < i; j++)
       if (strcmp(v->e[i].name, v->e[j].name) == 0) { or_index_free(v); return OR_E_DUP_KEY; }

@@ -779,3 +779,44 @@ st_status st_view_rename(const st_index *parent, const char *const *from, const 
 }
 
 }  // extern "C"
+
+extern "C" {
+
+st_status st_index_concat(const st_index *const *parts, size_t n, uint64_t align, uint64_t *bases, st_index **out) {
+  if (!parts || !n || !bases || !out) return set_error(ST_E_INVAL, "NULL argument or no parts");
+  *out = nullptr;
+  if (align == 0 || (align & (align - 1))) return set_error(ST_E_INVAL, "align %llu is not a power of two",
+                                                            (unsigned long long)align);
+  for (size_t k = 0; k < n; ++k)
+    if (!parts[k]) return set_error(ST_E_INVAL, "NULL part %zu", k);
+  try {
+    auto core = std::make_shared<Core>();
+    uint64_t at = 0;
+    for (size_t k = 0; k < n; ++k) {
+      const IndexData &p = *parts[k]->d;
+      const uint64_t size = p.core->data_bytes;
+      const uint64_t base = (at + align - 1) & ~(align - 1);
+      if (base < at || base + size < base) return set_error(ST_E_OFFSETS, "the joined data sections overflow 64 bits");
+      bases[k] = base;
+      at = base + size;
+      for (size_t i = 0; i < p.ent.size(); ++i) {
+        Tensor t = p.core->tensors[p.ent[i]];
+        t.name = p.names[i];
+        t.begin += base;
+        t.end += base;
+        core->tensors.push_back(std::move(t));
+      }
+      for (const auto &kv : p.core->meta) {
+        bool seen = false;
+        for (const auto &m : core->meta) seen = seen || m.first == kv.first;
+        if (!seen) core->meta.push_back(kv);
+      }
+    }
+    core->data_bytes = at;
+    return wrap(make_root(core), out);
+  } catch (const std::bad_alloc &) {
+    return set_error(ST_E_NOMEM, "out of host memory");
+  }
+}
+
+}  // extern "C"

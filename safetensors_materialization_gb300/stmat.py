@@ -27,7 +27,8 @@ STATUS = ["ST_OK", "ST_E_INVAL", "ST_E_TRUNCATED", "ST_E_HEADER_JSON", "ST_E_HEA
 EXPORTS = [
     "st_header_size", "st_index_build", "st_index_build_file", "st_index_free", "st_index_count",
     "st_index_get", "st_index_find", "st_index_sizes", "st_index_numel", "st_index_metadata_count",
-    "st_index_metadata_get", "st_view_prefix", "st_view_filter", "st_view_rename", "st_plan",
+    "st_index_metadata_get", "st_view_prefix", "st_view_filter", "st_view_rename", "st_index_concat",
+    "st_plan",
     "st_plan_free", "st_plan_count", "st_plan_output", "st_plan_arena", "st_plan_stats",
     "st_plan_piece", "st_plan_worker", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
     "st_materialize_noalloc",
@@ -99,6 +100,7 @@ def lib():
             "st_view_prefix": [P, C.c_char_p, PP],
             "st_view_filter": [P, C.POINTER(C.c_char_p), S, PP],
             "st_view_rename": [P, C.POINTER(C.c_char_p), C.POINTER(C.c_char_p), S, PP],
+            "st_index_concat": [C.POINTER(P), S, U64, C.POINTER(U64), PP],
             "st_plan": [P, C.POINTER(Selection), I, C.POINTER(PlanOptions), PP],
             "st_plan_count": [P, C.POINTER(S)],
             "st_plan_output": [P, S, C.POINTER(OutputInfo)],
@@ -258,6 +260,17 @@ class Index:
         _check(lib().st_view_rename(self._h, _strs([a for a, _ in rules]), _strs([b for _, b in rules]),
                                     len(rules), C.byref(out)))
         return Index(out.value)
+
+    @classmethod
+    def concat(cls, parts, align=256):
+        """st_index_concat: one index over shard indexes; returns (index, bases),
+        shard k's data section belonging at arena offset bases[k]."""
+        n = len(parts)
+        hs = (C.c_void_p * max(1, n))(*[p.handle.value for p in parts])
+        bases = (C.c_uint64 * max(1, n))()
+        out = C.c_void_p()
+        _check(lib().st_index_concat(hs, n, align, bases, C.byref(out)))
+        return cls(out.value), [int(b) for b in bases[:n]]
 
     def plan(self, dst="BF16", names=None, scale_names=None, scale_suffix=None, part=0, n_parts=0,
              workers=0, chunk_bytes=0, host_only=False, blocks_per_sm=0, unit_bytes=0, kernel=0, order=0,

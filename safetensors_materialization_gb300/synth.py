@@ -334,7 +334,24 @@ WORKLOADS = {"tiny": tiny, "unet": unet, "scaled_fp8": scaled_fp8, "llm8b": llm8
              "scaled_fp8_5blk": lambda: scaled_fp8(blocks=5),
              # a UNet with 8 of the 38 1280-channel resblocks (0.83 GB source), for profiling
              "unet_small": lambda: unet(n1280=8),
-             "llm8b_tp4": llm8b_tp4}
+             "llm8b_tp4": llm8b_tp4,
+             # the same 4-shard checkpoint cast to F16 (the second run of the LLM config)
+             "llm8b_f16": lambda: _with_dst(llm8b(), ["F16"])}
+
+
+def _with_dst(wl: Workload, dst):
+    wl.dst = dst
+    wl.name += "_to_" + dst[0].lower()
+    return wl
+
+
+def build_workload_data(wl: Workload, k: int, out: np.ndarray):
+    """Data section of shard k of workload `wl` into `out` (uint8, data_bytes long)."""
+    lay = wl.files[k]
+    fill(lay, out, wl.seeds[k])
+    if wl.scale_suffix:
+        fill_scales(lay, out, wl.seeds[k])
+    return out
 
 
 def build_workload_file(wl: Workload, k: int, out: np.ndarray | None = None):

@@ -294,16 +294,76 @@ def test_scaled_fp8_workload(stmat, oracle):
     workload_case(stmat, oracle, "scaled_fp8")
 
 
-@pytest.mark.parametrize("shard", [0, 3])
-def test_llm_copy_is_byte_identical(stmat, oracle, shard):
-    """BF16 -> BF16 is a raw copy: at full size every output equals its source bytes."""
-    plan, outs, buf, lay, img = workload_case(stmat, oracle, "llm8b", shard=shard, dst_index=0)
+def joined(stmat, oracle, w, align=256):
+    """Every shard of `w` under one joined index (library and oracle) and one
+    host arena holding each shard's data section at its base."""
+    from safetensors_materialization_gb300 import synth
+    ix, bases = stmat.Index.concat([stmat.Index.from_header(l.header, l.data_bytes) for l in w.files], align)
+    oix, obases = oracle.concat([oracle.parse_header(l.header, l.data_bytes) for l in w.files], align)
+    assert bases == obases
+    arena = np.zeros(ix.sizes()[1], np.uint8)
+    for k, lay in enumerate(w.files):
+        synth.build_workload_data(w, k, arena[bases[k]:bases[k] + lay.data_bytes])
+    return ix, oix, arena
+
+
+@pytest.mark.parametrize("align", [1, 256])
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_joined_shards_one_launch(stmat, oracle, align, kernel):
+    """A 4-shard checkpoint joined into one arena and materialized by one
+    launch; align=1 packs the shards back to back, so later shards' sources
+    lose their alignment."""
+    from safetensors_materialization_gb300 import synth
+    w = synth.llm8b(seed=5, layers=4, hidden=256, inter=704, vocab=1000, kv=64, shards=4)
+    ix, oix, arena = joined(stmat, oracle, w, align)
+    dev = torch.from_numpy(arena).cuda()
+    for dst in ("BF16", "F16", "F32"):
+        plan = ix.plan(dst=dst, kernel=kernel)
+        assert plan.stats()["chunks"] == 1
+        outs = stmat.Outputs(plan)
+        plan.materialize(dev.data_ptr(), outs.ptrs)
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        sel = oix.select(dst=dst)
+        assert_same(plan, outs, sel, [sel.materialize(i, arena) for i in range(len(sel))])
+
+
+@pytest.fixture(scope="module")
+def llm_joined(stmat, oracle):
+    """The full 8B LLM checkpoint: 4 shard files, 16.06 GB, joined."""
+    from safetensors_materialization_gb300 import synth
+    ix, oix, arena = joined(stmat, oracle, synth.llm8b())
+    dev = torch.from_numpy(arena).cuda()
+    yield ix, oix, arena, dev
+    del dev
+    torch.cuda.empty_cache()
+
+
+def test_llm_copy_is_byte_identical(stmat, oracle, llm_joined):
+    """BF16 -> BF16 over all 4 shards in one launch is a raw copy: at full
+    size every output equals its source bytes; windows match the oracle."""
+    ix, oix, arena, dev = llm_joined
+    plan = ix.plan(dst="BF16")
+    outs = stmat.Outputs(plan)
+    plan.materialize(dev.data_ptr(), outs.ptrs)
+    torch.cuda.synchronize()
+    assert plan.check() == 0
     for i, o in enumerate(plan.outputs()):
-        assert torch.equal(outs.raw(i), buf[o["begin"]:o["begin"] + o["bytes"]]), o["name"]
+        assert torch.equal(outs.raw(i), dev[o["begin"]:o["begin"] + o["bytes"]]), o["name"]
+    window_compare(oix.select(dst="BF16"), plan, outs, arena, np.random.Generator(np.random.PCG64(12)),
+                   windows=1)
 
 
-def test_llm_cast_to_f16(stmat, oracle):
-    workload_case(stmat, oracle, "llm8b", shard=1, dst_index=1)
+def test_llm_cast_to_f16(stmat, oracle, llm_joined):
+    """BF16 -> F16 over all 4 shards in one launch, compared with the oracle on
+    windows of every tensor."""
+    ix, oix, arena, dev = llm_joined
+    plan = ix.plan(dst="F16")
+    outs = stmat.Outputs(plan)
+    plan.materialize(dev.data_ptr(), outs.ptrs)
+    torch.cuda.synchronize()
+    assert plan.check() == 0
+    window_compare(oix.select(dst="F16"), plan, outs, arena, np.random.Generator(np.random.PCG64(13)))
 
 
 # ------------------------------------------------------ pipeline and misc
