@@ -38,12 +38,13 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="unet")
+    ap.add_argument("--dst", default=None, help="output dtype (default: the workload's)")
     ap.add_argument("--e2e-chunk-mb", type=int, default=128)
     ap.add_argument("--workers", type=int, default=0, help="warps to balance over (0: from --blocks-per-sm)")
     ap.add_argument("--blocks-per-sm", type=int, default=0, help="resident 8-warp blocks per SM (0: library default)")
     ap.add_argument("--unit-bytes", type=int, default=0, help="traffic per interleaved unit (0: library default)")
     ap.add_argument("--kernel", type=int, default=0, help="kernel build: 0 auto, 1 streaming, 2 latency")
-    ap.add_argument("--order", type=int, default=0, help="unit order: 0 class-major, 1 source")
+    ap.add_argument("--order", type=int, default=0, help="unit order: 0 the build's default, 1 source, 2 class-major")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -143,9 +144,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def build_workload(name):
+def build_workload(name, dst=None):
     from safetensors_materialization_gb300 import synth
     w = synth.WORKLOADS[name]()
+    if dst and dst != w.dst[0]:
+        w.dst = [dst]
+        w.name += "_to_" + dst.lower()
+        if dst == "KEEP":
+            w.scale_suffix = None
     return w
 
 
@@ -226,7 +232,7 @@ def run_reference(args, rank, world):
     each step materializes a bounded sample of the workload on one host core."""
     if rank != 0:
         return
-    w = build_workload(args.workload)
+    w = build_workload(args.workload, args.dst)
     per_step = max(0.5, min(8.0, 60.0 / max(1, args.steps + args.warmup)))
     from oracle import oracle as O
     from safetensors_materialization_gb300 import synth
@@ -279,7 +285,7 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    w = build_workload(args.workload)
+    w = build_workload(args.workload, args.dst)
     # source bytes in pinned host memory (the e2e source); data section on the device
     root, host, data_start = host_image(w, stmat, torch)
     ix = view_of(w)(root)

@@ -64,7 +64,7 @@ typedef enum st_status {
   ST_E_ALIGN = 11,           /* a pointer is not aligned as required */
   ST_E_NOMEM = 12,           /* host allocation failed */
   ST_E_CUDA = 13,            /* a CUDA runtime call failed (message has the CUDA error) */
-  ST_E_DEVICE = 14           /* the kernel reported a bad destination (st_plan_check) */
+  ST_E_DEVICE = 14           /* the kernel reported a bad destination or a wait that gave up (st_plan_check) */
 } st_status;
 
 /* Dtypes in the header's spelling; ST_KEEP is only an output request. */
@@ -214,11 +214,17 @@ typedef struct st_plan_options {
   int32_t host_only;      /* nonzero: build the plan without touching the GPU (requires workers) */
   uint32_t blocks_per_sm; /* 0 = 3 for the streaming build, the most that fit for the latency build */
   uint64_t unit_bytes;    /* traffic per interleaved unit; 0 = 32768 */
-  uint32_t kernel;        /* 0 = choose: the latency build when outputs average under 64 KiB of
+  uint32_t kernel;        /* 0 = choose: the TMA build when outputs average under 64 KiB of
                              traffic (many small tensors), else the streaming build; 1 = streaming
-                             build (deep unroll); 2 = latency build (high occupancy) */
-  uint32_t order;         /* unit order within a chunk: 0 = grouped by conversion class, then
-                             source order (all warps run one class at a time); 1 = source order */
+                             build (deep unroll); 2 = latency build (high occupancy); 3 = TMA
+                             build (source bytes staged in shared memory by bulk copies; the
+                             data section must then be device or managed memory, else
+                             st_materialize returns ST_E_INVAL) */
+  uint32_t order;         /* unit order within a chunk: 0 = the build's default (2 for builds 1
+                             and 2, 1 for the TMA build); 1 = source order (the TMA build then
+                             fetches adjacent small tensors with one bulk copy); 2 = grouped by
+                             conversion class, then source order (all warps run one class at a
+                             time) */
 } st_plan_options;
 
 /* Builds the plan: outputs, then pieces (output element ranges).  Each chunk
@@ -250,7 +256,7 @@ st_status st_plan_output(const st_plan_t *plan, size_t i, st_output_info *info);
 /* Offsets of every output in one buffer, each aligned to `align` (a power of
  * two >= 16); offsets has st_plan_count entries.  `total` is the size. */
 st_status st_plan_arena(const st_plan_t *plan, uint64_t align, uint64_t *offsets, uint64_t *total);
-/* Piece/worker layout and kernel build (1 streaming, 2 latency), for tests and
+/* Piece/worker layout and kernel build (1 streaming, 2 latency, 3 TMA), for tests and
  * tuning; any pointer may be NULL. */
 st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chunks, uint64_t *pieces,
                         uint32_t *kernel);
@@ -331,7 +337,9 @@ st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *plan, vo
                                  const float *scales, void *stream);
 
 /* Waits for `stream`, then reads and clears the plan's device error flags:
- * bit 0 = a non-empty output had a NULL or misaligned destination.
+ * bit 0 = a non-empty output had a NULL or misaligned destination;
+ * bit 1 = the TMA build gave up a bounded wait for a staged copy (its warp
+ * stopped early; outputs are incomplete).
  * Returns ST_E_DEVICE when any flag was set. */
 st_status st_plan_check(const st_plan_t *plan, void *stream, uint32_t *flags);
 

@@ -53,9 +53,10 @@ constexpr uint32_t kClsBits = 5;
 constexpr uint32_t kMaxOutputs = 1u << (32 - kClsBits);
 constexpr int kWarpsPerBlock = 8;
 
-// Bit set in the device error word when an output's destination is NULL or
-// not aligned to its itemsize.
+// Bits of the device error word: an output's destination is NULL or not
+// aligned to its itemsize; a bounded wait for a staged copy gave up.
 constexpr uint32_t kErrBadDst = 1u;
+constexpr uint32_t kErrTimeout = 2u;
 
 struct LaunchArgs {
   const uint8_t *data;     // data section on the device
@@ -69,7 +70,7 @@ struct LaunchArgs {
 };
 
 // Output itemsize of a class (bytes written per counted unit).
-ST_HD inline int cls_out_size(uint32_t c) {
+ST_HD constexpr int cls_out_size(uint32_t c) {
   switch (c) {
     case CLS_COPY: return 1;
     case CLS_F32_BF16: case CLS_F32_F16: case CLS_F16_BF16: case CLS_BF16_F16:
@@ -79,7 +80,7 @@ ST_HD inline int cls_out_size(uint32_t c) {
 }
 
 // Source itemsize of a class (bytes read per counted unit).
-ST_HD inline int cls_in_size(uint32_t c) {
+ST_HD constexpr int cls_in_size(uint32_t c) {
   switch (c) {
     case CLS_COPY: return 1;
     case CLS_F32_BF16: case CLS_F32_F16: return 4;
@@ -88,10 +89,26 @@ ST_HD inline int cls_in_size(uint32_t c) {
   }
 }
 
-// Kernel builds (st_kernels.cu): deep unroll for large tensors, or higher
-// occupancy for many small tensors.
+// log2 of the two itemsizes, packed two bits per class, for shift-only address
+// arithmetic in the kernels.
+constexpr uint32_t pack_shifts(bool out) {
+  uint32_t v = 0;
+  for (uint32_t c = 0; c < CLS_COUNT; ++c) {
+    const int size = out ? cls_out_size(c) : cls_in_size(c);
+    v |= static_cast<uint32_t>(size == 4 ? 2 : size == 2 ? 1 : 0) << (2 * c);
+  }
+  return v;
+}
+constexpr uint32_t kInShifts = pack_shifts(false), kOutShifts = pack_shifts(true);
+ST_HD constexpr uint32_t cls_in_shift(uint32_t c) { return (kInShifts >> (2 * c)) & 3u; }
+ST_HD constexpr uint32_t cls_out_shift(uint32_t c) { return (kOutShifts >> (2 * c)) & 3u; }
+
+// Kernel builds (st_kernels.cu): deep unroll for large tensors, higher
+// occupancy for many small tensors, or source bytes staged in shared memory
+// by the bulk-copy (TMA) engine.
 constexpr uint32_t kKernelStream = 1;
 constexpr uint32_t kKernelLatency = 2;
+constexpr uint32_t kKernelTma = 3;
 
 // Resident 256-thread blocks per SM for a kernel build, and the SM count of
 // the current device.

@@ -34,11 +34,16 @@
 //  - code size matters: one kernel serves every class, and workloads that
 //    mix classes (many small tensors) otherwise stall on instruction fetch,
 //    so each class has just an aligned and a misaligned body.
+// Three builds share the codecs: streaming (deep register batches, for large
+// tensors), latency (shallow batches at high occupancy) and TMA (source bytes
+// staged in shared memory by bulk copies, for many small tensors; see "the
+// TMA build" below).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 #include <mutex>
 #include <string>
@@ -497,17 +502,406 @@ __global__ void __launch_bounds__(kThreads, ST_LAT_MIN_BLOCKS) materialize_laten
   materialize_body<LatencyCfg>(a);
 }
 
+// ------------------------------------------------------------ the TMA build
+//
+// Source bytes travel through shared memory instead of registers: each warp
+// cuts its pieces into segments of up to kSeg source bytes and keeps kSlots
+// of them in flight, each fetched by one bulk copy (cp.async.bulk, the TMA
+// engine) into a slot of the warp's shared memory and tracked by an mbarrier.
+// The bytes a warp has in flight no longer cost registers, so an SM keeps
+// about kWarps * kSlots * kSeg bytes of reads outstanding however small the
+// tensors are; the registers-only builds hold far less while a warp walks
+// many small tensors one dependent round trip at a time.
+//  - A bulk copy needs 16-byte aligned global and shared addresses and a
+//    multiple of 16 bytes, so a segment is fetched as the aligned window
+//    covering it, clipped to the 16-byte aligned interior of the data
+//    section; the few elements outside that interior (only at the two ends
+//    of the data section) are read with byte loads.  No byte outside the
+//    data section is read.
+//  - The consumer reads the window from shared memory: lane c takes source
+//    step c (SB bytes) as two aligned words and realigns them by the
+//    window's byte offset, converts, and stores one 16- or 8-byte vector;
+//    elements before the first aligned destination vector or after the
+//    last are converted one by one from shared memory.
+//  - Piece descriptors arrive the same way, 32 at a time, one batch ahead.
+//  - One warp is both producer and consumer, so a slot is refilled only
+//    after the warp has finished reading it (program order, __syncwarp and
+//    a proxy fence).  Every wait is bounded: a wait that gives up sets
+//    kErrTimeout, waits (bounded) for the warp's copies still in flight and
+//    ends the warp.
+#ifndef ST_TMA_SEG
+#define ST_TMA_SEG 2048
+#endif
+#ifndef ST_TMA_SLOTS
+#define ST_TMA_SLOTS 4
+#endif
+
+constexpr uint32_t kSeg = ST_TMA_SEG;
+constexpr int kSlots = ST_TMA_SLOTS;
+constexpr uint32_t kSlotBytes = kSeg + 32;  // a clipped window is at most kSeg + 16 bytes
+constexpr uint32_t kSpinLimit = 1u << 22;
+static_assert(kSeg % 16 == 0 && kSeg >= 64, "segment size");
+
+// One staged segment: a run of one piece, elements [0, len); elements
+// [a, z) are in the slot, the rest are read with byte loads.
+struct SegMeta {
+  uint8_t *dst;         // output address of element 0
+  const uint8_t *gsrc;  // data-section address of element 0
+  uint32_t len;         // elements (bytes for CLS_COPY)
+  uint32_t a, z;
+  uint32_t off;         // slot offset of element a
+  float scale;
+  uint32_t cls;
+};
+
+struct alignas(128) WarpSmem {
+  uint8_t buf[kSlots][kSlotBytes];
+  Piece desc[2][32];
+  uint8_t *dstp[2][32];
+  float scl[2][32];
+  SegMeta meta[kSlots];
+  uint64_t bar[kSlots];
+  uint64_t dbar[2];
+};
+static_assert(offsetof(WarpSmem, desc) % 16 == 0 && kSlotBytes % 16 == 0, "bulk-copy destinations");
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void proxy_fence() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Lane 0: one arrival that also expects `bytes` of copies, then the copy.
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+  if (bytes == 0) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+    return;
+  }
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+template <int N>
+__device__ __forceinline__ void lds(const uint8_t *p, uint32_t (&v)[N]) {
+  if constexpr (N == 4) {
+    const uint4 x = *reinterpret_cast<const uint4 *>(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else if constexpr (N == 2) {
+    const uint2 x = *reinterpret_cast<const uint2 *>(p);
+    v[0] = x.x; v[1] = x.y;
+  } else {
+    v[0] = *reinterpret_cast<const uint32_t *>(p);
+  }
+}
+
+template <class CV>
+__device__ __forceinline__ void convert_one(const uint8_t *p, uint8_t *q, float scale) {
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < CV::SI; ++i) bits |= static_cast<uint32_t>(p[i]) << (8 * i);
+  const uint32_t y = CV::one(bits, scale);
+  if constexpr (CV::SO == 1) *q = static_cast<uint8_t>(y);
+  else if constexpr (CV::SO == 2) *reinterpret_cast<uint16_t *>(q) = static_cast<uint16_t>(y);
+  else *reinterpret_cast<uint32_t *>(q) = y;
+}
+
+// A staged segment: elements [a, z) from the slot (element a at slot offset
+// `off`), the rest from global with byte loads.
+template <class CV>
+__device__ __forceinline__ void consume_seg(const uint8_t *buf, const SegMeta &m, uint32_t lane) {
+  constexpr int SI = CV::SI, SO = CV::SO, SB = CV::SB, KS = CV::KS, OS = CV::OS, N = SB / 4;
+  const float scale = m.scale;
+  uint8_t *const dst = m.dst;
+  const uint32_t len = m.len, off = m.off, a = m.a, z = m.z;
+  const uint32_t edge = a + (len - z);
+  for (uint32_t t = lane; t < edge; t += 32) {
+    const uint32_t e = t < a ? t : z + (t - a);
+    convert_one<CV>(m.gsrc + static_cast<uint64_t>(e) * SI, dst + static_cast<uint64_t>(e) * SO, scale);
+  }
+  const uint32_t n = z - a;
+  const uint8_t *sp = buf + off;
+  uint8_t *dp = dst + static_cast<uint64_t>(a) * SO;
+  uint32_t h = static_cast<uint32_t>(((OS - (reinterpret_cast<uintptr_t>(dp) & (OS - 1))) & (OS - 1)) / SO);
+  if (h > n) h = n;
+  const uint32_t nst = (n - h) / KS, t0 = h + nst * KS;
+  const uint32_t ends = h + (n - t0);
+  for (uint32_t t = lane; t < ends; t += 32) {
+    const uint32_t e = t < h ? t : t0 + (t - h);
+    convert_one<CV>(sp + e * SI, dp + e * SO, scale);
+  }
+  const uint32_t q = off + h * SI, r = q & (SB - 1);
+  const uint8_t *wb = buf + (q - r);
+  uint8_t *db = dp + h * SO;
+  for (uint32_t c = lane; c < nst; c += 32) {
+    uint32_t x[N], sv[N];
+    lds<N>(wb + c * SB, x);
+    if (r) {
+      uint32_t y[N];
+      lds<N>(wb + (c + 1) * SB, y);
+      realign<N>(x, y, r, sv);
+    } else {
+#pragma unroll
+      for (int i = 0; i < N; ++i) sv[i] = x[i];
+    }
+    uint32_t o[OS / 4];
+    CV::step(sv, scale, o);
+    store_out<OS / 4>(db + c * OS, o);
+  }
+}
+
+__device__ __forceinline__ void consume_any(const uint8_t *buf, const SegMeta &m, uint32_t lane) {
+  switch (m.cls) {
+    case CLS_COPY: consume_seg<CopyBytes>(buf, m, lane); break;
+    case CLS_F32_BF16: consume_seg<Conv<S_F32, D_BF16>>(buf, m, lane); break;
+    case CLS_F32_F16: consume_seg<Conv<S_F32, D_F16>>(buf, m, lane); break;
+    case CLS_F16_BF16: consume_seg<Conv<S_F16, D_BF16>>(buf, m, lane); break;
+    case CLS_F16_F32: consume_seg<Conv<S_F16, D_F32>>(buf, m, lane); break;
+    case CLS_BF16_F16: consume_seg<Conv<S_BF16, D_F16>>(buf, m, lane); break;
+    case CLS_BF16_F32: consume_seg<Conv<S_BF16, D_F32>>(buf, m, lane); break;
+    case CLS_E4M3_BF16: consume_seg<Conv<S_E4M3, D_BF16>>(buf, m, lane); break;
+    case CLS_E4M3_F16: consume_seg<Conv<S_E4M3, D_F16>>(buf, m, lane); break;
+    case CLS_E4M3_F32: consume_seg<Conv<S_E4M3, D_F32>>(buf, m, lane); break;
+    case CLS_E5M2_BF16: consume_seg<Conv<S_E5M2, D_BF16>>(buf, m, lane); break;
+    case CLS_E5M2_F16: consume_seg<Conv<S_E5M2, D_F16>>(buf, m, lane); break;
+    case CLS_E5M2_F32: consume_seg<Conv<S_E5M2, D_F32>>(buf, m, lane); break;
+    default: break;
+  }
+}
+
+// Producer cursor over a warp's pieces: batch, piece in batch, run, element.
+struct Cursor {
+  uint32_t b, i, r, n;  // n = pieces in batch b
+  uint32_t e;
+};
+
+__global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs a) {
+  extern __shared__ __align__(128) uint8_t tma_smem[];
+  const uint32_t lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const uint32_t w = blockIdx.x * kWarpsPerBlock + wib;
+  if (w >= a.workers) return;
+  const uint32_t p0 = a.parts[w], p1 = a.parts[w + 1];
+  if (p0 >= p1) return;
+  WarpSmem &ws = reinterpret_cast<WarpSmem *>(tma_smem)[wib];
+  const uint32_t nbatch = (p1 - p0 + 31) / 32;
+  const uintptr_t lo16 = (reinterpret_cast<uintptr_t>(a.data) + 15) & ~uintptr_t(15);
+  const uintptr_t hi16 = (reinterpret_cast<uintptr_t>(a.data) + a.data_bytes) & ~uintptr_t(15);
+
+  auto issue_desc = [&](uint32_t bb) {  // lane 0
+    const uint32_t cnt = min(32u, p1 - p0 - 32 * bb);
+    bulk_load(ws.desc[bb & 1], a.pieces + p0 + 32 * bb, cnt * static_cast<uint32_t>(sizeof(Piece)), &ws.dbar[bb & 1]);
+  };
+  if (lane == 0) {
+    for (int k = 0; k < kSlots; ++k) mbar_init(&ws.bar[k]);
+    mbar_init(&ws.dbar[0]);
+    mbar_init(&ws.dbar[1]);
+    mbar_init_fence();
+    issue_desc(0);
+  }
+  uint32_t dissued = 1, dseen = 0;  // descriptor batches fetched / waited for
+  __syncwarp();
+
+  // Waits for descriptor batch b, resolves its destinations and scales, and
+  // fetches batch b + 1 into the other descriptor slot.
+  auto enter_batch = [&](uint32_t b) -> bool {
+    if (!mbar_wait(&ws.dbar[b & 1], (b >> 1) & 1)) return false;
+    dseen = b + 1;
+    const uint32_t cnt = min(32u, p1 - p0 - 32 * b);
+    if (lane < cnt) {
+      const Piece &pc = ws.desc[b & 1][lane];
+      const uint32_t out = pc.out_cls >> kClsBits, cls = pc.out_cls & ((1u << kClsBits) - 1);
+      uint8_t *d = static_cast<uint8_t *>(a.dst[out]);
+      float scale = 1.0f;
+      if (cls >= CLS_E4M3_BF16) {
+        if (a.scales) scale = a.scales[out];
+        else if (pc.scale != kNoScale) scale = load_f32_le(a.data + pc.scale);
+      }
+      if (d == nullptr || cls >= CLS_COUNT ||
+          (reinterpret_cast<uintptr_t>(d) & static_cast<uintptr_t>(cls_out_size(cls) - 1))) {
+        atomicOr(a.err, kErrBadDst);
+        d = nullptr;
+      }
+      ws.dstp[b & 1][lane] = d;
+      ws.scl[b & 1][lane] = scale;
+    }
+    __syncwarp();
+    if (b + 1 < nbatch) {
+      if (lane == 0) {
+        proxy_fence();
+        issue_desc(b + 1);
+      }
+      dissued = b + 2;
+    }
+    return true;
+  };
+
+  // The piece being cut into segments: its fields are loaded once, when the
+  // cursor reaches it, and the run's source/output addresses advance by the
+  // pitch / run size, so a segment costs no divisions or multiplications.
+  Cursor cur{0, 0, 0, min(32u, p1 - p0), 0};
+  const uint8_t *run_src = nullptr;  // source of the current run's element 0
+  uint8_t *run_dst = nullptr;        // output address of the current run's element 0
+  uint64_t pitch = 0;
+  uint32_t count = 0, rows = 0, cls = 0, sis = 0, sos = 0;
+  float scale = 1.0f;
+  bool loaded = false;
+  auto load_piece_state = [&]() -> bool {  // false: skip this piece
+    const Piece &pc = ws.desc[cur.b & 1][cur.i];
+    uint8_t *dp = ws.dstp[cur.b & 1][cur.i];
+    count = pc.count;
+    rows = pc.rows;
+    if (dp == nullptr || count == 0 || rows == 0) return false;
+    cls = pc.out_cls & ((1u << kClsBits) - 1);
+    sis = cls_in_shift(cls);
+    sos = cls_out_shift(cls);
+    pitch = pc.pitch;
+    run_src = a.data + pc.src;
+    run_dst = dp + pc.dst;
+    scale = ws.scl[cur.b & 1][cur.i];
+    return true;
+  };
+  auto produce = [&](int slot) -> int {  // 1 issued, 0 done, -1 timed out
+    for (;;) {
+      if (cur.i == cur.n) {
+        if (++cur.b == nbatch) return 0;
+        cur.i = 0;
+        cur.r = 0;
+        cur.e = 0;
+        cur.n = min(32u, p1 - p0 - 32 * cur.b);
+        if (!enter_batch(cur.b)) return -1;
+        continue;
+      }
+      if (!loaded) {
+        if (!load_piece_state()) {
+          ++cur.i;
+          continue;
+        }
+        loaded = true;
+      }
+      const uint32_t len = min(kSeg >> sis, count - cur.e);
+      const uint8_t *s0 = run_src + (static_cast<uint64_t>(cur.e) << sis);
+      const uintptr_t s = reinterpret_cast<uintptr_t>(s0);
+      const uintptr_t send = s + (static_cast<uint64_t>(len) << sis);
+      uint32_t A = 0, Z = len;
+      if (s < lo16) A = min(len, static_cast<uint32_t>((lo16 - s + (1u << sis) - 1) >> sis));
+      if (send > hi16) Z = hi16 > s ? static_cast<uint32_t>((hi16 - s) >> sis) : 0;
+      if (Z < A) Z = A;
+      uint32_t bytes = 0, off = 0;
+      uintptr_t w0 = 0;
+      if (Z > A) {
+        const uintptr_t sa = s + (static_cast<uint64_t>(A) << sis);
+        w0 = sa & ~uintptr_t(15);
+        bytes = static_cast<uint32_t>(((s + (static_cast<uint64_t>(Z) << sis) + 15) & ~uintptr_t(15)) - w0);
+        off = static_cast<uint32_t>(sa - w0);
+      }
+      if (lane == 0) {
+        SegMeta &m = ws.meta[slot];
+        m.dst = run_dst + (static_cast<uint64_t>(cur.e) << sos);
+        m.gsrc = s0;
+        m.len = len;
+        m.a = A;
+        m.z = Z;
+        m.off = off;
+        m.scale = scale;
+        m.cls = cls;
+        proxy_fence();
+        bulk_load(ws.buf[slot], reinterpret_cast<const void *>(w0), bytes, &ws.bar[slot]);
+      }
+      cur.e += len;
+      if (cur.e == count) {
+        cur.e = 0;
+        run_src += pitch;
+        run_dst += static_cast<uint64_t>(count) << sos;
+        if (++cur.r == rows) {
+          cur.r = 0;
+          ++cur.i;
+          loaded = false;
+        }
+      }
+      return 1;
+    }
+  };
+
+  bool ok = enter_batch(0);
+  uint32_t jp = 0, jc = 0;
+  bool more = ok;
+  while (ok) {
+    while (more && jp - jc < static_cast<uint32_t>(kSlots)) {
+      const int got = produce(static_cast<int>(jp % kSlots));
+      if (got > 0) ++jp;
+      else {
+        more = false;
+        ok = got == 0;
+      }
+    }
+    if (!ok || jc == jp) break;
+    const int slot = static_cast<int>(jc % kSlots);
+    if (!mbar_wait(&ws.bar[slot], (jc / kSlots) & 1)) {
+      ok = false;
+      break;
+    }
+    __syncwarp();
+    consume_any(ws.buf[slot], ws.meta[slot], lane);
+    __syncwarp();
+    ++jc;
+  }
+  if (!ok) {
+    // A wait gave up: record it, then give the warp's outstanding copies a
+    // bounded chance to land before the warp (and its shared memory) ends.
+    if (lane == 0) atomicOr(a.err, kErrTimeout);
+    for (; jc < jp; ++jc) mbar_wait(&ws.bar[jc % kSlots], (jc / kSlots) & 1);
+    for (; dseen < dissued; ++dseen) mbar_wait(&ws.dbar[dseen & 1], (dseen >> 1) & 1);
+  }
+}
+
 std::string cuda_msg(cudaError_t e) { return std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e); }
 
+}  // namespace
+
+namespace {
+constexpr size_t kTmaSmem = sizeof(WarpSmem) * kWarpsPerBlock;
+constexpr int kMaxDevices = 256;
+std::mutex g_attr_mu;
+bool g_tma_attr[kMaxDevices] = {};
+
+// The TMA build's dynamic shared memory exceeds the default 48 KiB: raise
+// the kernel's limit once per device.
+cudaError_t tma_attr(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (g_tma_attr[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(materialize_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kTmaSmem));
+  if (e == cudaSuccess) g_tma_attr[dev] = true;
+  return e;
+}
 }  // namespace
 
 st_status kernel_occupancy(uint32_t variant, int *sms, int *blocks_per_sm) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && variant == kKernelTma) e = tma_attr(dev);
   if (e == cudaSuccess)
     e = variant == kKernelLatency
             ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_latency, kThreads, 0)
+        : variant == kKernelTma
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_tma, kThreads, kTmaSmem)
             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_stream, kThreads, 0);
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "querying the device: %s", cuda_msg(e).c_str());
   if (*blocks_per_sm < 1) *blocks_per_sm = 1;
@@ -517,8 +911,17 @@ st_status kernel_occupancy(uint32_t variant, int *sms, int *blocks_per_sm) {
 st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream) {
   const uint32_t blocks = (a.workers + kWarpsPerBlock - 1) / kWarpsPerBlock;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (variant == kKernelLatency) materialize_latency<<<blocks, kThreads, 0, st>>>(a);
-  else materialize_stream<<<blocks, kThreads, 0, st>>>(a);
+  if (variant == kKernelTma) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = tma_attr(dev);
+    if (e != cudaSuccess) return set_error(ST_E_CUDA, "enabling %zu bytes of shared memory: %s", kTmaSmem, cuda_msg(e).c_str());
+    materialize_tma<<<blocks, kThreads, kTmaSmem, st>>>(a);
+  } else if (variant == kKernelLatency) {
+    materialize_latency<<<blocks, kThreads, 0, st>>>(a);
+  } else {
+    materialize_stream<<<blocks, kThreads, 0, st>>>(a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "materialize launch (%u blocks): %s", blocks, cuda_msg(e).c_str());
   return ST_OK;
@@ -536,7 +939,6 @@ st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 namespace {
-constexpr int kMaxDevices = 256;
 std::mutex g_static_mu;
 void *g_static_addr[kMaxDevices] = {};
 }  // namespace

@@ -477,8 +477,8 @@ st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst
     uint32_t workers = opts ? opts->workers : 0;
     p->chunk_bytes = opts ? opts->chunk_bytes : 0;
     if (opts && opts->unit_bytes) p->unit_bytes = opts->unit_bytes;
-    if (opts && opts->order > 1) return set_error(ST_E_INVAL, "options.order must be 0 or 1");
-    p->class_major = !(opts && opts->order == 1);
+    const uint32_t order = opts ? opts->order : 0;
+    if (order > 2) return set_error(ST_E_INVAL, "options.order must be 0, 1 or 2");
     uint64_t cost = 0, traffic = 0, nonempty = 0;
     for (const Output &o : p->outs) {
       const uint64_t t = o.units * (cls_in_size(o.cls) + cls_out_size(o.cls));
@@ -486,14 +486,21 @@ st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst
       traffic += t;
       nonempty += t > 0;
     }
-    // Many small tensors: the latency build at full occupancy; else streaming.
+    // Many small tensors: the TMA build (reads staged in shared memory, so a
+    // warp keeps kilobytes in flight whatever the tensor size); else the
+    // streaming build.
     if (opts && opts->kernel) {
-      if (opts->kernel != kKernelStream && opts->kernel != kKernelLatency)
-        return set_error(ST_E_INVAL, "options.kernel must be 0, 1 or 2");
+      if (opts->kernel != kKernelStream && opts->kernel != kKernelLatency && opts->kernel != kKernelTma)
+        return set_error(ST_E_INVAL, "options.kernel must be 0, 1, 2 or 3");
       p->kernel = opts->kernel;
     } else {
-      p->kernel = nonempty && traffic / nonempty < kSmallOutputBytes ? kKernelLatency : kKernelStream;
+      p->kernel = nonempty && traffic / nonempty < kSmallOutputBytes ? kKernelTma : kKernelStream;
     }
+    // Unit order: the register builds run one class at a time (their
+    // per-class code is large, and mixing classes stalls on instruction
+    // fetch); the TMA build's code is small, and source order lets adjacent
+    // small tensors share one bulk copy.
+    p->class_major = order == 2 || (order == 0 && p->kernel != kKernelTma);
     int sms = 0, blocks = 0;
     if (!host_only || workers == 0) {
       if (host_only) return set_error(ST_E_INVAL, "a host-only plan needs options.workers");
@@ -624,6 +631,18 @@ st_status check_device_plan(const st_plan_t *p) {
   return ST_OK;
 }
 
+// The TMA build's bulk copies read the data section: it must be device (or
+// managed) memory.
+st_status check_tma_source(const st_plan_t *p, const void *data_dev) {
+  if (p->kernel != kKernelTma || !data_dev) return ST_OK;
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, data_dev);
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "cudaPointerGetAttributes: %s", cuda_msg(e).c_str());
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+    return set_error(ST_E_INVAL, "the TMA build needs the data section in device or managed memory");
+  return ST_OK;
+}
+
 st_status launch_chunk(const st_plan_t *p, uint32_t k, const void *data_dev, void *const *dst, const float *scales,
                        void *stream) {
   if (p->pieces.empty()) return ST_OK;
@@ -652,6 +671,8 @@ st_status st_materialize(const void *data_dev, const st_plan_t *p, void *const *
   if (s != ST_OK) return s;
   if (p->pieces.empty()) return ST_OK;
   if (!data_dev || !dst_ptrs) return set_error(ST_E_INVAL, "NULL data or destination array");
+  s = check_tma_source(p, data_dev);
+  if (s != ST_OK) return s;
   for (uint32_t k = 0; k < p->n_chunks; ++k) {
     s = launch_chunk(p, k, data_dev, dst_ptrs, scales, stream);
     if (s != ST_OK) return s;
@@ -686,6 +707,8 @@ st_status st_load(const void *data_host, void *data_dev, const st_plan_t *p, voi
   if (s != ST_OK) return s;
   const uint64_t data = p->index->core->data_bytes;
   if ((data && (!data_host || !data_dev)) || !dst_ptrs) return set_error(ST_E_INVAL, "NULL pointer");
+  s = check_tma_source(p, data_dev);
+  if (s != ST_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(copy_stream), ks = static_cast<cudaStream_t>(compute_stream);
   // The copies overwrite data_dev: order them after work already on the compute stream.
   cudaEvent_t start = p->events[p->n_chunks];
@@ -716,6 +739,8 @@ st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *p, void 
   if (!p) return set_error(ST_E_INVAL, "NULL plan");
   if (p->pieces.empty()) return ST_OK;
   if (!data_dev || !dst_ptrs) return set_error(ST_E_INVAL, "NULL data or destination array");
+  st_status s = check_tma_source(p, data_dev);
+  if (s != ST_OK) return s;
   // Layout inside the static array: pieces | warp ranges | error word.
   const size_t pieces_bytes = p->pieces.size() * sizeof(Piece);
   const size_t parts_off = (pieces_bytes + 255) & ~size_t(255);
@@ -728,7 +753,7 @@ st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *p, void 
                      "holds %zu; plan with a larger unit_bytes or fewer workers",
                      need, p->pieces.size(), p->workers, p->n_chunks, kStaticScratchBytes);
   void *scratch = nullptr;
-  st_status s = static_scratch(&scratch);
+  s = static_scratch(&scratch);
   if (s != ST_OK) return s;
   uint8_t *base = static_cast<uint8_t *>(scratch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -764,7 +789,10 @@ st_status st_plan_check(const st_plan_t *p, void *stream, uint32_t *flags) {
   if (e == cudaSuccess && v) e = cudaMemset(p->d_err, 0, sizeof v);
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "reading the error word: %s", cuda_msg(e).c_str());
   *flags = v;
-  if (v) return set_error(ST_E_DEVICE, "device flags 0x%x: a non-empty output had a NULL or misaligned destination", v);
+  if (v)
+    return set_error(ST_E_DEVICE, "device flags 0x%x:%s%s", v,
+                     (v & kErrBadDst) ? " a non-empty output had a NULL or misaligned destination;" : "",
+                     (v & kErrTimeout) ? " a wait for a staged copy gave up;" : "");
   return ST_OK;
 }
 

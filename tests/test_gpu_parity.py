@@ -151,12 +151,12 @@ def special_image(seed=0):
 
 @pytest.mark.parametrize("dst", ["BF16", "F16", "F32"])
 @pytest.mark.parametrize("packed", [False, True])
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_every_bit_pattern(stmat, oracle, dst, packed, kernel):
     img = special_image()
     sfx = (".weight", ".scale_weight")
     plan, outs, _ = run(stmat, img, dst=dst, scale_suffix=sfx, packed=packed, kernel=kernel)
-    assert plan.stats()["kernel"] == {1: "stream", 2: "latency"}[kernel]
+    assert plan.stats()["kernel"] == {1: "stream", 2: "latency", 3: "tma"}[kernel]
     sel, want = oracle_all(oracle, img, dst=dst, scale_suffix=sfx)
     assert_same(plan, outs, sel, want)
 
@@ -197,7 +197,7 @@ def test_alignment_sweep(stmat, oracle, residue):
     for dst in ("BF16", "F16", "F32", "KEEP"):
         sel, want = oracle_all(oracle, img, dst=dst)
         for packed in (False, True):
-            for kernel in (1, 2):
+            for kernel in (1, 2, 3):
                 plan, outs, _ = run(stmat, img, dst=dst, offset=residue, packed=packed,
                                     workers=[0, 7, 333][residue % 3], kernel=kernel)
                 assert_same(plan, outs, sel, want)
@@ -215,16 +215,17 @@ def test_data_section_edges(stmat, oracle):
         img = image_of(ents, a.tobytes() + b.tobytes())
         sel, want = oracle_all(oracle, img, dst="BF16")
         ix = stmat.Index.from_file(img)
-        plan = ix.plan(dst="BF16")
         data = img[8 + ix.sizes()[0]:]
-        for shift in (1, 5, 9, 15):
-            buf = torch.zeros(data.size + 32, dtype=torch.uint8, device="cuda")
-            buf[shift:shift + data.size].copy_(torch.from_numpy(data.copy()))
-            outs = stmat.Outputs(plan)
-            plan.materialize(buf.data_ptr() + shift, outs.ptrs)
-            torch.cuda.synchronize()
-            assert plan.check() == 0
-            assert_same(plan, outs, sel, want)
+        for kernel in (1, 2, 3):
+            plan = ix.plan(dst="BF16", kernel=kernel)
+            for shift in (1, 5, 9, 15):
+                buf = torch.zeros(data.size + 32, dtype=torch.uint8, device="cuda")
+                buf[shift:shift + data.size].copy_(torch.from_numpy(data.copy()))
+                outs = stmat.Outputs(plan)
+                plan.materialize(buf.data_ptr() + shift, outs.ptrs)
+                torch.cuda.synchronize()
+                assert plan.check() == 0
+                assert_same(plan, outs, sel, want)
 
 
 # ------------------------------------------------------------- workloads
@@ -246,7 +247,7 @@ def window_compare(oracle_sel, plan, outs, data, rng, width=4096, windows=3):
             assert np.array_equal(got, want), (o["name"], s)
 
 
-def workload_case(stmat, oracle, name, shard=0, dst_index=0, full=False):
+def workload_case(stmat, oracle, name, shard=0, dst_index=0, full=False, kernel=0):
     from safetensors_materialization_gb300 import synth
     w = synth.WORKLOADS[name]()
     lay = w.files[shard]
@@ -258,7 +259,7 @@ def workload_case(stmat, oracle, name, shard=0, dst_index=0, full=False):
         view = lambda ix: ix.view_prefix(w.prefix)  # noqa: E731
     dst = w.dst[dst_index]
     plan, outs, buf = run(stmat, img, dst=dst, view=view, scale_suffix=w.scale_suffix,
-                          whole=w.whole_file_on_device)
+                          whole=w.whole_file_on_device, kernel=kernel)
     oix = oracle.parse(img)
     if view:
         oix = view(oix)
@@ -276,13 +277,15 @@ def test_tiny_workload_full(stmat, oracle):
     workload_case(stmat, oracle, "tiny", full=True)
 
 
-def test_stress_workload_full(stmat, oracle):
+@pytest.mark.parametrize("kernel", [0, 2])
+def test_stress_workload_full(stmat, oracle, kernel):
     """100k tensors, 7 dtypes, every source 1-15 bytes off 16-byte alignment."""
-    workload_case(stmat, oracle, "stress", full=True)
+    workload_case(stmat, oracle, "stress", full=True, kernel=kernel)
 
 
-def test_unet_workload(stmat, oracle):
-    plan, outs, buf, lay, img = workload_case(stmat, oracle, "unet")
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_unet_workload(stmat, oracle, kernel):
+    plan, outs, buf, lay, img = workload_case(stmat, oracle, "unet", kernel=kernel)
     # full size: F16 -> BF16 of N(0, 0.02) data (no NaN) equals torch's cast on every element
     data = buf[:lay.data_bytes]
     for i, o in enumerate(plan.outputs()):
@@ -290,8 +293,9 @@ def test_unet_workload(stmat, oracle):
         assert torch.equal(outs.raw(i).view(torch.int16), src.to(torch.bfloat16).view(torch.int16)), o["name"]
 
 
-def test_scaled_fp8_workload(stmat, oracle):
-    workload_case(stmat, oracle, "scaled_fp8")
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_scaled_fp8_workload(stmat, oracle, kernel):
+    workload_case(stmat, oracle, "scaled_fp8", kernel=kernel)
 
 
 def joined(stmat, oracle, w, align=256):
@@ -308,7 +312,7 @@ def joined(stmat, oracle, w, align=256):
 
 
 @pytest.mark.parametrize("align", [1, 256])
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_joined_shards_one_launch(stmat, oracle, align, kernel):
     """A 4-shard checkpoint joined into one arena and materialized by one
     launch; align=1 packs the shards back to back, so later shards' sources
@@ -472,7 +476,7 @@ def sliced_image(seed):
     return image_of(ents, b"".join(parts), pad=5), shapes, rng
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_sliced_outputs(stmat, oracle, kernel):
     """Slices on every dimension (contiguous and strided runs) at misaligned
     sources, into aligned and packed outputs."""

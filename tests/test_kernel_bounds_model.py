@@ -8,7 +8,9 @@ lies in the data section, every byte it writes lies in the piece's output,
 and head + body + tail cover the piece's elements exactly once.  Data bases
 are taken at every residue mod 16 and destinations at 256-byte and at
 itemsize-only alignment.  This must be kept in step with
-csrc/st_kernels.cu (run_piece).
+csrc/st_kernels.cu (run_piece; produce and consume_seg of the TMA build,
+whose bulk copies also need 16-byte aligned windows inside the data
+section that fit the warp's shared-memory slot).
 """
 import numpy as np
 import pytest
@@ -43,6 +45,149 @@ def split(src, dst, n, si, so, lo, hi):
     return head, nst, KS, win, (dbase, dbase + nst * OS) if nst else None, A
 
 
+def _tma_consts():
+    """Segment size and slots of the TMA build, read from the kernel source."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "safetensors_materialization_gb300", "csrc", "st_kernels.cu")).read()
+    seg = int(re.search(r"#define ST_TMA_SEG (\d+)", src).group(1))
+    slots = int(re.search(r"#define ST_TMA_SLOTS (\d+)", src).group(1))
+    return seg, slots
+
+
+SEG, SLOTS = _tma_consts()
+SLOT_BYTES = SEG + 32
+
+
+def tma_run(src, dst, n, si, so, lo, hi):
+    """Mirror of the TMA build on one run (materialize_tma's produce and
+    consume_seg): yields per segment the bulk-copy window, the global scalar
+    reads, the shared-memory reads and the stores, and checks each against
+    the rules a bulk copy and the slot impose."""
+    SB = 16 * si // so if so > si else 16
+    KS = SB // si
+    OS = KS * so
+    lo16 = (lo + 15) & ~15
+    hi16 = hi & ~15
+    covered = []
+    e = 0
+    while e < n:
+        ln = min(SEG // si, n - e)
+        s = src + e * si
+        A, Z = 0, ln
+        if s < lo16:
+            A = min(ln, (lo16 - s + si - 1) // si)
+        if s + ln * si > hi16:
+            Z = (hi16 - s) // si if hi16 > s else 0
+        Z = max(Z, A)
+        nbytes, off = 0, 0
+        if Z > A:
+            w0 = (s + A * si) & ~15
+            w1 = (s + Z * si + 15) & ~15
+            nbytes, off = w1 - w0, s + A * si - w0
+            assert w0 % 16 == 0 and nbytes % 16 == 0 and 0 < nbytes <= SEG + 16
+            assert lo <= lo16 <= w0 and w1 <= hi16 <= hi, (w0, w1, lo16, hi16)
+            assert 0 <= off < 16
+        for x in list(range(0, A)) + list(range(Z, ln)):   # byte loads from the data section
+            assert lo <= s + x * si and s + (x + 1) * si <= hi
+        m = Z - A
+        dp = dst + (e + A) * so
+        h = min(((OS - (dp & (OS - 1))) & (OS - 1)) // so, m)
+        nst = (m - h) // KS
+        t0 = h + nst * KS
+        for x in list(range(0, h)) + list(range(t0, m)):   # scalar reads from the slot
+            assert off + (x + 1) * si <= nbytes
+        if nst:
+            q = off + h * si
+            r = q & (SB - 1)
+            end = (q - r) + (nst + (1 if r else 0)) * SB
+            assert end <= SLOT_BYTES
+            assert q + nst * SB <= nbytes          # the bytes used were copied
+            assert (dp + h * so) % OS == 0
+        covered.append((e, e + ln))
+        e += ln
+    return covered
+
+
+def consume_model(off, ln, a, z, nbytes, dst, si, so):
+    """Mirror of consume_seg for one piece's part of a slot: the slot reads
+    stay inside the slot and inside the copied bytes; vector stores aligned."""
+    SB = 16 * si // so if so > si else 16
+    KS = SB // si
+    OS = KS * so
+    m = z - a
+    dp = dst + a * so
+    h = min(((OS - (dp & (OS - 1))) & (OS - 1)) // so, m)
+    nst = (m - h) // KS
+    t0 = h + nst * KS
+    for x in list(range(0, h)) + list(range(t0, m)):   # scalar reads from the slot
+        assert off + (x + 1) * si <= nbytes
+    if nst:
+        q = off + h * si
+        r = q & (SB - 1)
+        assert (q - r) + (nst + (1 if r else 0)) * SB <= SLOT_BYTES
+        assert q + nst * SB <= nbytes
+        assert (dp + h * so) % OS == 0
+
+
+def tma_warp(plan, pieces, bases, data_base, lo, hi):
+    """Mirror of materialize_tma's producer over one warp's pieces (batches of
+    32, segments of at most SEG source bytes): every bulk copy is 16-byte
+    aligned, inside the 16-byte aligned interior of the data section and fits
+    its slot; every element of every run is produced exactly once."""
+    lo16, hi16 = (lo + 15) & ~15, hi & ~15
+    done = {}
+    for b0 in range(0, len(pieces), 32):
+        batch = pieces[b0:b0 + 32]
+        i, r, e = 0, 0, 0
+        while i < len(batch):
+            p = batch[i]
+            if p["count"] == 0 or r >= p["rows"]:
+                i, r, e = i + 1, 0, 0
+                continue
+            si, so = CLS[p["cls"]]
+            cnt = p["count"]
+            ln = min(SEG // si, cnt - e)
+            s = data_base + p["src"] + r * p["pitch"] + e * si
+            A, Z = 0, ln
+            if s < lo16:
+                A = min(ln, (lo16 - s + si - 1) // si)
+            if s + ln * si > hi16:
+                Z = (hi16 - s) // si if hi16 > s else 0
+            Z = max(Z, A)
+            nbytes = off = w0 = 0
+            if Z > A:
+                w0 = (s + A * si) & ~15
+                w1 = (s + Z * si + 15) & ~15
+                nbytes, off = w1 - w0, s + A * si - w0
+            for x in list(range(0, A)) + list(range(Z, ln)):
+                assert lo <= s + x * si and s + (x + 1) * si <= hi
+            dst0 = bases[p["output"]] + p["dst"] + (r * cnt + e) * so
+            subs = [(off, ln, A, Z, dst0, si, so)]
+            done.setdefault((id(p), r), []).append((e, e + ln))
+            e += ln
+            if e == cnt:
+                e = 0
+                r += 1
+                if r == p["rows"]:
+                    r = 0
+                    i += 1
+            if nbytes:
+                assert w0 % 16 == 0 and nbytes % 16 == 0 and 0 < nbytes <= SEG + 16
+                assert lo <= lo16 <= w0 and w0 + nbytes <= hi16 <= hi
+            for (o, ln2, a2, z2, d2, si2, so2) in subs:
+                consume_model(o, ln2, a2, z2, nbytes, d2, si2, so2)
+    for p in pieces:
+        for r in range(p["rows"]):
+            got = sorted(done.get((id(p), r), []))
+            pos = 0
+            for a_, b_ in got:
+                assert a_ == pos
+                pos = b_
+            assert pos == p["count"]
+
+
 def check_plan(plan, data_base, dst_align, data_bytes):
     outs = plan.outputs()
     st = plan.stats()
@@ -57,10 +202,14 @@ def check_plan(plan, data_base, dst_align, data_bytes):
         bases.append(at)
         at += o["bytes"]
     lo, hi = data_base, data_base + data_bytes
-    for k in range(st["pieces"]):
-        p = plan.piece(k)
+    pieces = [plan.piece(k) for k in range(st["pieces"])]
+    for p in pieces:
         for r in range(p["rows"]):
             check_run(p, r, bases, outs, data_base, lo, hi)
+    for c in range(st["chunks"]):
+        for w in range(st["workers"]):
+            a, b = plan.worker(c, w)
+            tma_warp(plan, pieces[a:b], bases, data_base, lo, hi)
     # grid: blocks of 8 warps cover every worker; parts arrays have workers + 1 entries
     blocks = (st["workers"] + 7) // 8
     assert blocks * 8 >= st["workers"]
@@ -92,7 +241,7 @@ def check_run(p, r, bases, outs, data_base, lo, hi):
             assert lo <= data_base + p["scale"] and data_base + p["scale"] + 4 <= hi
 
 
-def _plan(stmat, wl, workers, chunk=0, dst=None):
+def _plan(stmat, wl, workers, chunk=0, dst=None, kernel=0):
     from safetensors_materialization_gb300 import synth
     w = synth.WORKLOADS[wl]()
     lay = w.files[0]
@@ -102,16 +251,17 @@ def _plan(stmat, wl, workers, chunk=0, dst=None):
     if w.prefix:
         ix = ix.view_prefix(w.prefix)
     return ix.plan(dst=dst or w.dst[0], scale_suffix=w.scale_suffix, workers=workers, chunk_bytes=chunk,
-                   host_only=True), lay
+                   host_only=True, kernel=kernel), lay
 
 
 @pytest.mark.parametrize("wl,workers,chunk", [("tiny", 664, 0), ("stress", 9728, 0), ("stress", 777, 1 << 26)])
 @pytest.mark.parametrize("residue", [0, 1, 7, 8, 15])
 def test_workload_accesses_stay_in_bounds(stmat, wl, workers, chunk, residue):
-    plan, lay = _plan(stmat, wl, workers, chunk)
-    base = (1 << 32) + residue + (lay.data_start if residue == 7 else 0)
-    for dst_align in (256, 2):
-        check_plan(plan, base, dst_align, lay.data_bytes)
+    for kernel in (0, 3):   # class-major and source unit order
+        plan, lay = _plan(stmat, wl, workers, chunk, kernel=kernel)
+        base = (1 << 32) + residue + (lay.data_start if residue == 7 else 0)
+        for dst_align in (256, 2):
+            check_plan(plan, base, dst_align, lay.data_bytes)
 
 
 @pytest.mark.parametrize("residue", [0, 3, 8, 13])
@@ -132,8 +282,8 @@ def test_special_value_files_in_bounds(stmat, residue):
     h = json.dumps(ents).encode()
     ix = stmat.Index.from_header(struct.pack("<Q", len(h)) + h, off)
     for dst in ("BF16", "F16", "F32", "KEEP"):
-        for workers in (1, 3, 64):
-            plan = ix.plan(dst=dst, workers=workers, host_only=True)
+        for workers, kernel in ((1, 0), (3, 3), (64, 0), (64, 3)):
+            plan = ix.plan(dst=dst, workers=workers, host_only=True, kernel=kernel)
             for dst_align in (256, 2, 1):
                 check_plan(plan, (1 << 32) + residue, dst_align, off)
 
@@ -165,6 +315,24 @@ def test_sliced_plans_in_bounds(stmat, residue):
         for dst in ("BF16", "F32", "KEEP"):
             for workers in (1, 5, 128):
                 plan = ix.plan(dst=dst, names=names, slices=slices, workers=workers, host_only=True,
-                               unit_bytes=[4096, 32768][trial % 2])
+                               unit_bytes=[4096, 32768][trial % 2], kernel=[0, 3][trial % 2])
                 for dst_align in (256, 2):
                     check_plan(plan, (1 << 32) + residue, dst_align, off)
+
+
+def test_tma_windows_on_tiny_data_sections():
+    """Data sections of 1..80 bytes at every residue mod 16, cut into two or
+    three tensors of every class: the TMA build's windows stay inside the
+    16-byte aligned interior (or are skipped) and the byte loads inside the
+    section."""
+    for nbytes in range(1, 81):
+        for residue in range(16):
+            lo = (1 << 32) + residue
+            hi = lo + nbytes
+            for cls, (si, so) in CLS.items():
+                n = nbytes // si
+                for cut in sorted({0, n // 3, n // 2, n}):
+                    for a, b in ((0, cut), (cut, n)):
+                        if b > a:
+                            segs = tma_run(lo + a * si, (1 << 40) + 256 + a * so, b - a, si, so, lo, hi)
+                            assert segs[-1][1] == b - a
