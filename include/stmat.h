@@ -166,7 +166,9 @@ st_status st_index_concat(const st_index_t *const *parts, size_t n, uint64_t ali
 
 /* ------------------------------------------------------------------ plan */
 
-/* A range along one dimension ("TensorFrame ... supports slicing metadata"):
+/* A range along one dimension (the slicing metadata a TensorFrame carries,
+ * "Disk tier safetensors streaming design audit (ComfyUI)", "FastSageTensors
+ * (fastsafetensors) capability audit"):
  * the output keeps indices [start, stop) of dimension `dim` and all of the
  * others, row-major, so its shape is the tensor's with shape[dim] =
  * stop - start.  dim < 0: the whole tensor.  0 <= dim < ndim and
