@@ -50,6 +50,11 @@ def lib():
             "or_convert": (I, [I, I, C.c_char_p, U64, I, C.c_float, P]),
             "or_select": (I, [P, C.POINTER(C.c_char_p), U64, C.POINTER(C.c_char_p), C.c_char_p,
                               C.c_char_p, I, U64, U64, C.POINTER(I64), C.POINTER(P)]),
+            "or_select_q": (I, [P, C.POINTER(C.c_char_p), U64, C.POINTER(C.c_char_p), C.c_char_p,
+                                C.c_char_p, I, U64, U64, C.POINTER(I64), C.POINTER(C.c_int),
+                                C.POINTER(C.c_char_p), C.POINTER(C.c_char_p), C.POINTER(I64), C.POINTER(P)]),
+            "or_plan_quant": (I, [P, U64]), "or_plan_qscale": (I64, [P, U64]),
+            "or_plan_qscale2": (I64, [P, U64]),
             "or_plan_numel": (U64, [P, U64]), "or_plan_ndim": (I, [P, P, U64]),
             "or_plan_dim": (I64, [P, P, U64, I]),
             "or_plan_free": (None, [P]), "or_plan_count": (U64, [P]),
@@ -153,8 +158,10 @@ class OIndex:
         return OIndex(out.value, keep=self)
 
     def select(self, names=None, dst="BF16", scale_names=None, scale_suffix=None,
-               part=0, nparts=1, slices=None):
-        """slices: per name None or (dim, start, stop)."""
+               part=0, nparts=1, slices=None, quant=None):
+        """slices: per name None or (dim, start, stop).  quant: per name None or
+        (kind, scale name, global scale name or None, (block rows, block cols)),
+        kind "block_fp8" or "nvfp4"."""
         out = C.c_void_p()
         nm = _strs(names) if names is not None else None
         sn = _strs(scale_names) if scale_names is not None else None
@@ -165,9 +172,19 @@ class OIndex:
             for x in slices:
                 flat += list(x) if x is not None else [-1, 0, 0]
             sl = (C.c_int64 * max(1, len(flat)))(*flat)
-        _check(lib().or_select(self._h, nm, len(names) if names is not None else 0, sn,
-                               fr.encode() if fr else None, to.encode() if to else None,
-                               DTYPES.index(dst), part, nparts, sl, C.byref(out)))
+        qk = qs = qs2 = qb = None
+        if quant is not None:
+            kinds = {"block_fp8": 2, "nvfp4": 3}
+            qk = (C.c_int * max(1, len(quant)))(*[kinds.get(q[0], 99) if q else 0 for q in quant])
+            qs = _strs([q[1] if q else None for q in quant])
+            qs2 = _strs([q[2] if q else None for q in quant])
+            blocks = []
+            for q in quant:
+                blocks += list(q[3]) if q and len(q) > 3 and q[3] else [0, 0]
+            qb = (C.c_int64 * max(1, len(blocks)))(*blocks)
+        _check(lib().or_select_q(self._h, nm, len(names) if names is not None else 0, sn,
+                                 fr.encode() if fr else None, to.encode() if to else None,
+                                 DTYPES.index(dst), part, nparts, sl, qk, qs, qs2, qb, C.byref(out)))
         return OPlan(out.value, self)
 
 
@@ -201,6 +218,7 @@ class OPlan:
             "begin": e["begin"],
             "scale": None if sc < 0 else self.index.entry(sc)["name"],
             "bytes": L.or_plan_bytes(self.index.handle, self._h, i),
+            "quant": {0: None, 2: "block_fp8", 3: "nvfp4"}[L.or_plan_quant(self._h, i)],
         }
 
     def outputs(self):

@@ -917,6 +917,10 @@ int or_convert(int src, int out, const uint8_t *in, uint64_t n, int scaled, floa
 /* 5. Selection and plan: which outputs, in which order, with which scale. */
 /* ===================================================================== */
 
+/* Block-scaled weight formats (an output of one of them reads a second
+   tensor of scales): */
+enum { OR_Q_NONE = 0, OR_Q_BLOCK_FP8 = 2, OR_Q_NVFP4 = 3 };
+
 typedef struct {
   char *name;       /* output name (the index/view name) */
   uint64_t entry;   /* index entry */
@@ -925,6 +929,11 @@ typedef struct {
   int sdim;         /* sliced dimension, or -1 */
   int64_t start, stop;
   uint64_t numel;   /* elements of the output (after slicing) */
+  int qkind;        /* OR_Q_* */
+  int64_t qscale;   /* block scales tensor, or -1 */
+  int64_t qscale2;  /* NVFP4 global scale tensor, or -1 */
+  uint64_t br, bc;  /* block rows, block columns (elements) */
+  uint64_t rows, cols;  /* the output as a matrix */
 } or_output;
 
 /* Products of the dimensions before and after `dim`. */
@@ -964,12 +973,68 @@ static int ends_with(const char *s, const char *suf) {
    tensor and may only scale an fp8 tensor.  Tensors used as scales are
    consumed: they are not outputs.  Optionally keeps only part `part` of
    `nparts` (balanced by output bytes, contiguous in output order). */
-int or_select(const or_index *ix, const char *const *names, uint64_t n_names,
-              const char *const *scale_names, const char *from, const char *to, int req,
-              uint64_t part, uint64_t nparts, const int64_t *slices, or_plan **out) {
+static int is_pow2(uint64_t v) { return v != 0 && (v & (v - 1)) == 0; }
+
+/* Checks the block-scaled format of selected name i and fills its output
+   fields (reading: the formats are only named on the pages).
+     OR_Q_BLOCK_FP8: an fp8 [M, N] weight and an F32 [ceil(M/br), ceil(N/bc)]
+       scale tensor; element (i, j) is multiplied by scale (i/br, j/bc).
+       Block sizes are powers of two, bc >= 16 (0: 128).
+     OR_Q_NVFP4: a U8 [M, K] weight holding M x 2K e2m1 values (element 2c in
+       the low nibble of byte c, 2c+1 in the high nibble), an F8_E4M3
+       [M, ceil(2K/16)] tensor of block scales (16 elements along a row) and a
+       one-element F32 global scale. */
+static int check_quant(const or_index *ix, const or_entry *e, int kind, const char *qs, const char *qs2,
+                       uint64_t br, uint64_t bc, or_output *o, char *consumed) {
+  int64_t si, si2 = -1;
+  const or_entry *sc;
+  if (kind != OR_Q_BLOCK_FP8 && kind != OR_Q_NVFP4) return OR_E_INVAL;
+  if (!qs) return OR_E_INVAL;
+  si = or_find(ix, qs);
+  if (si < 0) return OR_E_NOT_FOUND;
+  sc = &ix->e[si];
+  if (e->ndim != 2) return OR_E_INVAL;
+  o->rows = (uint64_t)e->shape[0];
+  if (kind == OR_Q_BLOCK_FP8) {
+    if (br == 0) br = 128;
+    if (bc == 0) bc = 128;
+    if (!is_fp8(e->dtype) || !is_pow2(br) || !is_pow2(bc) || bc < 16) return OR_E_INVAL;
+    o->cols = (uint64_t)e->shape[1];
+    if (sc->dtype != OR_F32 || sc->ndim != 2 || (uint64_t)sc->shape[0] != (o->rows + br - 1) / br ||
+        (uint64_t)sc->shape[1] != (o->cols + bc - 1) / bc)
+      return OR_E_INVAL;
+  } else {
+    if (!((br == 0 && bc == 0) || (br == 1 && bc == 16))) return OR_E_INVAL;
+    br = 1;
+    bc = 16;
+    if (e->dtype != OR_U8 || !qs2) return OR_E_INVAL;
+    si2 = or_find(ix, qs2);
+    if (si2 < 0) return OR_E_NOT_FOUND;
+    o->cols = 2 * (uint64_t)e->shape[1];
+    if (sc->dtype != OR_F8_E4M3 || sc->ndim != 2 || (uint64_t)sc->shape[0] != o->rows ||
+        (uint64_t)sc->shape[1] != (o->cols + 15) / 16)
+      return OR_E_INVAL;
+    if (ix->e[si2].dtype != OR_F32 || ix->e[si2].numel != 1) return OR_E_INVAL;
+    consumed[si2] = 1;
+  }
+  consumed[si] = 1;
+  o->qkind = kind;
+  o->qscale = si;
+  o->qscale2 = si2;
+  o->br = br;
+  o->bc = bc;
+  o->numel = o->rows * o->cols;
+  return OR_OK;
+}
+
+int or_select_q(const or_index *ix, const char *const *names, uint64_t n_names,
+                const char *const *scale_names, const char *from, const char *to, int req,
+                uint64_t part, uint64_t nparts, const int64_t *slices, const int *qkind,
+                const char *const *qscale, const char *const *qscale2, const int64_t *qblock, or_plan **out) {
   uint64_t n = names ? n_names : ix->n, i, j, k;
   int64_t *ent = NULL, *sc = NULL;
   char *consumed = NULL;
+  or_output *qo = NULL;
   or_plan *p = NULL;
   int st = OR_OK;
   *out = NULL;
@@ -993,8 +1058,23 @@ int or_select(const or_index *ix, const char *const *names, uint64_t n_names,
     if (dim < 0) continue;
     if (dim >= e->ndim || a < 0 || a > b || b > e->shape[dim]) { st = OR_E_INVAL; goto done; }
   }
+  /* Block-scaled formats: explicit per name; not sliced, no per-tensor scale,
+     and only to a float dtype. */
+  if (qkind && !names) { st = OR_E_INVAL; goto done; }
+  qo = (or_output *)calloc(n ? n : 1, sizeof(or_output));
+  if (!qo) { st = OR_E_NOMEM; goto done; }
+  for (i = 0; qkind && i < n; i++) {
+    if (qkind[i] == OR_Q_NONE) continue;
+    if ((slices && slices[3 * i] >= 0) || (scale_names && scale_names[i])) { st = OR_E_INVAL; goto done; }
+    if (req == OR_KEEP) { st = OR_E_UNSUPPORTED_CAST; goto done; }
+    st = check_quant(ix, &ix->e[ent[i]], qkind[i], qscale ? qscale[i] : NULL, qscale2 ? qscale2[i] : NULL,
+                     qblock ? (uint64_t)qblock[2 * i] : 0, qblock ? (uint64_t)qblock[2 * i + 1] : 0, &qo[i],
+                     consumed);
+    if (st != OR_OK) goto done;
+  }
   for (i = 0; i < n; i++) {
     const or_entry *e = &ix->e[ent[i]];
+    if (qo[i].qkind != OR_Q_NONE) continue;
     if (scale_names) {
       if (scale_names[i]) {
         sc[i] = or_find(ix, scale_names[i]);
@@ -1026,12 +1106,16 @@ int or_select(const or_index *ix, const char *const *names, uint64_t n_names,
     if (consumed[ent[i]]) continue;
     od = or_out_dtype(e->dtype, req);
     if (od < 0) { st = OR_E_UNSUPPORTED_CAST; goto done; }
+    p->o[p->n] = qo[i];
     p->o[p->n].name = dupstr(e->name);
     p->o[p->n].entry = (uint64_t)ent[i];
-    p->o[p->n].out_dtype = od;
+    p->o[p->n].out_dtype = qo[i].qkind != OR_Q_NONE ? req : od;
     p->o[p->n].scale = sc[i];
     p->o[p->n].sdim = -1;
-    p->o[p->n].numel = e->numel;
+    if (qo[i].qkind == OR_Q_NONE) {
+      p->o[p->n].numel = e->numel;
+      p->o[p->n].qscale = p->o[p->n].qscale2 = -1;
+    }
     if (slices && slices[3 * i] >= 0) {
       uint64_t outer, inner;
       int dim = (int)slices[3 * i];
@@ -1068,9 +1152,21 @@ done:
   free(ent);
   free(sc);
   free(consumed);
+  free(qo);
   or_plan_free(p);
   return st;
 }
+
+int or_select(const or_index *ix, const char *const *names, uint64_t n_names,
+              const char *const *scale_names, const char *from, const char *to, int req,
+              uint64_t part, uint64_t nparts, const int64_t *slices, or_plan **out) {
+  return or_select_q(ix, names, n_names, scale_names, from, to, req, part, nparts, slices, NULL, NULL, NULL, NULL,
+                     out);
+}
+
+int or_plan_quant(const or_plan *p, uint64_t i) { return p->o[i].qkind; }
+int64_t or_plan_qscale(const or_plan *p, uint64_t i) { return p->o[i].qscale; }
+int64_t or_plan_qscale2(const or_plan *p, uint64_t i) { return p->o[i].qscale2; }
 
 uint64_t or_plan_count(const or_plan *p) { return p->n; }
 const char *or_plan_name(const or_plan *p, uint64_t i) { return p->o[i].name; }
@@ -1083,6 +1179,7 @@ uint64_t or_plan_numel(const or_plan *p, uint64_t i) { return p->o[i].numel; }
 int or_plan_ndim(const or_index *ix, const or_plan *p, uint64_t i) { return ix->e[p->o[i].entry].ndim; }
 int64_t or_plan_dim(const or_index *ix, const or_plan *p, uint64_t i, int d) {
   const or_output *o = &p->o[i];
+  if (o->qkind != OR_Q_NONE) return d == 0 ? (int64_t)o->rows : (int64_t)o->cols;
   if (d == o->sdim) return o->stop - o->start;
   return ix->e[o->entry].shape[d];
 }
@@ -1096,12 +1193,61 @@ uint64_t or_plan_bytes(const or_index *ix, const or_plan *p, uint64_t i) {
 /* Converts output elements [first, first + count) of output o (source
    element index of output element e: the row e / run of the slice, then the
    column e % run, run = (stop - start) * inner elements per row). */
+/* OCP MX E2M1 (FP4): sign, 2 exponent bits (bias 1), 1 mantissa bit; no
+   infinities or NaN. */
+static double decode_e2m1(unsigned nib) {
+  unsigned sgn = (nib >> 3) & 1, ex = (nib >> 1) & 3, m = nib & 1;
+  double v = ex == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, (int)ex - 1);
+  return sgn ? -v : v;
+}
+
+static float load_f32(const uint8_t *p) {
+  uint32_t u = (uint32_t)load_le(p, 4);
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* Output element (i, j) of a block-scaled output: the weight value times its
+   block's scale, each product one binary32 multiply (NVFP4: the block scale
+   times the global scale first, then the value times that). */
+static void convert_quant(const or_index *ix, const or_output *o, const uint8_t *data, uint64_t first,
+                          uint64_t count, uint8_t *dst) {
+  const or_entry *e = &ix->e[o->entry], *sc = &ix->e[o->qscale];
+  const int so = kSize[o->out_dtype];
+  const uint64_t scols = (uint64_t)sc->shape[1];
+  uint64_t k;
+  for (k = 0; k < count; k++) {
+    const uint64_t oe = first + k, i = oe / o->cols, j = oe % o->cols;
+    const uint64_t blk = (i / o->br) * scols + j / o->bc;
+    int nan = 0;
+    float v, s, x;
+    if (o->qkind == OR_Q_BLOCK_FP8) {
+      v = (float)decode_value(e->dtype, data[e->begin + oe], &nan);
+      s = load_f32(data + sc->begin + 4 * blk);
+    } else {
+      const uint8_t byte = data[e->begin + i * (o->cols / 2) + j / 2];
+      int snan = 0;
+      const float sb = (float)decode_e4m3(data[sc->begin + blk], &snan);
+      const float g = load_f32(data + ix->e[o->qscale2].begin);
+      v = (float)decode_e2m1((j & 1) ? (unsigned)(byte >> 4) : (unsigned)(byte & 15));
+      s = snan ? NAN : sb * g;
+    }
+    x = v * s;
+    store_le(dst + k * (uint64_t)so, encode_to(o->out_dtype, (double)x, nan || x != x), so);
+  }
+}
+
 static int convert_window(const or_index *ix, const or_output *o, const uint8_t *data, uint64_t first,
                           uint64_t count, uint8_t *dst) {
   const or_entry *e = &ix->e[o->entry];
   const int si = kSize[e->dtype], so = kSize[o->out_dtype];
   float scale = 1.0f;
   uint64_t done = 0;
+  if (o->qkind != OR_Q_NONE) {
+    convert_quant(ix, o, data, first, count, dst);
+    return OR_OK;
+  }
   if (o->scale >= 0) {
     const or_entry *s = &ix->e[o->scale];
     uint32_t u = (uint32_t)load_le(data + s->begin, 4);
