@@ -158,11 +158,34 @@ def build_workload(name, dst=None):
 
 
 def selection_of(w, ix):
-    """names/slices arguments of a workload's selection (sliced loads)."""
-    if not w.slices:
+    """names/slices/quant arguments of a workload's selection (sliced loads,
+    block-scaled weights)."""
+    if not w.slices and not w.quant:
         return {}
     names = [e["name"] for e in ix.entries()]
-    return {"names": names, "slices": [w.slices.get(n) for n in names]}
+    sel = {"names": names}
+    if w.slices:
+        sel["slices"] = [w.slices.get(n) for n in names]
+    if w.quant:
+        sel["quant"] = [w.quant.get(n) for n in names]
+    return sel
+
+
+def source_bytes(ix, infos):
+    """Algorithmic source bytes of a plan's outputs: each output's source
+    elements once (a slice reads only its elements), plus the block scales of
+    block-scaled outputs."""
+    size = {"F16": 2, "BF16": 2, "F32": 4, "F8_E4M3": 1, "F8_E5M2": 1, "I64": 8, "BOOL": 1, "U8": 1}
+    total = 0
+    for o in infos:
+        if o.get("quant") == "nvfp4":
+            total += o["numel"] // 2
+        else:
+            total += o["numel"] * size.get(o["src_dtype"], 1)
+        if o.get("quant"):
+            e = ix.entry(ix.find(o["scale"]))
+            total += e["end"] - e["begin"]
+    return total
 
 
 def host_image(w, stmat, torch):
@@ -306,8 +329,7 @@ def run_ours(args, rank, world, local):
     outs = stmat.Outputs(plan)
     infos = plan.outputs()
     dst_bytes = sum(o["bytes"] for o in infos)
-    src_bytes = sum(o["numel"] * {"F16": 2, "BF16": 2, "F32": 4, "F8_E4M3": 1, "F8_E5M2": 1, "I64": 8,
-                                  "BOOL": 1}.get(o["src_dtype"], 1) for o in infos)
+    src_bytes = source_bytes(ix, infos)
     stream = torch.cuda.current_stream()
 
     for _ in range(max(3, args.warmup)):

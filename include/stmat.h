@@ -181,6 +181,31 @@ typedef struct st_slice {
   int64_t start, stop;
 } st_slice;
 
+/* A block-scaled weight format (the resident-LLM architecture page, "Current
+ * Backend Boundary", names block-FP8 and NVFP4 checkpoints but not their
+ * layouts; these are the readings the library implements):
+ *   ST_QUANT_BLOCK_FP8: an F8_E4M3 or F8_E5M2 [M, N] weight and an F32
+ *     [ceil(M/br), ceil(N/bc)] tensor of block scales; output element (i, j)
+ *     = weight (i, j) * scale (i/br, j/bc), one binary32 multiply, rounded to
+ *     the output dtype.  br, bc powers of two, bc >= 16; 0 means 128.
+ *   ST_QUANT_NVFP4: a U8 [M, K] weight holding M x 2K OCP MX E2M1 values
+ *     (element 2c in the low nibble of byte c, 2c+1 in the high nibble), an
+ *     F8_E4M3 [M, ceil(2K/16)] tensor of scales for 16 elements of a row,
+ *     and a one-element F32 global scale; output element (i, j) = e2m1 *
+ *     (scale (i, j/16) * global), each product one binary32 multiply; the
+ *     output has shape [M, 2K].  block_rows/block_cols must be 0 (or 1/16).
+ * The output dtype must be BF16, F16 or F32; a block-scaled output takes no
+ * slice and no per-tensor scale; its scale tensors are consumed.  Plans with
+ * block-scaled outputs run the TMA kernel build. */
+typedef enum st_quant_kind { ST_QUANT_NONE = 0, ST_QUANT_BLOCK_FP8 = 2, ST_QUANT_NVFP4 = 3 } st_quant_kind;
+
+typedef struct st_block_quant {
+  int32_t kind;            /* st_quant_kind */
+  const char *scale;       /* the block-scales tensor */
+  const char *scale2;      /* ST_QUANT_NVFP4: the global scale tensor; else NULL */
+  uint32_t block_rows, block_cols;
+} st_block_quant;
+
 typedef struct st_selection {
   /* Names to materialize, in output order; NULL selects every tensor of the
    * index in index order. */
@@ -201,6 +226,9 @@ typedef struct st_selection {
   /* Optional, n_names entries (requires names): a slice per selected name.
    * Parts (above) weigh outputs by their sliced bytes. */
   const st_slice *slices;
+  /* Optional, n_names entries (requires names): a block-scaled format per
+   * selected name (kind ST_QUANT_NONE: an ordinary tensor). */
+  const st_block_quant *quant;
 } st_selection;
 /* A scale must be a one-element F32 tensor and may scale only an fp8 tensor
  * (ST_E_INVAL otherwise); scale tensors are consumed, not output.  Output
@@ -248,9 +276,10 @@ typedef struct st_output_info {
   uint64_t numel;         /* elements of the output */
   uint64_t bytes;         /* numel * itemsize(dtype) */
   uint64_t src_begin;     /* data-section offset of the source tensor */
-  const char *scale_name; /* scale tensor, or NULL */
+  const char *scale_name; /* scale tensor (block scales for a block-scaled output), or NULL */
   int32_t slice_dim;      /* the slice, or -1 */
   int64_t slice_start, slice_stop;
+  int32_t quant_kind;     /* st_quant_kind of the output */
 } st_output_info;
 
 st_status st_plan_count(const st_plan_t *plan, size_t *count);

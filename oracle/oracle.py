@@ -207,6 +207,8 @@ class OPlan:
         L = lib()
         e = self.index.entry(L.or_plan_entry(self._h, i))
         sc = L.or_plan_scale(self._h, i)
+        if L.or_plan_quant(self._h, i):
+            sc = L.or_plan_qscale(self._h, i)   # the block scales
         return {
             "name": L.or_plan_name(self._h, i).decode(),
             "entry": L.or_plan_entry(self._h, i),

@@ -30,8 +30,23 @@ enum Cls : uint32_t {
   CLS_E5M2_BF16,
   CLS_E5M2_F16,
   CLS_E5M2_F32,
+  // Block-scaled weights (a scale per block read from a second tensor):
+  // fp8 elements, and NVFP4 bytes (two e2m1 elements per counted byte).
+  CLS_QE4M3_BF16,
+  CLS_QE4M3_F16,
+  CLS_QE4M3_F32,
+  CLS_QE5M2_BF16,
+  CLS_QE5M2_F16,
+  CLS_QE5M2_F32,
+  CLS_NVFP4_BF16,
+  CLS_NVFP4_F16,
+  CLS_NVFP4_F32,
   CLS_COUNT
 };
+static_assert(CLS_COUNT <= 32, "classes fit kClsBits");
+
+ST_HD constexpr bool cls_quant(uint32_t c) { return c >= CLS_QE4M3_BF16 && c < CLS_COUNT; }
+ST_HD constexpr bool cls_nvfp4(uint32_t c) { return c >= CLS_NVFP4_BF16 && c < CLS_COUNT; }
 
 // `rows` runs of `count` elements of one output: the unit a warp processes.
 // Run r reads from data + src + r * pitch and writes to the output at
@@ -58,6 +73,17 @@ constexpr int kWarpsPerBlock = 8;
 constexpr uint32_t kErrBadDst = 1u;
 constexpr uint32_t kErrTimeout = 2u;
 
+// Block scales of a block-scaled output (device table indexed by output).
+struct alignas(16) QuantInfo {
+  uint64_t scale;      // data-section offset of the block-scales tensor
+  uint64_t scale2;     // NVFP4: data-section offset of the F32 global scale; else kNoScale
+  uint32_t row_units;  // counted units per weight row (N elements, or K bytes for NVFP4)
+  uint32_t scols;      // scale tensor columns
+  uint32_t br_shift;   // log2 block rows
+  uint32_t bc_shift;   // log2 block columns, in elements
+};
+static_assert(sizeof(QuantInfo) == 32, "quant layout");
+
 struct LaunchArgs {
   const uint8_t *data;     // data section on the device
   uint64_t data_bytes;
@@ -67,17 +93,23 @@ struct LaunchArgs {
   void *const *dst;        // device array: output index -> destination
   const float *scales;     // device array of per-output scales, or nullptr
   uint32_t *err;           // device error word
+  const QuantInfo *quant;  // device array indexed by output (block-scaled outputs), or nullptr
 };
 
-// Output itemsize of a class (bytes written per counted unit).
+// Bytes written per counted unit of a class.
 ST_HD constexpr int cls_out_size(uint32_t c) {
   switch (c) {
     case CLS_COPY: return 1;
     case CLS_F32_BF16: case CLS_F32_F16: case CLS_F16_BF16: case CLS_BF16_F16:
-    case CLS_E4M3_BF16: case CLS_E4M3_F16: case CLS_E5M2_BF16: case CLS_E5M2_F16: return 2;
+    case CLS_E4M3_BF16: case CLS_E4M3_F16: case CLS_E5M2_BF16: case CLS_E5M2_F16:
+    case CLS_QE4M3_BF16: case CLS_QE4M3_F16: case CLS_QE5M2_BF16: case CLS_QE5M2_F16: return 2;
+    case CLS_NVFP4_F32: return 8;
     default: return 4;
   }
 }
+
+// Itemsize of a class's output dtype (the alignment its destination needs).
+ST_HD constexpr int cls_out_item(uint32_t c) { return cls_nvfp4(c) ? cls_out_size(c) / 2 : cls_out_size(c); }
 
 // Source itemsize of a class (bytes read per counted unit).
 ST_HD constexpr int cls_in_size(uint32_t c) {
@@ -89,19 +121,20 @@ ST_HD constexpr int cls_in_size(uint32_t c) {
   }
 }
 
-// log2 of the two itemsizes, packed two bits per class, for shift-only address
-// arithmetic in the kernels.
-constexpr uint32_t pack_shifts(bool out) {
-  uint32_t v = 0;
+// log2 of the two sizes per counted unit (0..3), packed two bits per class,
+// for shift-only address arithmetic in the kernels.
+constexpr uint64_t pack_shifts(bool out) {
+  uint64_t v = 0;
   for (uint32_t c = 0; c < CLS_COUNT; ++c) {
     const int size = out ? cls_out_size(c) : cls_in_size(c);
-    v |= static_cast<uint32_t>(size == 4 ? 2 : size == 2 ? 1 : 0) << (2 * c);
+    v |= static_cast<uint64_t>(size == 8 ? 3 : size == 4 ? 2 : size == 2 ? 1 : 0) << (2 * c);
   }
   return v;
 }
-constexpr uint32_t kInShifts = pack_shifts(false), kOutShifts = pack_shifts(true);
-ST_HD constexpr uint32_t cls_in_shift(uint32_t c) { return (kInShifts >> (2 * c)) & 3u; }
-ST_HD constexpr uint32_t cls_out_shift(uint32_t c) { return (kOutShifts >> (2 * c)) & 3u; }
+static_assert(2 * CLS_COUNT <= 64, "shift tables fit 64 bits");
+constexpr uint64_t kInShifts = pack_shifts(false), kOutShifts = pack_shifts(true);
+ST_HD constexpr uint32_t cls_in_shift(uint32_t c) { return static_cast<uint32_t>(kInShifts >> (2 * c)) & 3u; }
+ST_HD constexpr uint32_t cls_out_shift(uint32_t c) { return static_cast<uint32_t>(kOutShifts >> (2 * c)) & 3u; }
 
 // Kernel builds (st_kernels.cu): deep unroll for large tensors, higher
 // occupancy for many small tensors, or source bytes staged in shared memory

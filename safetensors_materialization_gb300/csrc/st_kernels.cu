@@ -257,8 +257,14 @@ __device__ __forceinline__ void realign(const uint32_t (&a)[N], const uint32_t (
 
 template <int NW>
 __device__ __forceinline__ void store_out(uint8_t *p, const uint32_t (&o)[NW]) {
-  if constexpr (NW == 2) *reinterpret_cast<uint2 *>(p) = make_uint2(o[0], o[1]);
-  else *reinterpret_cast<uint4 *>(p) = make_uint4(o[0], o[1], o[2], o[3]);
+  if constexpr (NW == 2) {
+    *reinterpret_cast<uint2 *>(p) = make_uint2(o[0], o[1]);
+  } else if constexpr (NW == 4) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(o[0], o[1], o[2], o[3]);
+  } else {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(p + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
 }
 
 template <class CV, bool kMis>
@@ -550,12 +556,24 @@ struct SegMeta {
   uint32_t len;         // elements (bytes for CLS_COPY)
   uint32_t a, z;
   uint32_t off;         // slot offset of element a
-  float scale;
+  float scale;          // per-tensor scale (fp8), or the NVFP4 global scale
   uint32_t cls;
+  // Block-scaled segments: the scale of the block holding element column
+  // col0 is at sptr (the slot's scale area, or the data section itself when
+  // the scales sit at an unaligned end of it); blocks are 1 << bcs columns.
+  const uint8_t *sptr;
+  uint32_t col0, bcs;
 };
+
+// A segment of a block-scaled weight brings at most this many bytes of block
+// scales (the producer shortens the segment to fit), fetched with the
+// segment into the slot's scale area.
+constexpr uint32_t kScalePayload = 128;
+constexpr uint32_t kScaleBytes = kScalePayload + 32;
 
 struct alignas(128) WarpSmem {
   uint8_t buf[kSlots][kSlotBytes];
+  uint8_t sbuf[kSlots][kScaleBytes];
   Piece desc[2][32];
   uint8_t *dstp[2][32];
   float scl[2][32];
@@ -563,6 +581,7 @@ struct alignas(128) WarpSmem {
   uint64_t bar[kSlots];
   uint64_t dbar[2];
 };
+static_assert(offsetof(WarpSmem, sbuf) % 16 == 0 && kScaleBytes % 16 == 0, "scale bulk-copy destinations");
 static_assert(offsetof(WarpSmem, desc) % 16 == 0 && kSlotBytes % 16 == 0, "bulk-copy destinations");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -580,6 +599,19 @@ __device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t
     return;
   }
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+// Lane 0: one arrival expecting `bytes`, then the copies that deliver them.
+__device__ __forceinline__ void mbar_expect(uint64_t *bar, uint32_t bytes) {
+  if (bytes == 0) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+    return;
+  }
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_copy(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(smem_u32(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
@@ -665,6 +697,126 @@ __device__ __forceinline__ void consume_seg(const uint8_t *buf, const SegMeta &m
   }
 }
 
+// ----------------------------------------------------- block-scaled weights
+
+constexpr int S_NV = 100;  // NVFP4 source marker for QConv
+
+// OCP MX E2M1: magnitudes x 2 of codes 0..7 are 0, 1, 2, 3, 4, 6, 8, 12
+// (nibbles of 0xC8643210); the sign is bit 3.  Exact in binary32.
+__device__ __forceinline__ float e2m1_value(uint32_t nib) {
+  const float mag = static_cast<float>((0xC8643210u >> ((nib & 7u) * 4u)) & 15u) * 0.5f;
+  return __uint_as_float(__float_as_uint(mag) | ((nib & 8u) << 28));
+}
+
+// The scale of element column `col` of a block-scaled segment: F32 block
+// scales (block FP8), or E4M3 block scale times the global scale (NVFP4).
+template <bool kNv>
+__device__ __forceinline__ float block_scale(const SegMeta &m, uint32_t col) {
+  const uint32_t blk = (col >> m.bcs) - (m.col0 >> m.bcs);
+  if constexpr (kNv) {
+    const float sb = decode1<S_E4M3>(m.sptr[blk]);
+    return __fmul_rn(sb, m.scale);
+  } else {
+    const uint8_t *p = m.sptr + 4 * blk;  // any alignment
+    return __uint_as_float(static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) |
+                           (static_cast<uint32_t>(p[2]) << 16) | (static_cast<uint32_t>(p[3]) << 24));
+  }
+}
+
+// A block-scaled class: counted units are bytes (an fp8 element, or two
+// NVFP4 elements); a lane step reads SB bytes and writes one 16-byte vector
+// (two for NVFP4 to F32).
+template <int S, int D>
+struct QConv {
+  static constexpr bool kNv = S == S_NV;
+  static constexpr int EPU = kNv ? 2 : 1;             // elements per unit
+  static constexpr int ES = DstInfo<D>::kSize;        // output element size
+  static constexpr int SO = EPU * ES;
+  static constexpr int SB = kNv ? 4 : (ES == 4 ? 4 : 8);
+  static constexpr int KS = SB, OS = KS * SO, KE = KS * EPU;
+
+  __device__ static float value(uint32_t byte, int k) {  // element k (0 or 1) of a unit
+    if constexpr (kNv) return e2m1_value(k ? byte >> 4 : byte & 15u);
+    else return decode1<S>(byte);
+  }
+  // One unit at p (any memory) to q; e = its unit index in the segment.
+  __device__ static void one(const uint8_t *p, uint8_t *q, uint32_t e, const SegMeta &m) {
+    const uint32_t byte = *p;
+#pragma unroll
+    for (int k = 0; k < EPU; ++k) {
+      const float x = __fmul_rn(value(byte, k), block_scale<kNv>(m, m.col0 + e * EPU + k));
+      const uint32_t y = encode1<D>(x);
+      if constexpr (ES == 2) reinterpret_cast<uint16_t *>(q)[k] = static_cast<uint16_t>(y);
+      else reinterpret_cast<uint32_t *>(q)[k] = y;
+    }
+  }
+  // KE elements from the step's words; elements [0, kb) take scale lo, the
+  // rest hi (a step crosses at most one block boundary: blocks hold >= 16).
+  __device__ static void step(const uint32_t (&w)[SB / 4], float lo, float hi, uint32_t kb,
+                              uint32_t (&o)[OS / 4]) {
+#pragma unroll
+    for (int k = 0; k < KE; k += 2) {
+      const uint32_t b0 = (w[(k / EPU) >> 2] >> (8 * ((k / EPU) & 3))) & 0xFFu;
+      const uint32_t b1 = (w[((k + 1) / EPU) >> 2] >> (8 * (((k + 1) / EPU) & 3))) & 0xFFu;
+      float2 f;
+      f.x = __fmul_rn(value(b0, k % EPU), static_cast<uint32_t>(k) < kb ? lo : hi);
+      f.y = __fmul_rn(value(b1, (k + 1) % EPU), static_cast<uint32_t>(k + 1) < kb ? lo : hi);
+      if constexpr (D == D_F32) {
+        o[k] = encode1<D_F32>(f.x);
+        o[k + 1] = encode1<D_F32>(f.y);
+      } else {
+        o[k / 2] = encode2_16<D>(f);
+      }
+    }
+  }
+};
+
+template <class QV>
+__device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta &m, uint32_t lane) {
+  constexpr int SO = QV::SO, SB = QV::SB, KS = QV::KS, OS = QV::OS, N = SB / 4, EPU = QV::EPU;
+  uint8_t *const dst = m.dst;
+  const uint32_t len = m.len, off = m.off, a = m.a, z = m.z;
+  const uint32_t edge = a + (len - z);
+  for (uint32_t t = lane; t < edge; t += 32) {
+    const uint32_t e = t < a ? t : z + (t - a);
+    QV::one(m.gsrc + e, dst + static_cast<uint64_t>(e) * SO, e, m);
+  }
+  const uint32_t n = z - a;
+  const uint8_t *sp = buf + off;
+  uint8_t *dp = dst + static_cast<uint64_t>(a) * SO;
+  uint32_t h = static_cast<uint32_t>(((OS - (reinterpret_cast<uintptr_t>(dp) & (OS - 1))) & (OS - 1)) / SO);
+  if (h > n) h = n;
+  const uint32_t nst = (n - h) / KS, t0 = h + nst * KS;
+  const uint32_t ends = h + (n - t0);
+  for (uint32_t t = lane; t < ends; t += 32) {
+    const uint32_t e = t < h ? t : t0 + (t - h);
+    QV::one(sp + e, dp + e * SO, a + e, m);
+  }
+  const uint32_t q = off + h, r = q & (SB - 1);
+  const uint8_t *wb = buf + (q - r);
+  uint8_t *db = dp + h * SO;
+  const uint32_t bc = 1u << m.bcs;
+  for (uint32_t c = lane; c < nst; c += 32) {
+    uint32_t x[N], sv[N];
+    lds<N>(wb + c * SB, x);
+    if (r) {
+      uint32_t y[N];
+      lds<N>(wb + (c + 1) * SB, y);
+      realign<N>(x, y, r, sv);
+    } else {
+#pragma unroll
+      for (int i = 0; i < N; ++i) sv[i] = x[i];
+    }
+    const uint32_t col = m.col0 + (a + h + c * KS) * EPU;  // column of the step's first element
+    const uint32_t kb = bc - (col & (bc - 1));
+    const float lo = block_scale<QV::kNv>(m, col);
+    const float hi = kb < static_cast<uint32_t>(QV::KE) ? block_scale<QV::kNv>(m, col + kb) : lo;
+    uint32_t o[OS / 4];
+    QV::step(sv, lo, hi, kb, o);
+    store_out<OS / 4>(db + c * OS, o);
+  }
+}
+
 __device__ __forceinline__ void consume_any(const uint8_t *buf, const SegMeta &m, uint32_t lane) {
   switch (m.cls) {
     case CLS_COPY: consume_seg<CopyBytes>(buf, m, lane); break;
@@ -680,6 +832,15 @@ __device__ __forceinline__ void consume_any(const uint8_t *buf, const SegMeta &m
     case CLS_E5M2_BF16: consume_seg<Conv<S_E5M2, D_BF16>>(buf, m, lane); break;
     case CLS_E5M2_F16: consume_seg<Conv<S_E5M2, D_F16>>(buf, m, lane); break;
     case CLS_E5M2_F32: consume_seg<Conv<S_E5M2, D_F32>>(buf, m, lane); break;
+    case CLS_QE4M3_BF16: consume_quant<QConv<S_E4M3, D_BF16>>(buf, m, lane); break;
+    case CLS_QE4M3_F16: consume_quant<QConv<S_E4M3, D_F16>>(buf, m, lane); break;
+    case CLS_QE4M3_F32: consume_quant<QConv<S_E4M3, D_F32>>(buf, m, lane); break;
+    case CLS_QE5M2_BF16: consume_quant<QConv<S_E5M2, D_BF16>>(buf, m, lane); break;
+    case CLS_QE5M2_F16: consume_quant<QConv<S_E5M2, D_F16>>(buf, m, lane); break;
+    case CLS_QE5M2_F32: consume_quant<QConv<S_E5M2, D_F32>>(buf, m, lane); break;
+    case CLS_NVFP4_BF16: consume_quant<QConv<S_NV, D_BF16>>(buf, m, lane); break;
+    case CLS_NVFP4_F16: consume_quant<QConv<S_NV, D_F16>>(buf, m, lane); break;
+    case CLS_NVFP4_F32: consume_quant<QConv<S_NV, D_F32>>(buf, m, lane); break;
     default: break;
   }
 }
@@ -727,12 +888,14 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
       const uint32_t out = pc.out_cls >> kClsBits, cls = pc.out_cls & ((1u << kClsBits) - 1);
       uint8_t *d = static_cast<uint8_t *>(a.dst[out]);
       float scale = 1.0f;
-      if (cls >= CLS_E4M3_BF16) {
+      if (cls_nvfp4(cls)) {
+        scale = load_f32_le(a.data + a.quant[out].scale2);  // the global scale
+      } else if (cls >= CLS_E4M3_BF16 && !cls_quant(cls)) {
         if (a.scales) scale = a.scales[out];
         else if (pc.scale != kNoScale) scale = load_f32_le(a.data + pc.scale);
       }
       if (d == nullptr || cls >= CLS_COUNT ||
-          (reinterpret_cast<uintptr_t>(d) & static_cast<uintptr_t>(cls_out_size(cls) - 1))) {
+          (reinterpret_cast<uintptr_t>(d) & static_cast<uintptr_t>(cls_out_item(cls) - 1))) {
         atomicOr(a.err, kErrBadDst);
         d = nullptr;
       }
@@ -760,6 +923,10 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
   uint32_t count = 0, rows = 0, cls = 0, sis = 0, sos = 0;
   float scale = 1.0f;
   bool loaded = false;
+  // Block-scaled pieces: the output's scale table entry and the output unit
+  // index of the piece's first unit.
+  QuantInfo qi{};
+  uint64_t unit0 = 0;
   auto load_piece_state = [&]() -> bool {  // false: skip this piece
     const Piece &pc = ws.desc[cur.b & 1][cur.i];
     uint8_t *dp = ws.dstp[cur.b & 1][cur.i];
@@ -773,6 +940,10 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
     run_src = a.data + pc.src;
     run_dst = dp + pc.dst;
     scale = ws.scl[cur.b & 1][cur.i];
+    if (cls_quant(cls)) {
+      qi = a.quant[pc.out_cls >> kClsBits];
+      unit0 = pc.dst >> sos;
+    }
     return true;
   };
   auto produce = [&](int slot) -> int {  // 1 issued, 0 done, -1 timed out
@@ -793,7 +964,37 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
         }
         loaded = true;
       }
-      const uint32_t len = min(kSeg >> sis, count - cur.e);
+      uint32_t len = min(kSeg >> sis, count - cur.e);
+      // Block-scaled: the segment stays in one weight row and its block scales
+      // fit the slot's scale area; they are fetched with it when they lie in
+      // the aligned interior of the data section (else read in place).
+      uint32_t col0 = 0, sbytes = 0;
+      const uint8_t *sptr = nullptr;
+      uintptr_t sw0 = 0;
+      if (cls_quant(cls)) {
+        const bool nv = cls_nvfp4(cls);
+        const uint64_t u = unit0 + cur.e;
+        const uint64_t row = u / qi.row_units;
+        const uint32_t colu = static_cast<uint32_t>(u - row * qi.row_units);
+        len = min(len, qi.row_units - colu);
+        col0 = nv ? 2 * colu : colu;
+        const uint32_t ss = nv ? 1 : 4;  // bytes per block scale
+        const uint32_t bc = 1u << qi.bc_shift, maxblk = kScalePayload / ss;
+        const uint32_t max_el = maxblk * bc - (col0 & (bc - 1));
+        len = min(len, nv ? max_el / 2 : max_el);
+        const uint32_t el = nv ? 2 * len : len;
+        const uint32_t b0 = col0 >> qi.bc_shift, nblk = ((col0 + el - 1) >> qi.bc_shift) - b0 + 1;
+        const uint8_t *sg = a.data + qi.scale + ((row >> qi.br_shift) * qi.scols + b0) * ss;
+        const uintptr_t g = reinterpret_cast<uintptr_t>(sg);
+        sw0 = g & ~uintptr_t(15);
+        const uintptr_t sw1 = (g + nblk * ss + 15) & ~uintptr_t(15);
+        if (sw0 >= lo16 && sw1 <= hi16) {
+          sbytes = static_cast<uint32_t>(sw1 - sw0);
+          sptr = ws.sbuf[slot] + (g - sw0);
+        } else {
+          sptr = sg;
+        }
+      }
       const uint8_t *s0 = run_src + (static_cast<uint64_t>(cur.e) << sis);
       const uintptr_t s = reinterpret_cast<uintptr_t>(s0);
       const uintptr_t send = s + (static_cast<uint64_t>(len) << sis);
@@ -819,8 +1020,13 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
         m.off = off;
         m.scale = scale;
         m.cls = cls;
+        m.sptr = sptr;
+        m.col0 = col0;
+        m.bcs = qi.bc_shift;
         proxy_fence();
-        bulk_load(ws.buf[slot], reinterpret_cast<const void *>(w0), bytes, &ws.bar[slot]);
+        mbar_expect(&ws.bar[slot], bytes + sbytes);
+        if (bytes) bulk_copy(ws.buf[slot], reinterpret_cast<const void *>(w0), bytes, &ws.bar[slot]);
+        if (sbytes) bulk_copy(ws.sbuf[slot], reinterpret_cast<const void *>(sw0), sbytes, &ws.bar[slot]);
       }
       cur.e += len;
       if (cur.e == count) {

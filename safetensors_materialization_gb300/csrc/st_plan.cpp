@@ -88,6 +88,10 @@ struct Output {
   std::vector<int64_t> shape;  // output shape
   int32_t sdim = -1;   // slice
   int64_t start = 0, stop = 0;
+  // Block-scaled weights: the format and its scale table entry.
+  int32_t qkind = ST_QUANT_NONE;
+  int64_t qscale_entry = -1;  // core tensor of the block scales
+  QuantInfo quant{};
   // Source geometry in counted units: `runs` runs of `run` units; run r
   // starts at data-section byte src0 + r * pitch.  One run unless an inner
   // dimension is sliced.
@@ -119,6 +123,8 @@ struct st_plan_s {
   Piece *d_pieces = nullptr;
   uint32_t *d_parts = nullptr;
   uint32_t *d_err = nullptr;
+  std::vector<QuantInfo> quant;  // per output, when any output is block-scaled
+  QuantInfo *d_quant = nullptr;
   std::vector<cudaEvent_t> events;  // one per chunk + one for st_load's start
   ~st_plan_s() {
     if (!on_device) return;
@@ -129,11 +135,78 @@ struct st_plan_s {
     cudaFree(d_pieces);
     cudaFree(d_parts);
     cudaFree(d_err);
+    cudaFree(d_quant);
     if (cur != device && cur >= 0) cudaSetDevice(cur);
   }
 };
 
 namespace {
+
+uint32_t log2_of(uint64_t v) {
+  uint32_t k = 0;
+  while ((1ull << k) < v) ++k;
+  return k;
+}
+
+// Checks selected name `p` against its block-scaled format (see st_block_quant)
+// and fills the output's format fields; marks the scale tensors consumed.
+st_status check_quant(const IndexData &ix, uint32_t p, const st_block_quant &q, Output *o,
+                      std::vector<char> *consumed) {
+  const Core &core = *ix.core;
+  const Tensor &t = core.tensors[ix.ent[p]];
+  const char *nm = ix.names[p];
+  if (q.kind != ST_QUANT_BLOCK_FP8 && q.kind != ST_QUANT_NVFP4)
+    return set_error(ST_E_INVAL, "\"%s\": unknown block-scaled format %d", nm, q.kind);
+  if (!q.scale) return set_error(ST_E_INVAL, "\"%s\": no block-scales tensor named", nm);
+  auto it = ix.pos.find(std::string_view(q.scale));
+  if (it == ix.pos.end()) return set_error(ST_E_NOT_FOUND, "no block-scales tensor named \"%s\"", q.scale);
+  const uint32_t sp = it->second;
+  const Tensor &sc = core.tensors[ix.ent[sp]];
+  if (t.shape.size() != 2) return set_error(ST_E_INVAL, "\"%s\": a block-scaled weight is 2-D", nm);
+  const uint64_t M = static_cast<uint64_t>(t.shape[0]);
+  uint64_t br = q.block_rows, bc = q.block_cols, N;
+  o->quant.scale2 = kNoScale;
+  if (q.kind == ST_QUANT_BLOCK_FP8) {
+    if (br == 0) br = 128;
+    if (bc == 0) bc = 128;
+    N = static_cast<uint64_t>(t.shape[1]);
+    if (!is_fp8(t.dtype) || (br & (br - 1)) || (bc & (bc - 1)) || bc < 16 || br > (1u << 30) || bc > (1u << 30))
+      return set_error(ST_E_INVAL, "\"%s\": block FP8 needs an fp8 weight and power-of-two blocks, >= 16 columns", nm);
+    if (sc.dtype != ST_F32 || sc.shape.size() != 2 || static_cast<uint64_t>(sc.shape[0]) != (M + br - 1) / br ||
+        static_cast<uint64_t>(sc.shape[1]) != (N + bc - 1) / bc)
+      return set_error(ST_E_INVAL, "\"%s\": block scales must be F32 [ceil(M/%llu), ceil(N/%llu)]", q.scale,
+                       static_cast<unsigned long long>(br), static_cast<unsigned long long>(bc));
+    o->quant.row_units = static_cast<uint32_t>(N);
+  } else {
+    if (!((br == 0 && bc == 0) || (br == 1 && bc == 16)))
+      return set_error(ST_E_INVAL, "\"%s\": NVFP4 blocks are 1 x 16", nm);
+    br = 1;
+    bc = 16;
+    if (t.dtype != ST_U8 || !q.scale2)
+      return set_error(ST_E_INVAL, "\"%s\": NVFP4 needs a U8 weight and a global scale", nm);
+    auto it2 = ix.pos.find(std::string_view(q.scale2));
+    if (it2 == ix.pos.end()) return set_error(ST_E_NOT_FOUND, "no global scale tensor named \"%s\"", q.scale2);
+    N = 2 * static_cast<uint64_t>(t.shape[1]);
+    if (sc.dtype != ST_F8_E4M3 || sc.shape.size() != 2 || static_cast<uint64_t>(sc.shape[0]) != M ||
+        static_cast<uint64_t>(sc.shape[1]) != (N + 15) / 16)
+      return set_error(ST_E_INVAL, "\"%s\": NVFP4 scales must be F8_E4M3 [M, ceil(2K/16)]", q.scale);
+    const Tensor &g = core.tensors[ix.ent[it2->second]];
+    if (g.dtype != ST_F32 || g.numel != 1)
+      return set_error(ST_E_INVAL, "\"%s\": the global scale is a one-element F32 tensor", q.scale2);
+    (*consumed)[it2->second] = 1;
+    o->quant.scale2 = g.begin;
+    o->quant.row_units = static_cast<uint32_t>(t.shape[1]);
+  }
+  if (N > (1u << 30)) return set_error(ST_E_INVAL, "\"%s\": a block-scaled row holds at most 2^30 elements", nm);
+  (*consumed)[sp] = 1;
+  o->qkind = q.kind;
+  o->qscale_entry = ix.ent[sp];
+  o->quant.scale = sc.begin;
+  o->quant.scols = static_cast<uint32_t>(sc.shape[1]);
+  o->quant.br_shift = log2_of(br);
+  o->quant.bc_shift = log2_of(bc);
+  return ST_OK;
+}
 
 // Selection -> outputs (order, dtype, scale), with the part filter.
 st_status select_outputs(const IndexData &ix, const st_selection *sel, int req, std::vector<Output> *outs) {
@@ -172,15 +245,30 @@ st_status select_outputs(const IndexData &ix, const st_selection *sel, int req, 
       return set_error(ST_E_INVAL, "slice (dim %d, %lld..%lld) does not fit \"%s\"", sl.dim,
                        static_cast<long long>(sl.start), static_cast<long long>(sl.stop), ix.names[pos[i]]);
   }
+  std::vector<char> consumed(ix.ent.size(), 0);
+  // Block-scaled formats (explicit, per name).
+  const st_block_quant *quant = sel ? sel->quant : nullptr;
+  if (quant && all) return set_error(ST_E_INVAL, "quant needs names");
+  std::vector<Output> qout(n);
+  for (size_t i = 0; quant && i < n; ++i) {
+    const st_block_quant &q = quant[i];
+    if (q.kind == ST_QUANT_NONE) continue;
+    const char *nm = ix.names[pos[i]];
+    if ((slices && slices[i].dim >= 0) || (sel->scale_names && sel->scale_names[i]))
+      return set_error(ST_E_INVAL, "\"%s\": a block-scaled output takes no slice and no per-tensor scale", nm);
+    if (req == ST_KEEP) return set_error(ST_E_UNSUPPORTED_CAST, "KEEP cannot apply block scales");
+    st_status st = check_quant(ix, pos[i], q, &qout[i], &consumed);
+    if (st != ST_OK) return st;
+  }
   // Scale pairing.
   std::vector<int64_t> scale(n, -1);  // position of the scale in the view
-  std::vector<char> consumed(ix.ent.size(), 0);
   const char *from = sel ? sel->scale_suffix_from : nullptr;
   const char *to = sel ? sel->scale_suffix_to : nullptr;
   const size_t flen = from ? strlen(from) : 0;
   std::string cand;
   for (size_t i = 0; i < n; ++i) {
     const Tensor &t = core.tensors[ix.ent[pos[i]]];
+    if (qout[i].qkind != ST_QUANT_NONE) continue;
     if (sel && sel->scale_names) {
       const char *sn = sel->scale_names[i];
       if (sn) {
@@ -209,6 +297,23 @@ st_status select_outputs(const IndexData &ix, const st_selection *sel, int req, 
   for (size_t i = 0; i < n; ++i) {
     if (consumed[pos[i]]) continue;
     const Tensor &t = core.tensors[ix.ent[pos[i]]];
+    if (qout[i].qkind != ST_QUANT_NONE) {
+      Output o = std::move(qout[i]);
+      o.name = ix.names[pos[i]];
+      o.pos = pos[i];
+      o.entry = ix.ent[pos[i]];
+      o.out_dtype = req;
+      const bool nv = o.qkind == ST_QUANT_NVFP4;
+      const uint32_t base = nv ? CLS_NVFP4_BF16 : t.dtype == ST_F8_E4M3 ? CLS_QE4M3_BF16 : CLS_QE5M2_BF16;
+      o.cls = base + (req == ST_BF16 ? 0 : req == ST_F16 ? 1 : 2);
+      o.shape = {t.shape[0], nv ? 2 * t.shape[1] : t.shape[1]};
+      o.numel = static_cast<uint64_t>(o.shape[0]) * static_cast<uint64_t>(o.shape[1]);
+      o.src0 = t.begin;
+      o.units = t.numel;  // elements, or NVFP4 bytes
+      o.run = o.units;
+      outs->push_back(std::move(o));
+      continue;
+    }
     int od = out_dtype_of(t.dtype, req);
     if (od < 0)
       return set_error(ST_E_UNSUPPORTED_CAST, "\"%s\": %s cannot be materialized as %s", ix.names[pos[i]],
@@ -395,6 +500,11 @@ void build_pieces(st_plan_s *p) {
       continue;
     }
     uint64_t scale_chunk = o.scale >= 0 ? (core.tensors[o.scale].end - 1) / C : 0;
+    if (o.qkind != ST_QUANT_NONE) {  // all of the block scales (and the global scale) staged first
+      const Tensor &qs = core.tensors[o.qscale_entry];
+      if (qs.end > qs.begin) scale_chunk = std::max(scale_chunk, (qs.end - 1) / C);
+      if (o.quant.scale2 != kNoScale) scale_chunk = std::max(scale_chunk, (o.quant.scale2 + 3) / C);
+    }
     if (o.runs > 1) {
       // Whole runs go to the chunk holding their last byte.
       uint64_t r0 = 0, k0 = 0;
@@ -496,10 +606,18 @@ st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst
     } else {
       p->kernel = nonempty && traffic / nonempty < kSmallOutputBytes ? kKernelTma : kKernelStream;
     }
+    // Block-scaled outputs are only in the TMA build.
+    bool has_quant = false;
+    for (const Output &o : p->outs) has_quant = has_quant || o.qkind != ST_QUANT_NONE;
+    if (has_quant) {
+      if (opts && opts->kernel && opts->kernel != kKernelTma)
+        return set_error(ST_E_INVAL, "block-scaled outputs need the TMA build (options.kernel 0 or 3)");
+      p->kernel = kKernelTma;
+    }
     // Unit order: the register builds run one class at a time (their
     // per-class code is large, and mixing classes stalls on instruction
-    // fetch); the TMA build's code is small, and source order lets adjacent
-    // small tensors share one bulk copy.
+    // fetch); the TMA build's code is small, and source order keeps DRAM
+    // rows local.
     p->class_major = order == 2 || (order == 0 && p->kernel != kKernelTma);
     int sms = 0, blocks = 0;
     if (!host_only || workers == 0) {
@@ -515,6 +633,10 @@ st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst
     uint64_t cap = std::max<uint64_t>(1, cost / kMinWorkerCost);
     p->workers = static_cast<uint32_t>(std::min<uint64_t>(workers, cap));
     build_pieces(p.get());
+    if (has_quant) {
+      p->quant.resize(p->outs.size());
+      for (size_t i = 0; i < p->outs.size(); ++i) p->quant[i] = p->outs[i].quant;
+    }
     if (!host_only) {
       cudaError_t e = cudaGetDevice(&p->device);
       size_t pb = p->pieces.size() * sizeof(Piece), qb = p->parts.size() * sizeof(uint32_t);
@@ -525,6 +647,11 @@ st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst
       if (e == cudaSuccess && pb) e = cudaMemcpy(p->d_pieces, p->pieces.data(), pb, cudaMemcpyHostToDevice);
       if (e == cudaSuccess) e = cudaMemcpy(p->d_parts, p->parts.data(), qb, cudaMemcpyHostToDevice);
       if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(uint32_t));
+      if (e == cudaSuccess && !p->quant.empty()) {
+        const size_t bytes = p->quant.size() * sizeof(QuantInfo);
+        e = cudaMalloc(reinterpret_cast<void **>(&p->d_quant), bytes);
+        if (e == cudaSuccess) e = cudaMemcpy(p->d_quant, p->quant.data(), bytes, cudaMemcpyHostToDevice);
+      }
       for (uint32_t k = 0; e == cudaSuccess && k <= p->n_chunks; ++k) {
         cudaEvent_t ev;
         e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
@@ -561,10 +688,12 @@ st_status st_plan_output(const st_plan_t *p, size_t i, st_output_info *info) {
   info->numel = o.numel;
   info->bytes = o.numel * dtype_size(o.out_dtype);
   info->src_begin = t.begin;
-  info->scale_name = o.scale >= 0 ? p->index->core->tensors[o.scale].name.c_str() : nullptr;
+  const int64_t sc = o.qkind != ST_QUANT_NONE ? o.qscale_entry : o.scale;
+  info->scale_name = sc >= 0 ? p->index->core->tensors[sc].name.c_str() : nullptr;
   info->slice_dim = o.sdim;
   info->slice_start = o.start;
   info->slice_stop = o.stop;
+  info->quant_kind = o.qkind;
   return ST_OK;
 }
 
@@ -657,6 +786,7 @@ st_status launch_chunk(const st_plan_t *p, uint32_t k, const void *data_dev, voi
   a.dst = dst;
   a.scales = scales;
   a.err = p->d_err;
+  a.quant = p->d_quant;
   return launch_materialize(a, p->kernel, stream);
 }
 
@@ -741,11 +871,13 @@ st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *p, void 
   if (!data_dev || !dst_ptrs) return set_error(ST_E_INVAL, "NULL data or destination array");
   st_status s = check_tma_source(p, data_dev);
   if (s != ST_OK) return s;
-  // Layout inside the static array: pieces | warp ranges | error word.
+  // Layout inside the static array: pieces | warp ranges | block-scale table | error word.
   const size_t pieces_bytes = p->pieces.size() * sizeof(Piece);
   const size_t parts_off = (pieces_bytes + 255) & ~size_t(255);
   const size_t parts_bytes = p->parts.size() * sizeof(uint32_t);
-  const size_t err_off = (parts_off + parts_bytes + 255) & ~size_t(255);
+  const size_t quant_off = (parts_off + parts_bytes + 255) & ~size_t(255);
+  const size_t quant_bytes = p->quant.size() * sizeof(QuantInfo);
+  const size_t err_off = (quant_off + quant_bytes + 255) & ~size_t(255);
   const size_t need = err_off + sizeof(uint32_t);
   if (need > kStaticScratchBytes)
     return set_error(ST_E_INVAL,
@@ -759,6 +891,8 @@ st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *p, void 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(base, p->pieces.data(), pieces_bytes, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(base + parts_off, p->parts.data(), parts_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && quant_bytes)
+    e = cudaMemcpyAsync(base + quant_off, p->quant.data(), quant_bytes, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(base + err_off, 0, sizeof(uint32_t), st);  // left over from the last call
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "filling the static scratch: %s", cuda_msg(e).c_str());
   for (uint32_t k = 0; k < p->n_chunks; ++k) {
@@ -773,6 +907,7 @@ st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *p, void 
     a.dst = dst_ptrs;
     a.scales = scales;
     a.err = reinterpret_cast<uint32_t *>(base + err_off);
+    a.quant = quant_bytes ? reinterpret_cast<const QuantInfo *>(base + quant_off) : nullptr;
     s = launch_materialize(a, p->kernel, stream);
     if (s != ST_OK) return s;
   }

@@ -53,18 +53,26 @@ class OutputInfo(C.Structure):
     _fields_ = [("name", C.c_char_p), ("dtype", C.c_int), ("src_dtype", C.c_int), ("ndim", C.c_int32),
                 ("shape", C.POINTER(C.c_int64)), ("numel", C.c_uint64), ("bytes", C.c_uint64),
                 ("src_begin", C.c_uint64), ("scale_name", C.c_char_p), ("slice_dim", C.c_int32),
-                ("slice_start", C.c_int64), ("slice_stop", C.c_int64)]
+                ("slice_start", C.c_int64), ("slice_stop", C.c_int64), ("quant_kind", C.c_int32)]
 
 
 class Slice(C.Structure):
     _fields_ = [("dim", C.c_int32), ("start", C.c_int64), ("stop", C.c_int64)]
 
 
+class BlockQuant(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("scale", C.c_char_p), ("scale2", C.c_char_p),
+                ("block_rows", C.c_uint32), ("block_cols", C.c_uint32)]
+
+
+QUANT_KINDS = {"block_fp8": 2, "nvfp4": 3}
+
+
 class Selection(C.Structure):
     _fields_ = [("names", C.POINTER(C.c_char_p)), ("n_names", C.c_size_t),
                 ("scale_names", C.POINTER(C.c_char_p)), ("scale_suffix_from", C.c_char_p),
                 ("scale_suffix_to", C.c_char_p), ("part", C.c_uint32), ("n_parts", C.c_uint32),
-                ("slices", C.POINTER(Slice))]
+                ("slices", C.POINTER(Slice)), ("quant", C.POINTER(BlockQuant))]
 
 
 class PlanOptions(C.Structure):
@@ -274,8 +282,10 @@ class Index:
 
     def plan(self, dst="BF16", names=None, scale_names=None, scale_suffix=None, part=0, n_parts=0,
              workers=0, chunk_bytes=0, host_only=False, blocks_per_sm=0, unit_bytes=0, kernel=0, order=0,
-             slices=None):
-        """st_plan: outputs and device work for a selection."""
+             slices=None, quant=None):
+        """st_plan: outputs and device work for a selection.  quant: per name
+        None or (kind, block-scales name, global-scale name or None,
+        (block rows, block cols) or None), kind "block_fp8" or "nvfp4"."""
         sel = Selection()
         keep = []
         if names is not None:
@@ -295,6 +305,15 @@ class Index:
                 arr[i] = Slice(*(x if x is not None else (-1, 0, 0)))
             keep.append(arr)
             sel.slices = C.cast(arr, C.POINTER(Slice))
+        if quant is not None:
+            arr = (BlockQuant * max(1, len(quant)))()
+            for i, q in enumerate(quant):
+                if q:
+                    br, bc = q[3] if len(q) > 3 and q[3] else (0, 0)
+                    arr[i] = BlockQuant(QUANT_KINDS.get(q[0], 99), q[1].encode() if q[1] else None,
+                                        q[2].encode() if q[2] else None, br, bc)
+            keep.append(arr)
+            sel.quant = C.cast(arr, C.POINTER(BlockQuant))
         opts = PlanOptions(workers, chunk_bytes, 1 if host_only else 0, blocks_per_sm, unit_bytes, kernel, order)
         out = C.c_void_p()
         _check(lib().st_plan(self._h, C.byref(sel), DTYPES.index(dst), C.byref(opts), C.byref(out)))
@@ -328,7 +347,8 @@ class Plan:
         return {"name": o.name.decode(), "dtype": DTYPES[o.dtype], "src_dtype": DTYPES[o.src_dtype],
                 "shape": [o.shape[d] for d in range(o.ndim)], "numel": o.numel, "bytes": o.bytes,
                 "begin": o.src_begin, "scale": o.scale_name.decode() if o.scale_name else None,
-                "slice": None if o.slice_dim < 0 else (o.slice_dim, o.slice_start, o.slice_stop)}
+                "slice": None if o.slice_dim < 0 else (o.slice_dim, o.slice_start, o.slice_stop),
+                "quant": {2: "block_fp8", 3: "nvfp4"}.get(o.quant_kind)}
 
     def outputs(self):
         return [self.output(i) for i in range(len(self))]

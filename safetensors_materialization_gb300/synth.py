@@ -175,6 +175,7 @@ class Workload:
     scale_suffix: tuple | None = None            # (weight suffix, scale suffix)
     whole_file_on_device: bool = False           # stage the header too (keeps its misalignment)
     slices: dict | None = None                   # name -> (dim, start, stop) for sliced loads
+    quant: dict | None = None                    # name -> (kind, scales, global scale, block) for block-scaled weights
 
 
 def tiny(seed=0):
@@ -329,6 +330,44 @@ def llm8b_tp4(seed=3):
                     slices=tp_slices(lay.entries, 4, 0))
 
 
+def _linears(blocks):
+    for b in range(blocks):
+        for lin, shape in [(f"self_attn.{k}_proj", [3072, 3072]) for k in ("q", "k", "v", "o")] + \
+                          [(f"mlp.{k}_proj", [12288, 3072]) for k in ("gate", "up")] + \
+                          [("mlp.down_proj", [3072, 12288])]:
+            yield f"model.layers.{b:02d}.{lin}.", shape
+
+
+def block_fp8(seed=5, blocks=40):
+    """Block-FP8 transformer weights (the DeepSeek/Qwen FP8 layout): E4M3
+    linears with an F32 'weight_scale_inv' per 128 x 128 block; BF16 out.
+    40 layers x (4 x [3072,3072] + 3 x [12288,3072]/[3072,12288]): 6.04 GB of
+    weights, 12.08 GB of BF16 out."""
+    ents, quant = [], {}
+    for base, (M, N) in _linears(blocks):
+        ents += [Entry(base + "weight", "F8_E4M3", [M, N]),
+                 Entry(base + "weight_scale_inv", "F32", [-(-M // 128), -(-N // 128)])]
+        quant[base + "weight"] = ("block_fp8", base + "weight_scale_inv", None, (128, 128))
+    ents.sort(key=lambda e: e.name)
+    lay = make_layout(ents, metadata={"format": "pt", "quantization": "block_fp8"})
+    return Workload(f"block_fp8_e4m3_{blocks}layer", [lay], [seed], ["BF16"], quant=quant)
+
+
+def nvfp4(seed=6, blocks=40):
+    """NVFP4 transformer weights (the ModelOpt layout): U8 [M, N/2] packed
+    E2M1 pairs, an E4M3 'weight_scale' per 16 elements of a row and an F32
+    'weight_scale_2'; the same 40 layers as block_fp8; BF16 out."""
+    ents, quant = [], {}
+    for base, (M, N) in _linears(blocks):
+        ents += [Entry(base + "weight", "U8", [M, N // 2]),
+                 Entry(base + "weight_scale", "F8_E4M3", [M, N // 16]),
+                 Entry(base + "weight_scale_2", "F32", [])]
+        quant[base + "weight"] = ("nvfp4", base + "weight_scale", base + "weight_scale_2", None)
+    ents.sort(key=lambda e: e.name)
+    lay = make_layout(ents, metadata={"format": "pt", "quantization": "nvfp4"})
+    return Workload(f"nvfp4_{blocks}layer", [lay], [seed], ["BF16"], quant=quant)
+
+
 WORKLOADS = {"tiny": tiny, "unet": unet, "scaled_fp8": scaled_fp8, "llm8b": llm8b, "stress": stress,
              # a 5-block slice of the scaled-fp8 checkpoint (1.04 GB source), for profiling
              "scaled_fp8_5blk": lambda: scaled_fp8(blocks=5),
@@ -336,7 +375,10 @@ WORKLOADS = {"tiny": tiny, "unet": unet, "scaled_fp8": scaled_fp8, "llm8b": llm8
              "unet_small": lambda: unet(n1280=8),
              "llm8b_tp4": llm8b_tp4,
              # the same 4-shard checkpoint cast to F16 (the second run of the LLM config)
-             "llm8b_f16": lambda: _with_dst(llm8b(), ["F16"])}
+             "llm8b_f16": lambda: _with_dst(llm8b(), ["F16"]),
+             "block_fp8": block_fp8, "nvfp4": nvfp4,
+             # 4-layer slices of the same constructions, for tests and profiling
+             "block_fp8_4l": lambda: block_fp8(blocks=4), "nvfp4_4l": lambda: nvfp4(blocks=4)}
 
 
 def _with_dst(wl: Workload, dst):
@@ -345,12 +387,32 @@ def _with_dst(wl: Workload, dst):
     return wl
 
 
+def fill_block_scales(wl: Workload, layout: FileLayout, data: np.ndarray, seed: int):
+    """Block scales of block-scaled weights: F32 block-FP8 scales uniform in
+    [1e-3, 1e-1]; NVFP4 E4M3 scales uniform over the codes of 2^-6 .. 2^2
+    (0x08..0x47); NVFP4 global scales uniform in [1e-4, 1e-2]."""
+    rng = np.random.Generator(np.random.PCG64([seed, 32452843]))
+    by_name = {e.name: e for e in layout.entries}
+    for kind, sname, gname, _ in (wl.quant or {}).values():
+        e = by_name.get(sname)
+        if e is None:
+            continue
+        if kind == "block_fp8":
+            data[e.begin:e.end] = rng.uniform(1e-3, 1e-1, size=e.numel).astype(np.float32).view(np.uint8)
+        else:
+            data[e.begin:e.end] = rng.integers(0x08, 0x48, size=e.numel, dtype=np.uint8)
+            g = by_name[gname]
+            data[g.begin:g.end] = np.frombuffer(np.float32(rng.uniform(1e-4, 1e-2)).tobytes(), dtype=np.uint8)
+
+
 def build_workload_data(wl: Workload, k: int, out: np.ndarray):
     """Data section of shard k of workload `wl` into `out` (uint8, data_bytes long)."""
     lay = wl.files[k]
     fill(lay, out, wl.seeds[k])
     if wl.scale_suffix:
         fill_scales(lay, out, wl.seeds[k])
+    if wl.quant:
+        fill_block_scales(wl, lay, out, wl.seeds[k])
     return out
 
 
@@ -360,4 +422,6 @@ def build_workload_file(wl: Workload, k: int, out: np.ndarray | None = None):
     buf = build_file(lay, wl.seeds[k], out)
     if wl.scale_suffix:
         fill_scales(lay, buf[lay.data_start:], wl.seeds[k])
+    if wl.quant:
+        fill_block_scales(wl, lay, buf[lay.data_start:], wl.seeds[k])
     return buf

@@ -17,7 +17,20 @@ import pytest
 
 # class -> (source itemsize, output itemsize) in counted units
 CLS = {0: (1, 1), 1: (4, 2), 2: (4, 2), 3: (2, 2), 4: (2, 4), 5: (2, 2), 6: (2, 4),
-       7: (1, 2), 8: (1, 2), 9: (1, 4), 10: (1, 2), 11: (1, 2), 12: (1, 4)}
+       7: (1, 2), 8: (1, 2), 9: (1, 4), 10: (1, 2), 11: (1, 2), 12: (1, 4),
+       # block-scaled: fp8 elements (13-18), NVFP4 bytes of two elements (19-21)
+       13: (1, 2), 14: (1, 2), 15: (1, 4), 16: (1, 2), 17: (1, 2), 18: (1, 4), 19: (1, 4), 20: (1, 4), 21: (1, 8)}
+NVFP4 = (19, 20, 21)
+
+
+def step_shape(cls):
+    """(SB, KS, OS) of a class's lane step in the TMA consumer."""
+    si, so = CLS[cls]
+    if cls >= 13:
+        sb = 4 if cls in NVFP4 or so == 4 else 8
+        return sb, sb, sb * so
+    sb = 16 * si // so if so > si else 16
+    return sb, sb // si, (sb // si) * so
 
 
 def split(src, dst, n, si, so, lo, hi):
@@ -110,12 +123,15 @@ def tma_run(src, dst, n, si, so, lo, hi):
     return covered
 
 
-def consume_model(off, ln, a, z, nbytes, dst, si, so):
-    """Mirror of consume_seg for one piece's part of a slot: the slot reads
+def consume_model(off, ln, a, z, nbytes, dst, si, so, cls=None):
+    """Mirror of consume_seg / consume_quant for one slot: the slot reads
     stay inside the slot and inside the copied bytes; vector stores aligned."""
-    SB = 16 * si // so if so > si else 16
-    KS = SB // si
-    OS = KS * so
+    if cls is not None:
+        SB, KS, OS = step_shape(cls)
+    else:
+        SB = 16 * si // so if so > si else 16
+        KS = SB // si
+        OS = KS * so
     m = z - a
     dp = dst + a * so
     h = min(((OS - (dp & (OS - 1))) & (OS - 1)) // so, m)
@@ -131,7 +147,7 @@ def consume_model(off, ln, a, z, nbytes, dst, si, so):
         assert (dp + h * so) % OS == 0
 
 
-def tma_warp(plan, pieces, bases, data_base, lo, hi):
+def tma_warp(plan, pieces, bases, data_base, lo, hi, quant=None):
     """Mirror of materialize_tma's producer over one warp's pieces (batches of
     32, segments of at most SEG source bytes): every bulk copy is 16-byte
     aligned, inside the 16-byte aligned interior of the data section and fits
@@ -149,6 +165,27 @@ def tma_warp(plan, pieces, bases, data_base, lo, hi):
             si, so = CLS[p["cls"]]
             cnt = p["count"]
             ln = min(SEG // si, cnt - e)
+            if p["cls"] >= 13:   # block-scaled: one row, scales fit the slot's scale area
+                q = quant[p["output"]]
+                nv = p["cls"] in NVFP4
+                u = p["dst"] // so + e
+                row, colu = divmod(u, q["row_units"])
+                ln = min(ln, q["row_units"] - colu)
+                col0 = 2 * colu if nv else colu
+                ss = 1 if nv else 4
+                bc = 1 << q["bc_shift"]
+                max_el = (128 // ss) * bc - (col0 & (bc - 1))
+                ln = min(ln, max_el // 2 if nv else max_el)
+                el = 2 * ln if nv else ln
+                b0 = col0 >> q["bc_shift"]
+                nblk = ((col0 + el - 1) >> q["bc_shift"]) - b0 + 1
+                g = data_base + q["scale"] + ((row >> q["br_shift"]) * q["scols"] + b0) * ss
+                sw0, sw1 = g & ~15, (g + nblk * ss + 15) & ~15
+                if sw0 >= lo16 and sw1 <= hi16:
+                    assert sw1 - sw0 <= 160 and (sw1 - sw0) % 16 == 0
+                else:
+                    assert lo <= g and g + nblk * ss <= hi
+                assert ln >= 1
             s = data_base + p["src"] + r * p["pitch"] + e * si
             A, Z = 0, ln
             if s < lo16:
@@ -164,7 +201,7 @@ def tma_warp(plan, pieces, bases, data_base, lo, hi):
             for x in list(range(0, A)) + list(range(Z, ln)):
                 assert lo <= s + x * si and s + (x + 1) * si <= hi
             dst0 = bases[p["output"]] + p["dst"] + (r * cnt + e) * so
-            subs = [(off, ln, A, Z, dst0, si, so)]
+            subs = [(off, ln, A, Z, dst0, si, so, p["cls"])]
             done.setdefault((id(p), r), []).append((e, e + ln))
             e += ln
             if e == cnt:
@@ -176,8 +213,8 @@ def tma_warp(plan, pieces, bases, data_base, lo, hi):
             if nbytes:
                 assert w0 % 16 == 0 and nbytes % 16 == 0 and 0 < nbytes <= SEG + 16
                 assert lo <= lo16 <= w0 and w0 + nbytes <= hi16 <= hi
-            for (o, ln2, a2, z2, d2, si2, so2) in subs:
-                consume_model(o, ln2, a2, z2, nbytes, d2, si2, so2)
+            for (o, ln2, a2, z2, d2, si2, so2, c2) in subs:
+                consume_model(o, ln2, a2, z2, nbytes, d2, si2, so2, c2)
     for p in pieces:
         for r in range(p["rows"]):
             got = sorted(done.get((id(p), r), []))
@@ -336,3 +373,42 @@ def test_tma_windows_on_tiny_data_sections():
                         if b > a:
                             segs = tma_run(lo + a * si, (1 << 40) + 256 + a * so, b - a, si, so, lo, hi)
                             assert segs[-1][1] == b - a
+
+
+@pytest.mark.parametrize("lead", [0, 1, 3, 8])
+def test_blockscaled_plans_in_bounds(stmat, lead):
+    """Block FP8 and NVFP4 weights (ragged rows, blocks of 16..512 columns,
+    unaligned weight and scale offsets): every TMA window, scale window and
+    slot read of the block-scaled consumer stays in bounds."""
+    import test_blockscale as TB
+    for fp8 in (("F8_E4M3", 257, 300, (128, 128)), ("F8_E5M2", 64, 48, (16, 16)), ("F8_E4M3", 3, 2000, (1, 16)),
+                ("F8_E4M3", 130, 1030, (64, 512))):
+        img, quant = TB.quant_file(lead, lead=lead, fp8=fp8, nv=(7, 2064))
+        ix = stmat.Index.from_file(img)
+        names, q = TB.selection(ix, quant)
+        hlen, dbytes = ix.sizes()
+        ents = {e["name"]: e for e in ix.entries()}
+        for workers in (1, 7, 64):
+            plan = ix.plan(dst="BF16", names=names, quant=q, workers=workers, host_only=True)
+            outs = plan.outputs()
+            qinfo = {}
+            for i, o in enumerate(outs):
+                if not o["quant"]:
+                    continue
+                sc = ents[o["scale"]]
+                nv = o["quant"] == "nvfp4"
+                br, bc = (1, 16) if nv else quant[o["name"]][3]
+                qinfo[i] = {"scale": sc["begin"], "row_units": o["shape"][1] // (2 if nv else 1),
+                            "scols": sc["shape"][1], "br_shift": br.bit_length() - 1, "bc_shift": bc.bit_length() - 1}
+            st = plan.stats()
+            pieces = [plan.piece(k) for k in range(st["pieces"])]
+            for residue in (0, 5, 11):
+                base = (1 << 32) + residue
+                bases, at = [], 1 << 20
+                for o in outs:
+                    at = (at + 255) // 256 * 256
+                    bases.append(at)
+                    at += o["bytes"]
+                for w in range(st["workers"]):
+                    a, b = plan.worker(0, w)
+                    tma_warp(plan, pieces[a:b], bases, base, base, base + dbytes, quant=qinfo)
