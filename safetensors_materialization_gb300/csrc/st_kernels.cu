@@ -567,9 +567,12 @@ struct SegMeta {
 
 // A segment of a block-scaled weight brings at most this many bytes of block
 // scales (the producer shortens the segment to fit), fetched with the
-// segment into the slot's scale area.
-constexpr uint32_t kScalePayload = 128;
+// segment into the slot's scale area: 256 NVFP4 scales cover a whole 2 KiB
+// segment; block-FP8 segments are held to kQscMax F32 scales, which the
+// consumer decodes into the warp's table.
+constexpr uint32_t kScalePayload = 256;
 constexpr uint32_t kScaleBytes = kScalePayload + 32;
+constexpr uint32_t kQscMax = 32;
 
 struct alignas(128) WarpSmem {
   uint8_t buf[kSlots][kSlotBytes];
@@ -580,7 +583,9 @@ struct alignas(128) WarpSmem {
   SegMeta meta[kSlots];
   uint64_t bar[kSlots];
   uint64_t dbar[2];
+  float qsc[kQscMax];  // the consumed block-FP8 segment's scales as binary32 (any alignment in the slot)
 };
+static_assert(sizeof(WarpSmem) * kWarpsPerBlock <= 113 * 1024, "two 8-warp blocks per SM");
 static_assert(offsetof(WarpSmem, sbuf) % 16 == 0 && kScaleBytes % 16 == 0, "scale bulk-copy destinations");
 static_assert(offsetof(WarpSmem, desc) % 16 == 0 && kSlotBytes % 16 == 0, "bulk-copy destinations");
 
@@ -708,16 +713,14 @@ __device__ __forceinline__ float e2m1_value(uint32_t nib) {
   return __uint_as_float(__float_as_uint(mag) | ((nib & 8u) << 28));
 }
 
-// The scale of element column `col` of a block-scaled segment: F32 block
-// scales (block FP8), or E4M3 block scale times the global scale (NVFP4).
+// Block scale k of a segment as binary32: an F32 block scale (block FP8,
+// any alignment), or an E4M3 block scale times the global scale g (NVFP4).
 template <bool kNv>
-__device__ __forceinline__ float block_scale(const SegMeta &m, uint32_t col) {
-  const uint32_t blk = (col >> m.bcs) - (m.col0 >> m.bcs);
+__device__ __forceinline__ float decode_scale(const uint8_t *sptr, uint32_t k, float g) {
   if constexpr (kNv) {
-    const float sb = decode1<S_E4M3>(m.sptr[blk]);
-    return __fmul_rn(sb, m.scale);
+    return __fmul_rn(decode1<S_E4M3>(sptr[k]), g);
   } else {
-    const uint8_t *p = m.sptr + 4 * blk;  // any alignment
+    const uint8_t *p = sptr + 4 * k;
     return __uint_as_float(static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) |
                            (static_cast<uint32_t>(p[2]) << 16) | (static_cast<uint32_t>(p[3]) << 24));
   }
@@ -735,51 +738,95 @@ struct QConv {
   static constexpr int SB = kNv ? 4 : (ES == 4 ? 4 : 8);
   static constexpr int KS = SB, OS = KS * SO, KE = KS * EPU;
 
-  __device__ static float value(uint32_t byte, int k) {  // element k (0 or 1) of a unit
-    if constexpr (kNv) return e2m1_value(k ? byte >> 4 : byte & 15u);
-    else return decode1<S>(byte);
+  // Elements 2j, 2j+1 of a step's words as binary32 (NVFP4: one hardware
+  // e2m1x2 -> f16x2 conversion, exact, then f16 -> f32, exact).
+  __device__ static float2 pair(const uint32_t (&w)[SB / 4], int j) {
+    if constexpr (kNv) {
+      const uint16_t byte = static_cast<uint16_t>((w[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+      uint32_t h2;
+      asm("{\n .reg .b8 t;\n cvt.u8.u16 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h2) : "h"(byte));
+      __half2_raw r;
+      r.x = static_cast<unsigned short>(h2 & 0xFFFFu);
+      r.y = static_cast<unsigned short>(h2 >> 16);
+      return __half22float2(__half2(r));
+    } else {
+      return decode2<S, SB / 4>(w, j);
+    }
   }
-  // One unit at p (any memory) to q; e = its unit index in the segment.
-  __device__ static void one(const uint8_t *p, uint8_t *q, uint32_t e, const SegMeta &m) {
+  // One unit at p (any memory) to q; `col` = its first element's column
+  // relative to the segment's first block; the scales are the table qsc
+  // (block FP8) or the E4M3 bytes at sptr times g (NVFP4).
+  __device__ static void one(const uint8_t *p, uint8_t *q, uint32_t col, uint32_t bcs, const float *qsc,
+                             const uint8_t *sptr, float g) {
     const uint32_t byte = *p;
 #pragma unroll
     for (int k = 0; k < EPU; ++k) {
-      const float x = __fmul_rn(value(byte, k), block_scale<kNv>(m, m.col0 + e * EPU + k));
-      const uint32_t y = encode1<D>(x);
+      const float v = kNv ? e2m1_value(k ? byte >> 4 : byte & 15u) : decode1<S>(byte);
+      const uint32_t blk = (col + k) >> bcs;
+      const float sc = kNv ? decode_scale<true>(sptr, blk, g) : qsc[blk];
+      const uint32_t y = encode1<D>(__fmul_rn(v, sc));
       if constexpr (ES == 2) reinterpret_cast<uint16_t *>(q)[k] = static_cast<uint16_t>(y);
       else reinterpret_cast<uint32_t *>(q)[k] = y;
     }
   }
-  // KE elements from the step's words; elements [0, kb) take scale lo, the
-  // rest hi (a step crosses at most one block boundary: blocks hold >= 16).
+  // KE elements; elements [0, kb) take scale lo, the rest hi (a step crosses
+  // at most one block boundary: blocks hold >= 16 elements).  kClean: no
+  // product can be NaN (NVFP4 values are finite and the segment's scales
+  // are finite), so the NaN canonicalization is skipped.
+  template <bool kClean>
   __device__ static void step(const uint32_t (&w)[SB / 4], float lo, float hi, uint32_t kb,
                               uint32_t (&o)[OS / 4]) {
 #pragma unroll
-    for (int k = 0; k < KE; k += 2) {
-      const uint32_t b0 = (w[(k / EPU) >> 2] >> (8 * ((k / EPU) & 3))) & 0xFFu;
-      const uint32_t b1 = (w[((k + 1) / EPU) >> 2] >> (8 * (((k + 1) / EPU) & 3))) & 0xFFu;
-      float2 f;
-      f.x = __fmul_rn(value(b0, k % EPU), static_cast<uint32_t>(k) < kb ? lo : hi);
-      f.y = __fmul_rn(value(b1, (k + 1) % EPU), static_cast<uint32_t>(k + 1) < kb ? lo : hi);
+    for (int j = 0; j < KE / 2; ++j) {
+      float2 f = pair(w, j);
+      f.x = __fmul_rn(f.x, static_cast<uint32_t>(2 * j) < kb ? lo : hi);
+      f.y = __fmul_rn(f.y, static_cast<uint32_t>(2 * j + 1) < kb ? lo : hi);
       if constexpr (D == D_F32) {
-        o[k] = encode1<D_F32>(f.x);
-        o[k + 1] = encode1<D_F32>(f.y);
+        o[2 * j] = kClean ? __float_as_uint(f.x) : encode1<D_F32>(f.x);
+        o[2 * j + 1] = kClean ? __float_as_uint(f.y) : encode1<D_F32>(f.y);
+      } else if constexpr (kClean && D == D_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
+        o[j] = *reinterpret_cast<uint32_t *>(&v);
+      } else if constexpr (kClean) {
+        __half2 v = __floats2half2_rn(f.x, f.y);
+        o[j] = *reinterpret_cast<uint32_t *>(&v);
       } else {
-        o[k / 2] = encode2_16<D>(f);
+        o[j] = encode2_16<D>(f);
       }
     }
   }
 };
 
+// A block-scaled segment: its block scales are decoded once into the warp's
+// table, then elements [a, z) come from the slot and the rest from global.
 template <class QV>
-__device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta &m, uint32_t lane) {
+__device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta &m, float *qsc, uint32_t lane) {
   constexpr int SO = QV::SO, SB = QV::SB, KS = QV::KS, OS = QV::OS, N = SB / 4, EPU = QV::EPU;
   uint8_t *const dst = m.dst;
-  const uint32_t len = m.len, off = m.off, a = m.a, z = m.z;
+  const uint8_t *const gsrc = m.gsrc;
+  const uint32_t len = m.len, off = m.off, a = m.a, z = m.z, bcs = m.bcs;
+  const uint32_t cbase = m.col0 & ((1u << bcs) - 1);  // column of unit 0 relative to its block's start
+  const uint32_t nblk = ((cbase + len * EPU - 1) >> bcs) + 1;
+  const uint8_t *const sptr = m.sptr;
+  const float g = m.scale;
+  // Block FP8: the F32 scales (any alignment) decoded once into the table.
+  // NVFP4: scales are decoded per step from the slot; here only checked.
+  bool finite = true;
+  for (uint32_t k = lane; k < nblk; k += 32) {
+    const float v = decode_scale<QV::kNv>(sptr, k, g);
+    finite = finite && isfinite(v);
+    if constexpr (!QV::kNv) qsc[k] = v;
+  }
+  __syncwarp();
+  const bool clean = QV::kNv && __all_sync(0xFFFFFFFFu, finite);
+  auto scale_at = [&](uint32_t blk) -> float {
+    if constexpr (QV::kNv) return decode_scale<true>(sptr, blk, g);
+    else return qsc[blk];
+  };
   const uint32_t edge = a + (len - z);
   for (uint32_t t = lane; t < edge; t += 32) {
     const uint32_t e = t < a ? t : z + (t - a);
-    QV::one(m.gsrc + e, dst + static_cast<uint64_t>(e) * SO, e, m);
+    QV::one(gsrc + e, dst + static_cast<uint64_t>(e) * SO, cbase + e * EPU, bcs, qsc, sptr, g);
   }
   const uint32_t n = z - a;
   const uint8_t *sp = buf + off;
@@ -790,13 +837,21 @@ __device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta 
   const uint32_t ends = h + (n - t0);
   for (uint32_t t = lane; t < ends; t += 32) {
     const uint32_t e = t < h ? t : t0 + (t - h);
-    QV::one(sp + e, dp + e * SO, a + e, m);
+    QV::one(sp + e, dp + e * SO, cbase + (a + e) * EPU, bcs, qsc, sptr, g);
   }
   const uint32_t q = off + h, r = q & (SB - 1);
   const uint8_t *wb = buf + (q - r);
   uint8_t *db = dp + h * SO;
-  const uint32_t bc = 1u << m.bcs;
+  const uint32_t bc = 1u << bcs;
+  const uint32_t col1 = cbase + (a + h) * EPU;  // the first step's first element, block-relative
+  // Steps that start on a multiple of KE columns never cross a block boundary
+  // (blocks are powers of two >= 16 >= KE): one scale per step.
+  const uint32_t kb_all = (col1 & (QV::KE - 1)) == 0 ? static_cast<uint32_t>(QV::KE) : 0u;
   for (uint32_t c = lane; c < nst; c += 32) {
+    const uint32_t col = col1 + c * KS * EPU;
+    const uint32_t kb = kb_all ? kb_all : bc - (col & (bc - 1));
+    const float lo = scale_at(col >> bcs);
+    const float hi = kb < static_cast<uint32_t>(QV::KE) ? scale_at((col >> bcs) + 1) : lo;
     uint32_t x[N], sv[N];
     lds<N>(wb + c * SB, x);
     if (r) {
@@ -807,17 +862,19 @@ __device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta 
 #pragma unroll
       for (int i = 0; i < N; ++i) sv[i] = x[i];
     }
-    const uint32_t col = m.col0 + (a + h + c * KS) * EPU;  // column of the step's first element
-    const uint32_t kb = bc - (col & (bc - 1));
-    const float lo = block_scale<QV::kNv>(m, col);
-    const float hi = kb < static_cast<uint32_t>(QV::KE) ? block_scale<QV::kNv>(m, col + kb) : lo;
     uint32_t o[OS / 4];
-    QV::step(sv, lo, hi, kb, o);
+    if (kb_all) {
+      if (clean) QV::template step<true>(sv, lo, lo, QV::KE, o);
+      else QV::template step<false>(sv, lo, lo, QV::KE, o);
+    } else {
+      if (clean) QV::template step<true>(sv, lo, hi, kb, o);
+      else QV::template step<false>(sv, lo, hi, kb, o);
+    }
     store_out<OS / 4>(db + c * OS, o);
   }
 }
 
-__device__ __forceinline__ void consume_any(const uint8_t *buf, const SegMeta &m, uint32_t lane) {
+__device__ __forceinline__ void consume_any(const uint8_t *buf, const SegMeta &m, float *qsc, uint32_t lane) {
   switch (m.cls) {
     case CLS_COPY: consume_seg<CopyBytes>(buf, m, lane); break;
     case CLS_F32_BF16: consume_seg<Conv<S_F32, D_BF16>>(buf, m, lane); break;
@@ -832,15 +889,15 @@ __device__ __forceinline__ void consume_any(const uint8_t *buf, const SegMeta &m
     case CLS_E5M2_BF16: consume_seg<Conv<S_E5M2, D_BF16>>(buf, m, lane); break;
     case CLS_E5M2_F16: consume_seg<Conv<S_E5M2, D_F16>>(buf, m, lane); break;
     case CLS_E5M2_F32: consume_seg<Conv<S_E5M2, D_F32>>(buf, m, lane); break;
-    case CLS_QE4M3_BF16: consume_quant<QConv<S_E4M3, D_BF16>>(buf, m, lane); break;
-    case CLS_QE4M3_F16: consume_quant<QConv<S_E4M3, D_F16>>(buf, m, lane); break;
-    case CLS_QE4M3_F32: consume_quant<QConv<S_E4M3, D_F32>>(buf, m, lane); break;
-    case CLS_QE5M2_BF16: consume_quant<QConv<S_E5M2, D_BF16>>(buf, m, lane); break;
-    case CLS_QE5M2_F16: consume_quant<QConv<S_E5M2, D_F16>>(buf, m, lane); break;
-    case CLS_QE5M2_F32: consume_quant<QConv<S_E5M2, D_F32>>(buf, m, lane); break;
-    case CLS_NVFP4_BF16: consume_quant<QConv<S_NV, D_BF16>>(buf, m, lane); break;
-    case CLS_NVFP4_F16: consume_quant<QConv<S_NV, D_F16>>(buf, m, lane); break;
-    case CLS_NVFP4_F32: consume_quant<QConv<S_NV, D_F32>>(buf, m, lane); break;
+    case CLS_QE4M3_BF16: consume_quant<QConv<S_E4M3, D_BF16>>(buf, m, qsc, lane); break;
+    case CLS_QE4M3_F16: consume_quant<QConv<S_E4M3, D_F16>>(buf, m, qsc, lane); break;
+    case CLS_QE4M3_F32: consume_quant<QConv<S_E4M3, D_F32>>(buf, m, qsc, lane); break;
+    case CLS_QE5M2_BF16: consume_quant<QConv<S_E5M2, D_BF16>>(buf, m, qsc, lane); break;
+    case CLS_QE5M2_F16: consume_quant<QConv<S_E5M2, D_F16>>(buf, m, qsc, lane); break;
+    case CLS_QE5M2_F32: consume_quant<QConv<S_E5M2, D_F32>>(buf, m, qsc, lane); break;
+    case CLS_NVFP4_BF16: consume_quant<QConv<S_NV, D_BF16>>(buf, m, qsc, lane); break;
+    case CLS_NVFP4_F16: consume_quant<QConv<S_NV, D_F16>>(buf, m, qsc, lane); break;
+    case CLS_NVFP4_F32: consume_quant<QConv<S_NV, D_F32>>(buf, m, qsc, lane); break;
     default: break;
   }
 }
@@ -979,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
         len = min(len, qi.row_units - colu);
         col0 = nv ? 2 * colu : colu;
         const uint32_t ss = nv ? 1 : 4;  // bytes per block scale
-        const uint32_t bc = 1u << qi.bc_shift, maxblk = kScalePayload / ss;
+        const uint32_t bc = 1u << qi.bc_shift, maxblk = nv ? kScalePayload : kQscMax;
         const uint32_t max_el = maxblk * bc - (col0 & (bc - 1));
         len = min(len, nv ? max_el / 2 : max_el);
         const uint32_t el = nv ? 2 * len : len;
@@ -1062,7 +1119,7 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
       break;
     }
     __syncwarp();
-    consume_any(ws.buf[slot], ws.meta[slot], lane);
+    consume_any(ws.buf[slot], ws.meta[slot], ws.qsc, lane);
     __syncwarp();
     ++jc;
   }

@@ -174,7 +174,7 @@ def tma_warp(plan, pieces, bases, data_base, lo, hi, quant=None):
                 col0 = 2 * colu if nv else colu
                 ss = 1 if nv else 4
                 bc = 1 << q["bc_shift"]
-                max_el = (128 // ss) * bc - (col0 & (bc - 1))
+                max_el = (256 if nv else 32) * bc - (col0 & (bc - 1))
                 ln = min(ln, max_el // 2 if nv else max_el)
                 el = 2 * ln if nv else ln
                 b0 = col0 >> q["bc_shift"]
@@ -182,7 +182,7 @@ def tma_warp(plan, pieces, bases, data_base, lo, hi, quant=None):
                 g = data_base + q["scale"] + ((row >> q["br_shift"]) * q["scols"] + b0) * ss
                 sw0, sw1 = g & ~15, (g + nblk * ss + 15) & ~15
                 if sw0 >= lo16 and sw1 <= hi16:
-                    assert sw1 - sw0 <= 160 and (sw1 - sw0) % 16 == 0
+                    assert sw1 - sw0 <= 288 and (sw1 - sw0) % 16 == 0
                 else:
                     assert lo <= g and g + nblk * ss <= hi
                 assert ln >= 1
