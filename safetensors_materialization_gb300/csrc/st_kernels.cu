@@ -738,6 +738,20 @@ struct QConv {
   static constexpr int SB = kNv ? 4 : (ES == 4 ? 4 : 8);
   static constexpr int KS = SB, OS = KS * SO, KE = KS * EPU;
 
+  // Block FP8: whether any element of the step could give a NaN product
+  // (E4M3: a NaN code, the low seven bits all set; E5M2: exponent all ones,
+  // infinity included since infinity times a zero scale is NaN),
+  // byte-parallel on the words.
+  __device__ static bool has_nan(const uint32_t (&w)[SB / 4]) {
+    uint32_t any = 0;
+#pragma unroll
+    for (int i = 0; i < SB / 4; ++i) {
+      const uint32_t t = w[i] & 0x7F7F7F7Fu;
+      any |= (t + (S == S_E4M3 ? 0x01010101u : 0x04040404u)) & 0x80808080u;
+    }
+    return any != 0;
+  }
+
   // Elements 2j, 2j+1 of a step's words as binary32 (NVFP4: one hardware
   // e2m1x2 -> f16x2 conversion, exact, then f16 -> f32, exact).
   __device__ static float2 pair(const uint32_t (&w)[SB / 4], int j) {
@@ -818,7 +832,9 @@ __device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta 
     if constexpr (!QV::kNv) qsc[k] = v;
   }
   __syncwarp();
-  const bool clean = QV::kNv && __all_sync(0xFFFFFFFFu, finite);
+  // NVFP4: no product can be NaN when the scales are finite.  Block FP8: also
+  // needs NaN-free elements, checked per step below.
+  const bool clean = __all_sync(0xFFFFFFFFu, finite);
   auto scale_at = [&](uint32_t blk) -> float {
     if constexpr (QV::kNv) return decode_scale<true>(sptr, blk, g);
     else return qsc[blk];
@@ -863,11 +879,13 @@ __device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta 
       for (int i = 0; i < N; ++i) sv[i] = x[i];
     }
     uint32_t o[OS / 4];
+    bool fast = clean;
+    if constexpr (!QV::kNv) fast = fast && __all_sync(__activemask(), !QV::has_nan(sv));
     if (kb_all) {
-      if (clean) QV::template step<true>(sv, lo, lo, QV::KE, o);
+      if (fast) QV::template step<true>(sv, lo, lo, QV::KE, o);
       else QV::template step<false>(sv, lo, lo, QV::KE, o);
     } else {
-      if (clean) QV::template step<true>(sv, lo, hi, kb, o);
+      if (fast) QV::template step<true>(sv, lo, hi, kb, o);
       else QV::template step<false>(sv, lo, hi, kb, o);
     }
     store_out<OS / 4>(db + c * OS, o);
@@ -983,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
   // Block-scaled pieces: the output's scale table entry and the output unit
   // index of the piece's first unit.
   QuantInfo qi{};
-  uint64_t unit0 = 0;
+  uint32_t q_row = 0, q_colu = 0;  // weight row and column (in units) of the cursor
   auto load_piece_state = [&]() -> bool {  // false: skip this piece
     const Piece &pc = ws.desc[cur.b & 1][cur.i];
     uint8_t *dp = ws.dstp[cur.b & 1][cur.i];
@@ -999,7 +1017,9 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
     scale = ws.scl[cur.b & 1][cur.i];
     if (cls_quant(cls)) {
       qi = a.quant[pc.out_cls >> kClsBits];
-      unit0 = pc.dst >> sos;
+      const uint64_t unit0 = pc.dst >> sos;  // one division per piece
+      q_row = static_cast<uint32_t>(unit0 / qi.row_units);
+      q_colu = static_cast<uint32_t>(unit0 - static_cast<uint64_t>(q_row) * qi.row_units);
     }
     return true;
   };
@@ -1030,9 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
       uintptr_t sw0 = 0;
       if (cls_quant(cls)) {
         const bool nv = cls_nvfp4(cls);
-        const uint64_t u = unit0 + cur.e;
-        const uint64_t row = u / qi.row_units;
-        const uint32_t colu = static_cast<uint32_t>(u - row * qi.row_units);
+        const uint32_t row = q_row, colu = q_colu;
         len = min(len, qi.row_units - colu);
         col0 = nv ? 2 * colu : colu;
         const uint32_t ss = nv ? 1 : 4;  // bytes per block scale
@@ -1041,7 +1059,12 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
         len = min(len, nv ? max_el / 2 : max_el);
         const uint32_t el = nv ? 2 * len : len;
         const uint32_t b0 = col0 >> qi.bc_shift, nblk = ((col0 + el - 1) >> qi.bc_shift) - b0 + 1;
-        const uint8_t *sg = a.data + qi.scale + ((row >> qi.br_shift) * qi.scols + b0) * ss;
+        const uint8_t *sg = a.data + qi.scale + (static_cast<uint64_t>(row >> qi.br_shift) * qi.scols + b0) * ss;
+        q_colu += len;  // the next segment: same row, or the next one
+        if (q_colu == qi.row_units) {
+          q_colu = 0;
+          ++q_row;
+        }
         const uintptr_t g = reinterpret_cast<uintptr_t>(sg);
         sw0 = g & ~uintptr_t(15);
         const uintptr_t sw1 = (g + nblk * ss + 15) & ~uintptr_t(15);

@@ -256,3 +256,28 @@ def test_chunked_plans_wait_for_block_scales(stmat, chunk):
                     assert ents[o["scale"]]["end"] <= (c + 1) * chunk
                     if o["quant"] == "nvfp4":
                         assert ents[quant[o["name"]][2]]["end"] <= (c + 1) * chunk
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dst", ["BF16", "F16", "F32"])
+def test_gpu_special_scales(stmat, oracle, dst):
+    """Every fp8 code (E5M2 infinities and NaNs included) against block
+    scales of 0, -0, inf, NaN, tiny and huge values, and NVFP4 with the same
+    global/block scale specials: 0 x inf and NaN products must come out as
+    the canonical NaN, the rest exactly as the oracle."""
+    specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, 3.4e38, 1.0], dtype=np.float32)
+    w = np.tile(np.arange(256, dtype=np.uint8), 8)                     # [8, 256]: each row every code
+    sc = np.repeat(specials, 16).reshape(8, 16)                        # 16 x 16 blocks, one special per row
+    for fmt in ("F8_E5M2", "F8_E4M3"):
+        ents = [("a.weight", fmt, [8, 256], w.tobytes()), ("a.s", "F32", [8, 16], sc.astype(np.float32).tobytes())]
+        nb = np.tile(np.arange(256, dtype=np.uint8), 2)                # NVFP4 [4, 128]: 256 elements per row
+        ns = np.array([0x00, 0x80, 0x7F, 0x38, 0x01, 0x7E, 0xFE, 0x08] * 8, dtype=np.uint8)   # [4, 16]
+        for g in (0.0, np.inf, np.nan, 2.5e-3):
+            img = image(ents + [("b.weight", "U8", [4, 128], nb.tobytes()), ("b.s", "F8_E4M3", [4, 16], ns.tobytes()),
+                                ("b.g", "F32", [], np.float32(g).tobytes())], lead=1)
+            quant = {"a.weight": ("block_fp8", "a.s", None, (1, 16)), "b.weight": ("nvfp4", "b.s", "b.g", None)}
+            plan, outs, names, q = run_gpu(stmat, img, quant, dst)
+            oix = oracle.parse(img)
+            sel = oix.select(dst=dst, names=names, quant=q)
+            data = img[8 + oix.header_len:]
+            assert_outputs(plan, outs, [sel.materialize(i, data) for i in range(len(sel))])
