@@ -46,6 +46,9 @@ def parse_args():
     ap.add_argument("--kernel", type=int, default=0, help="kernel build: 0 auto, 1 streaming, 2 latency")
     ap.add_argument("--order", type=int, default=0, help="unit order: 0 the build's default, 1 source, 2 class-major")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-files", choices=["auto", "on", "off"], default="auto",
+                    help="also time st_load_files from shard files written to a temp dir (auto: below 8 GB)")
+    ap.add_argument("--io-threads", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -300,6 +303,58 @@ def run_reference(args, rank, world):
 
 # -------------------------------------------------------------------- ours
 
+def time_load_files(args, w, host, data_start, data_bytes, dev, outs, sel, stream, dist, world, gb_dst, stmat, torch):
+    """st_load_files from the workload's shard files, written to a temp dir
+    just before (so they are read from the page cache): dst GB/s per step."""
+    import shutil
+    import tempfile
+    tmp = tempfile.mkdtemp(prefix="stmat_bench_")
+    try:
+        paths, at = [], data_start
+        hb = host.numpy()
+        for k, lay in enumerate(w.files):
+            path = os.path.join(tmp, f"shard{k}.safetensors")
+            with open(path, "wb") as f:
+                f.write(lay.header)
+                if len(w.files) == 1:
+                    f.write(memoryview(hb[data_start:data_start + lay.data_bytes]))
+                else:
+                    _, bases = stmat.Index.concat([stmat.Index.from_header(x.header, x.data_bytes) for x in w.files])
+                    f.write(memoryview(hb[bases[k]:bases[k] + lay.data_bytes]))
+            paths.append(path)
+        files, fix = stmat.Files.of_checkpoint(paths)
+        chunk = args.e2e_chunk_mb << 20
+        fplan = view_of(w)(fix).plan(dst=w.dst[0], scale_suffix=w.scale_suffix, chunk_bytes=chunk,
+                                     blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes,
+                                     kernel=args.kernel, order=args.order, **sel)
+        ring = torch.empty(3 * chunk, dtype=torch.uint8).pin_memory()
+        copy = torch.cuda.Stream()
+        ddata = dev[:data_bytes]
+        for _ in range(2):
+            fplan.load_files(files, ddata, outs.ptrs, ring, threads=args.io_threads, copy_stream=copy,
+                             compute_stream=stream)
+            fplan.check(stream)
+        if dist:
+            dist.barrier()
+        steps = max(3, min(args.steps, 5))
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            fplan.load_files(files, ddata, outs.ptrs, ring, threads=args.io_threads, copy_stream=copy,
+                             compute_stream=stream)
+            if fplan.check(stream) != 0:
+                raise RuntimeError("st_load_files flagged a bad destination")
+        es = (time.perf_counter() - t0) / steps
+        if dist:
+            t = torch.tensor([es], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            es = float(t.item())
+        return {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "ms_per_step": round(es * 1e3, 3),
+                "files": len(paths), "file_bytes_per_step": data_bytes, "chunk_bytes": chunk,
+                "ring_bytes": 3 * chunk, "io_threads": args.io_threads,
+                "source": "shard files in the page cache (written just before), pread into a pinned ring"}
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+
 def run_ours(args, rank, world, local):
     import torch
     from safetensors_materialization_gb300 import stmat, synth
@@ -417,6 +472,12 @@ def run_ours(args, rank, world, local):
                "d2h_bytes_per_step": 4, "ms_per_step": round(es * 1e3, 3),
                "chunk_bytes": args.e2e_chunk_mb << 20, "chunks": eplan.stats()["chunks"]}
 
+    # ---- end to end from shard files: disk (page cache) -> pinned ring -> device -> materialize
+    e2e_files = None
+    if not args.no_e2e and (args.e2e_files == "on" or (args.e2e_files == "auto" and data_bytes < 8e9)):
+        e2e_files = time_load_files(args, w, host, data_start, data_bytes, dev, outs, sel, stream, dist, world,
+                                    gb_dst, stmat, torch)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, nbytes, dt = oracle_sample(w, args.cpu_seconds)
@@ -445,6 +506,7 @@ def run_ours(args, rank, world, local):
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clk,
             "e2e": e2e,
+            "e2e_files": e2e_files,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -64,7 +64,8 @@ typedef enum st_status {
   ST_E_ALIGN = 11,           /* a pointer is not aligned as required */
   ST_E_NOMEM = 12,           /* host allocation failed */
   ST_E_CUDA = 13,            /* a CUDA runtime call failed (message has the CUDA error) */
-  ST_E_DEVICE = 14           /* the kernel reported a bad destination or a wait that gave up (st_plan_check) */
+  ST_E_DEVICE = 14,          /* the kernel reported a bad destination or a wait that gave up (st_plan_check) */
+  ST_E_IO = 15               /* a file could not be opened or read (the message has the OS error) */
 } st_status;
 
 /* Dtypes in the header's spelling; ST_KEEP is only an output request. */
@@ -76,6 +77,7 @@ typedef enum st_dtype {
 
 typedef struct st_index st_index_t; /* a parsed header, or a view of one */
 typedef struct st_plan_s st_plan_t; /* a selection turned into device work */
+typedef struct st_files_s st_files_t; /* open shard files addressed as one arena */
 
 /* ---------------------------------------------------------------- header */
 
@@ -303,6 +305,37 @@ st_status st_plan_worker(const st_plan_t *plan, uint32_t chunk, uint32_t w, uint
 
 /* ------------------------------------------------------------ device path */
 
+/* ------------------------------------------------------------- files */
+/* "Range reads and tiering" (Disk->RAM->GPU): bytes are read from the files
+ * with pread into host memory, only the ranges asked for. */
+
+/* Parses the header of the safetensors file at `path` (reads 8 + N bytes)
+ * into an index; *data_offset (may be NULL) = 8 + N, the file offset of the
+ * data section.  ST_E_IO when the file cannot be opened or read; the header
+ * errors of st_index_build otherwise. */
+st_status st_index_open(const char *path, st_index_t **out, uint64_t *data_offset);
+
+/* One file's data section placed in an arena: arena bytes [base, base +
+ * bytes) are the file's bytes [offset, offset + bytes).  For a checkpoint
+ * joined by st_index_concat: offset = data_offset of shard k, bytes = its
+ * data section size, base = bases[k]. */
+typedef struct st_file_part {
+  const char *path;
+  uint64_t offset, bytes, base;
+} st_file_part;
+
+/* Opens the files of `n` parts (read-only) and checks each holds its range;
+ * the parts must not overlap in the arena.  ST_E_IO on open/stat failures or
+ * a file too short, ST_E_INVAL on overlap.  The paths are copied. */
+st_status st_files_open(const st_file_part *parts, size_t n, st_files_t **out);
+void st_files_close(st_files_t *files);
+/* Reads arena bytes [begin, begin + bytes) into host[0, bytes) with up to
+ * `threads` reader threads (0 or 1: the calling thread); bytes of the range
+ * that no part covers are left as they are.  Synchronous.  ST_E_INVAL when
+ * the range leaves the arena, ST_E_IO on a failed read. */
+st_status st_files_read(const st_files_t *files, uint64_t begin, uint64_t bytes, void *host,
+                        uint32_t threads);
+
 /* Materializes every output of the plan on `stream` (a cudaStream_t; NULL is
  * the legacy default stream), asynchronously, with no host synchronization.
  *   data_dev  device pointer to the data section (any alignment; the plan's
@@ -336,6 +369,24 @@ st_status st_stage_h2d(void *dst_dev, const void *src_host, uint64_t bytes, uint
  * st_materialize.  Returns without synchronizing. */
 st_status st_load(const void *data_host, void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
                   const float *scales, void *copy_stream, void *compute_stream);
+
+/* The disk -> pinned RAM -> device -> materialize pipeline: for each chunk of
+ * the plan (its chunk_bytes; one chunk when 0) reads the chunk's arena bytes
+ * from `files` into a slot of the host ring with `threads` reader threads,
+ * copies the slot to data_dev on copy_stream, and runs that chunk's pieces on
+ * compute_stream once its copy is done, so reading chunk k + 1 overlaps the
+ * copy and kernel of chunk k.  ring_host: ring_bytes of host memory, pinned
+ * for the copies to be asynchronous, holding at least one chunk (two or more
+ * for overlap); a slot is reused only after its previous copy finished.
+ * The first copy waits for work already queued on compute_stream.  Blocks
+ * the calling thread until every chunk is read and its copy finished (the
+ * ring is then free); the kernels may still be running on compute_stream.
+ * The plan's index must describe the files' arena (data_bytes = the arena
+ * size).  Errors: ST_E_INVAL (arguments, ring too small, arena size),
+ * ST_E_IO (reads), ST_E_CUDA. */
+st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t *plan,
+                        void *const *dst_ptrs, const float *scales, void *ring_host, uint64_t ring_bytes,
+                        uint32_t threads, void *copy_stream, void *compute_stream);
 
 /* Allocation-free st_materialize.  No counterpart on the pages: it exists for
  * callers that cannot allocate device memory, for example code running while a

@@ -586,8 +586,8 @@ const char *st_status_name(st_status s) {
   static const char *const n[] = {"ST_OK",       "ST_E_INVAL",    "ST_E_TRUNCATED", "ST_E_HEADER_JSON",
                                   "ST_E_HEADER_TOO_LARGE", "ST_E_DUP_KEY", "ST_E_DTYPE", "ST_E_SHAPE",
                                   "ST_E_OFFSETS", "ST_E_NOT_FOUND", "ST_E_UNSUPPORTED_CAST",
-                                  "ST_E_ALIGN",  "ST_E_NOMEM",    "ST_E_CUDA",      "ST_E_DEVICE"};
-  return (s >= 0 && s <= ST_E_DEVICE) ? n[s] : "ST_E_UNKNOWN";
+                                  "ST_E_ALIGN",  "ST_E_NOMEM",    "ST_E_CUDA",      "ST_E_DEVICE", "ST_E_IO"};
+  return (s >= 0 && s <= ST_E_IO) ? n[s] : "ST_E_UNKNOWN";
 }
 
 size_t st_dtype_size(st_dtype d) { return dtype_size(d); }

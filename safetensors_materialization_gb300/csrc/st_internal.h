@@ -154,6 +154,10 @@ st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;
 st_status static_scratch(void **addr);
 
+// Shard-file reads (st_io.cpp): arena bytes [begin, begin + bytes) into host.
+st_status read_arena(const st_files_s *f, uint64_t begin, uint64_t bytes, void *host, uint32_t threads);
+uint64_t files_arena_bytes(const st_files_s *f);
+
 // Error reporting shared by the host files.
 st_status set_error(st_status s, const char *fmt, ...);
 

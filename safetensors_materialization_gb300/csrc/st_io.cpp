@@ -1,0 +1,212 @@
+// st_io.cpp -- range reads of safetensors shard files into host memory.
+//
+// "Disk tier safetensors streaming design audit (ComfyUI)", "Range reads and
+// tiering": a tensor's bytes are read from disk into (optionally pinned) host
+// memory and copied to the GPU, without reading the rest of the file.  Here a
+// set of shard files is addressed as one arena (the layout st_index_concat
+// gives): arena byte x of part k lives at file offset offset_k + (x - base_k).
+// Reads use pread on host threads; the disk -> pinned -> device -> materialize
+// pipeline built on them is st_load_files (st_plan.cpp).
+#include <fcntl.h>
+#include <sys/stat.h>
+#include <unistd.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cerrno>
+#include <cstring>
+#include <memory>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "st_internal.h"
+
+struct st_files_s {
+  struct Part {
+    std::string path;
+    int fd = -1;
+    uint64_t offset = 0, bytes = 0, base = 0;
+  };
+  std::vector<Part> parts;  // sorted by base, non-overlapping
+  uint64_t arena_bytes = 0;
+  ~st_files_s() {
+    for (Part &p : parts)
+      if (p.fd >= 0) close(p.fd);
+  }
+};
+
+namespace stmat {
+
+namespace {
+
+// pread until `n` bytes arrived; false on an error or end of file.
+bool pread_all(int fd, uint8_t *dst, uint64_t n, uint64_t off, int *err) {
+  while (n) {
+    const size_t want = static_cast<size_t>(std::min<uint64_t>(n, 1ull << 30));
+    const ssize_t got = pread(fd, dst, want, static_cast<off_t>(off));
+    if (got < 0) {
+      if (errno == EINTR) continue;
+      *err = errno;
+      return false;
+    }
+    if (got == 0) {
+      *err = 0;  // the file ended early
+      return false;
+    }
+    dst += got;
+    off += static_cast<uint64_t>(got);
+    n -= static_cast<uint64_t>(got);
+  }
+  return true;
+}
+
+// Arena bytes [lo, hi) into host + (lo - begin), one thread's share.
+bool read_span(const st_files_s &f, uint64_t begin, uint64_t lo, uint64_t hi, uint8_t *host, std::string *msg) {
+  for (const auto &p : f.parts) {
+    const uint64_t a = std::max(lo, p.base), b = std::min(hi, p.base + p.bytes);
+    if (a >= b) continue;
+    int err = 0;
+    if (!pread_all(p.fd, host + (a - begin), b - a, p.offset + (a - p.base), &err)) {
+      *msg = "reading " + std::to_string(b - a) + " bytes at " + std::to_string(p.offset + (a - p.base)) + " of " +
+             p.path + ": " + (err ? std::strerror(err) : "the file ended early");
+      return false;
+    }
+  }
+  return true;
+}
+
+}  // namespace
+
+st_status read_arena(const st_files_s *f, uint64_t begin, uint64_t bytes, void *host, uint32_t threads) {
+  if (!f || (bytes && !host)) return set_error(ST_E_INVAL, "NULL argument");
+  if (begin > f->arena_bytes || bytes > f->arena_bytes - begin)
+    return set_error(ST_E_INVAL, "range %llu + %llu is beyond the %llu-byte arena", (unsigned long long)begin,
+                     (unsigned long long)bytes, (unsigned long long)f->arena_bytes);
+  if (!bytes) return ST_OK;
+  uint8_t *dst = static_cast<uint8_t *>(host);
+  // Split in up to `threads` spans of whole 1 MiB blocks.
+  constexpr uint64_t kBlock = 1ull << 20;
+  const uint64_t blocks = (bytes + kBlock - 1) / kBlock;
+  const uint32_t t = static_cast<uint32_t>(std::max<uint64_t>(1, std::min<uint64_t>(threads ? threads : 1, blocks)));
+  if (t == 1) {
+    std::string msg;
+    if (!read_span(*f, begin, begin, begin + bytes, dst, &msg)) return set_error(ST_E_IO, "%s", msg.c_str());
+    return ST_OK;
+  }
+  std::vector<std::string> msgs(t);
+  std::atomic<bool> ok{true};
+  std::vector<std::thread> pool;
+  try {
+    for (uint32_t i = 0; i < t; ++i) {
+      const uint64_t lo = begin + std::min(bytes, blocks * i / t * kBlock);
+      const uint64_t hi = begin + std::min(bytes, blocks * (i + 1) / t * kBlock);
+      pool.emplace_back([&, i, lo, hi] {
+        if (!read_span(*f, begin, lo, hi, dst, &msgs[i])) ok = false;
+      });
+    }
+  } catch (const std::exception &) {
+    for (auto &th : pool) th.join();
+    return set_error(ST_E_NOMEM, "starting %u reader threads", t);
+  }
+  for (auto &th : pool) th.join();
+  if (!ok) {
+    for (const auto &m : msgs)
+      if (!m.empty()) return set_error(ST_E_IO, "%s", m.c_str());
+  }
+  return ST_OK;
+}
+
+uint64_t files_arena_bytes(const st_files_s *f) { return f->arena_bytes; }
+
+}  // namespace stmat
+
+using namespace stmat;
+
+extern "C" {
+
+st_status st_index_open(const char *path, st_index_t **out, uint64_t *data_offset) {
+  if (!path || !out) return set_error(ST_E_INVAL, "NULL argument");
+  *out = nullptr;
+  const int fd = open(path, O_RDONLY | O_CLOEXEC);
+  if (fd < 0) return set_error(ST_E_IO, "opening %s: %s", path, std::strerror(errno));
+  struct FdGuard {
+    int fd;
+    ~FdGuard() { close(fd); }
+  } guard{fd};
+  struct stat sb;
+  if (fstat(fd, &sb) != 0) return set_error(ST_E_IO, "stat %s: %s", path, std::strerror(errno));
+  const uint64_t size = static_cast<uint64_t>(sb.st_size);
+  uint8_t first[8];
+  int err = 0;
+  if (size < 8 || !pread_all(fd, first, 8, 0, &err))
+    return set_error(ST_E_TRUNCATED, "%s holds %llu bytes, fewer than the 8-byte header length", path,
+                     (unsigned long long)size);
+  uint64_t n = 0;
+  st_status s = st_header_size(first, 8, &n);
+  if (s != ST_OK) return s;
+  if (n > size - 8)
+    return set_error(ST_E_TRUNCATED, "%s: header of %llu bytes but only %llu follow", path, (unsigned long long)n,
+                     (unsigned long long)(size - 8));
+  std::vector<uint8_t> hdr;
+  try {
+    hdr.resize(8 + n);
+  } catch (const std::bad_alloc &) {
+    return set_error(ST_E_NOMEM, "out of host memory");
+  }
+  std::memcpy(hdr.data(), first, 8);
+  if (n && !pread_all(fd, hdr.data() + 8, n, 8, &err))
+    return set_error(ST_E_IO, "reading the header of %s: %s", path, err ? std::strerror(err) : "the file ended early");
+  s = st_index_build(hdr.data(), hdr.size(), size - 8 - n, out);
+  if (s == ST_OK && data_offset) *data_offset = 8 + n;
+  return s;
+}
+
+st_status st_files_open(const st_file_part *parts, size_t n, st_files_t **out) {
+  if (!out || (n && !parts)) return set_error(ST_E_INVAL, "NULL argument");
+  *out = nullptr;
+  std::unique_ptr<st_files_s> f(new (std::nothrow) st_files_s);
+  if (!f) return set_error(ST_E_NOMEM, "out of host memory");
+  try {
+    for (size_t k = 0; k < n; ++k) {
+      const st_file_part &p = parts[k];
+      if (!p.path) return set_error(ST_E_INVAL, "NULL path of part %zu", k);
+      if (p.base + p.bytes < p.base || p.offset + p.bytes < p.offset)
+        return set_error(ST_E_INVAL, "part %zu overflows 64 bits", k);
+      st_files_s::Part q;
+      q.path = p.path;
+      q.offset = p.offset;
+      q.bytes = p.bytes;
+      q.base = p.base;
+      q.fd = open(p.path, O_RDONLY | O_CLOEXEC);
+      if (q.fd < 0) return set_error(ST_E_IO, "opening %s: %s", p.path, std::strerror(errno));
+      f->parts.push_back(std::move(q));
+      struct stat sb;
+      if (fstat(f->parts.back().fd, &sb) != 0) return set_error(ST_E_IO, "stat %s: %s", p.path, std::strerror(errno));
+      if (static_cast<uint64_t>(sb.st_size) < p.offset + p.bytes)
+        return set_error(ST_E_IO, "%s holds %llu bytes; part %zu needs %llu", p.path, (unsigned long long)sb.st_size,
+                         k, (unsigned long long)(p.offset + p.bytes));
+    }
+    std::sort(f->parts.begin(), f->parts.end(),
+              [](const st_files_s::Part &a, const st_files_s::Part &b) { return a.base < b.base; });
+    for (size_t k = 0; k < f->parts.size(); ++k) {
+      const auto &p = f->parts[k];
+      if (k && f->parts[k - 1].base + f->parts[k - 1].bytes > p.base)
+        return set_error(ST_E_INVAL, "parts overlap in the arena at %llu", (unsigned long long)p.base);
+      f->arena_bytes = std::max(f->arena_bytes, p.base + p.bytes);
+    }
+  } catch (const std::bad_alloc &) {
+    return set_error(ST_E_NOMEM, "out of host memory");
+  }
+  *out = f.release();
+  return ST_OK;
+}
+
+void st_files_close(st_files_t *files) { delete files; }
+
+st_status st_files_read(const st_files_t *files, uint64_t begin, uint64_t bytes, void *host, uint32_t threads) {
+  return read_arena(files, begin, bytes, host, threads);
+}
+
+}  // extern "C"

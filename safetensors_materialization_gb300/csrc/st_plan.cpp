@@ -864,6 +864,64 @@ st_status st_load(const void *data_host, void *data_dev, const st_plan_t *p, voi
   return ST_OK;
 }
 
+st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t *p, void *const *dst_ptrs,
+                        const float *scales, void *ring_host, uint64_t ring_bytes, uint32_t threads,
+                        void *copy_stream, void *compute_stream) {
+  if (!p || !files) return set_error(ST_E_INVAL, "NULL plan or files");
+  st_status s = check_device_plan(p);
+  if (s != ST_OK) return s;
+  const uint64_t data = p->index->core->data_bytes;
+  if (files_arena_bytes(files) != data)
+    return set_error(ST_E_INVAL, "the files' arena (%llu bytes) is not the plan's data section (%llu bytes)",
+                     (unsigned long long)files_arena_bytes(files), (unsigned long long)data);
+  if ((data && (!data_dev || !ring_host)) || !dst_ptrs) return set_error(ST_E_INVAL, "NULL pointer");
+  s = check_tma_source(p, data_dev);
+  if (s != ST_OK) return s;
+  const uint64_t C = p->chunk_bytes ? p->chunk_bytes : (data ? data : 1);
+  const uint64_t slots = ring_bytes / C;
+  if (data && slots == 0)
+    return set_error(ST_E_INVAL, "the ring (%llu bytes) holds no %llu-byte chunk", (unsigned long long)ring_bytes,
+                     (unsigned long long)C);
+  cudaStream_t cs = static_cast<cudaStream_t>(copy_stream), ks = static_cast<cudaStream_t>(compute_stream);
+  cudaEvent_t start = p->events[p->n_chunks];
+  cudaError_t e = cudaEventRecord(start, ks);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, start, 0);
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "ordering the copy stream: %s", cuda_msg(e).c_str());
+  uint8_t *ring = static_cast<uint8_t *>(ring_host);
+  for (uint32_t k = 0; k < p->n_chunks; ++k) {
+    const uint64_t off = static_cast<uint64_t>(k) * C;
+    const uint64_t n = off < data ? std::min(C, data - off) : 0;
+    uint8_t *slot = ring + (k % (slots ? slots : 1)) * C;
+    if (k >= slots && slots) {  // the slot's previous copy must be done
+      e = cudaEventSynchronize(p->events[k - slots]);
+      if (e != cudaSuccess) return set_error(ST_E_CUDA, "waiting for chunk %llu: %s", (unsigned long long)(k - slots),
+                                             cuda_msg(e).c_str());
+    }
+    if (n) {
+      const uint64_t arena = files_arena_bytes(files);
+      const uint64_t rn = off < arena ? std::min(n, arena - off) : 0;
+      if (rn) {
+        s = read_arena(files, off, rn, slot, threads);
+        if (s != ST_OK) return s;
+      }
+      e = cudaMemcpyAsync(static_cast<uint8_t *>(data_dev) + off, slot, n, cudaMemcpyHostToDevice, cs);
+      if (e != cudaSuccess)
+        return set_error(ST_E_CUDA, "copy of chunk %u (%llu bytes): %s", k, (unsigned long long)n, cuda_msg(e).c_str());
+    }
+    e = cudaEventRecord(p->events[k], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ks, p->events[k], 0);
+    if (e != cudaSuccess) return set_error(ST_E_CUDA, "chunk %u event: %s", k, cuda_msg(e).c_str());
+    s = launch_chunk(p, k, data_dev, dst_ptrs, scales, compute_stream);
+    if (s != ST_OK) return s;
+  }
+  // The ring is free once the last copies finished.
+  for (uint32_t k = p->n_chunks > slots ? static_cast<uint32_t>(p->n_chunks - slots) : 0; k < p->n_chunks; ++k) {
+    e = cudaEventSynchronize(p->events[k]);
+    if (e != cudaSuccess) return set_error(ST_E_CUDA, "waiting for chunk %u: %s", k, cuda_msg(e).c_str());
+  }
+  return ST_OK;
+}
+
 st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *p, void *const *dst_ptrs,
                                  const float *scales, void *stream) {
   if (!p) return set_error(ST_E_INVAL, "NULL plan");

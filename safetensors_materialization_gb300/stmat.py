@@ -21,7 +21,7 @@ DTYPES = ["BOOL", "U8", "I8", "I16", "U16", "I32", "U32", "I64", "U64", "F16", "
           "F8_E4M3", "F8_E5M2", "KEEP"]
 STATUS = ["ST_OK", "ST_E_INVAL", "ST_E_TRUNCATED", "ST_E_HEADER_JSON", "ST_E_HEADER_TOO_LARGE",
           "ST_E_DUP_KEY", "ST_E_DTYPE", "ST_E_SHAPE", "ST_E_OFFSETS", "ST_E_NOT_FOUND",
-          "ST_E_UNSUPPORTED_CAST", "ST_E_ALIGN", "ST_E_NOMEM", "ST_E_CUDA", "ST_E_DEVICE"]
+          "ST_E_UNSUPPORTED_CAST", "ST_E_ALIGN", "ST_E_NOMEM", "ST_E_CUDA", "ST_E_DEVICE", "ST_E_IO"]
 
 # Every symbol the C ABI exports (include/stmat.h).
 EXPORTS = [
@@ -31,7 +31,8 @@ EXPORTS = [
     "st_plan",
     "st_plan_free", "st_plan_count", "st_plan_output", "st_plan_arena", "st_plan_stats",
     "st_plan_piece", "st_plan_worker", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
-    "st_materialize_noalloc",
+    "st_materialize_noalloc", "st_index_open", "st_files_open", "st_files_close", "st_files_read",
+    "st_load_files",
     "st_last_error", "st_status_name", "st_dtype_size", "st_dtype_name", "st_version",
 ]
 
@@ -58,6 +59,10 @@ class OutputInfo(C.Structure):
 
 class Slice(C.Structure):
     _fields_ = [("dim", C.c_int32), ("start", C.c_int64), ("stop", C.c_int64)]
+
+
+class FilePart(C.Structure):
+    _fields_ = [("path", C.c_char_p), ("offset", C.c_uint64), ("bytes", C.c_uint64), ("base", C.c_uint64)]
 
 
 class BlockQuant(C.Structure):
@@ -122,12 +127,16 @@ def lib():
             "st_stage_h2d": [P, P, U64, U64, P, P],
             "st_load": [P, P, P, P, P, P, P],
             "st_plan_check": [P, P, C.POINTER(U32)],
+            "st_index_open": [C.c_char_p, PP, C.POINTER(U64)],
+            "st_files_open": [C.POINTER(FilePart), S, PP],
+            "st_files_read": [P, U64, U64, P, U32],
+            "st_load_files": [P, P, P, P, P, P, U64, U32, P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
             f.argtypes = args
             f.restype = I
-        for name in ("st_index_free", "st_plan_free"):
+        for name in ("st_index_free", "st_plan_free", "st_files_close"):
             getattr(L, name).argtypes = [P]
             getattr(L, name).restype = None
         L.st_last_error.restype = C.c_char_p
@@ -270,6 +279,14 @@ class Index:
         return Index(out.value)
 
     @classmethod
+    def open(cls, path):
+        """st_index_open: the index of a file on disk (reads its header only);
+        returns (index, data-section offset in the file)."""
+        out, off = C.c_void_p(), C.c_uint64()
+        _check(lib().st_index_open(os.fsencode(path), C.byref(out), C.byref(off)))
+        return cls(out.value), off.value
+
+    @classmethod
     def concat(cls, parts, align=256):
         """st_index_concat: one index over shard indexes; returns (index, bases),
         shard k's data section belonging at arena offset bases[k]."""
@@ -318,6 +335,42 @@ class Index:
         out = C.c_void_p()
         _check(lib().st_plan(self._h, C.byref(sel), DTYPES.index(dst), C.byref(opts), C.byref(out)))
         return Plan(out.value, self)
+
+
+class Files:
+    """st_files_t: shard files addressed as one arena.  parts: (path, file
+    offset of the data section, bytes, arena base) per file."""
+
+    def __init__(self, parts):
+        self._paths = [os.fsencode(p[0]) for p in parts]
+        arr = (FilePart * max(1, len(parts)))()
+        for i, (path, off, n, base) in enumerate(parts):
+            arr[i] = FilePart(self._paths[i], off, n, base)
+        out = C.c_void_p()
+        _check(lib().st_files_open(arr, len(parts), C.byref(out)))
+        self._h = C.c_void_p(out.value)
+
+    @classmethod
+    def of_checkpoint(cls, paths, align=256):
+        """Opens the shard files of one checkpoint: returns (Files, joined
+        Index) with each shard's data section at its st_index_concat base."""
+        opened = [Index.open(p) for p in paths]
+        ix, bases = Index.concat([o[0] for o in opened], align)
+        parts = [(p, off, o.sizes()[1], b) for p, (o, off), b in zip(paths, opened, bases)]
+        return cls(parts), ix
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value and _lib is not None:
+            _lib.st_files_close(self._h)
+            self._h = C.c_void_p(None)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def read(self, begin, nbytes, host, threads=4):
+        """st_files_read into `host` (a numpy uint8 array or torch tensor)."""
+        _check(lib().st_files_read(self._h, begin, nbytes, _addr(host), threads))
 
 
 class Plan:
@@ -393,6 +446,16 @@ class Plan:
         """st_load: staged copy of the data section overlapped with materialize."""
         _check(lib().st_load(_addr(data_host), _addr(data_dev), self._h, _addr(dst_ptrs), _addr(scales),
                              _stream(copy_stream), _stream(compute_stream)))
+
+    def load_files(self, files, data_dev, dst_ptrs, ring_host, ring_bytes=None, threads=8, scales=None,
+                   copy_stream=None, compute_stream=None):
+        """st_load_files: disk -> pinned ring -> device, each chunk materialized
+        as soon as it lands."""
+        if ring_bytes is None:
+            ring_bytes = ring_host.numel() if hasattr(ring_host, "numel") else len(ring_host)
+        _check(lib().st_load_files(files.handle, _addr(data_dev), self._h, _addr(dst_ptrs), _addr(scales),
+                                   _addr(ring_host), ring_bytes, threads, _stream(copy_stream),
+                                   _stream(compute_stream)))
 
     def check(self, stream=None):
         flags = C.c_uint32()

@@ -1,0 +1,136 @@
+"""Shard files on disk: st_index_open (header only), st_files_open/read
+(range reads with pread, several threads) against the bytes the files were
+written from, the error statuses, and (GPU) st_load_files, the disk -> pinned
+-> device -> materialize pipeline, against the oracle.
+
+"Disk tier safetensors streaming design audit (ComfyUI)", "Range reads and
+tiering": Disk->RAM->GPU reads only the ranges asked for into (pinned) host
+memory and copies them to the GPU."""
+import os
+
+import numpy as np
+import pytest
+
+from safetensors_materialization_gb300 import synth
+
+
+def write_shards(tmp_path, w):
+    """Writes every shard of workload `w`; returns (paths, data sections)."""
+    paths, datas = [], []
+    for k, lay in enumerate(w.files):
+        img = synth.build_workload_file(w, k)
+        path = os.path.join(tmp_path, f"shard{k}.safetensors")
+        img.tofile(path)
+        paths.append(path)
+        datas.append(img[lay.data_start:])
+    return paths, datas
+
+
+def small_llm():
+    return synth.llm8b(seed=7, layers=4, hidden=128, inter=352, vocab=500, kv=32, shards=4)
+
+
+def test_index_open_reads_only_the_header(stmat, oracle, tmp_path):
+    w = small_llm()
+    paths, datas = write_shards(str(tmp_path), w)
+    for path, lay in zip(paths, w.files):
+        ix, off = stmat.Index.open(path)
+        assert off == lay.data_start
+        assert ix.sizes() == (lay.header_len, lay.data_bytes)
+        assert ix.entries() == stmat.Index.from_header(lay.header, lay.data_bytes).entries()
+
+
+@pytest.mark.parametrize("threads", [1, 3, 8])
+def test_files_read_the_joined_arena(stmat, tmp_path, threads):
+    w = small_llm()
+    paths, datas = write_shards(str(tmp_path), w)
+    files, ix = stmat.Files.of_checkpoint(paths)
+    _, bases = stmat.Index.concat([stmat.Index.open(p)[0] for p in paths])
+    total = ix.sizes()[1]
+    want = np.zeros(total, np.uint8)
+    for b, d in zip(bases, datas):
+        want[b:b + d.size] = d
+    got = np.zeros(total, np.uint8)
+    files.read(0, total, got, threads=threads)
+    assert np.array_equal(got, want)
+    rng = np.random.Generator(np.random.PCG64(threads))
+    for _ in range(20):                       # ranges crossing shard boundaries
+        a = int(rng.integers(0, total))
+        n = int(rng.integers(0, min(3 << 20, total - a) + 1))
+        part = np.full(n, 0xEE, np.uint8)
+        files.read(a, n, part, threads=threads)
+        # gap bytes between shards are left untouched
+        ref = want[a:a + n].copy()
+        covered = np.zeros(total, bool)
+        for b, d in zip(bases, datas):
+            covered[b:b + d.size] = True
+        ref[~covered[a:a + n]] = 0xEE
+        assert np.array_equal(part, ref)
+
+
+def test_file_errors(stmat, tmp_path):
+    w = small_llm()
+    paths, datas = write_shards(str(tmp_path), w)
+    with pytest.raises(stmat.StmatError) as e:
+        stmat.Index.open(os.path.join(str(tmp_path), "missing.safetensors"))
+    assert e.value.status == "ST_E_IO"
+    short = os.path.join(str(tmp_path), "short.safetensors")
+    with open(paths[0], "rb") as f:
+        head = f.read(100)
+    with open(short, "wb") as f:
+        f.write(head)
+    with pytest.raises(stmat.StmatError) as e:
+        stmat.Index.open(short)
+    assert e.value.status == "ST_E_TRUNCATED"
+    size0 = os.path.getsize(paths[0])
+    with pytest.raises(stmat.StmatError) as e:          # the file is shorter than the part
+        stmat.Files([(paths[0], 0, size0 + 1, 0)])
+    assert e.value.status == "ST_E_IO"
+    with pytest.raises(stmat.StmatError) as e:          # parts overlap in the arena
+        stmat.Files([(paths[0], 0, 100, 0), (paths[1], 0, 100, 50)])
+    assert e.value.status == "ST_E_INVAL"
+    files = stmat.Files([(paths[0], 0, 100, 0)])
+    with pytest.raises(stmat.StmatError) as e:          # beyond the arena
+        files.read(50, 51, np.zeros(51, np.uint8))
+    assert e.value.status == "ST_E_INVAL"
+    # a file truncated after opening: the read fails with the OS's story
+    victim = os.path.join(str(tmp_path), "victim.safetensors")
+    with open(paths[1], "rb") as f:
+        blob = f.read()
+    with open(victim, "wb") as f:
+        f.write(blob)
+    files = stmat.Files([(victim, 0, len(blob), 0)])
+    os.truncate(victim, len(blob) // 2)
+    with pytest.raises(stmat.StmatError) as e:
+        files.read(0, len(blob), np.zeros(len(blob), np.uint8), threads=2)
+    assert e.value.status == "ST_E_IO"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("chunk,slots", [(0, 1), (1 << 16, 2), (1 << 20, 3), (3 << 20, 2)])
+def test_load_files_matches_oracle(stmat, oracle, tmp_path, chunk, slots):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    w = small_llm()
+    paths, datas = write_shards(str(tmp_path), w)
+    files, ix = stmat.Files.of_checkpoint(paths)
+    total = ix.sizes()[1]
+    for dst in ("BF16", "F16"):
+        plan = ix.plan(dst=dst, chunk_bytes=chunk)
+        C = chunk or total
+        ring = torch.empty(C * slots, dtype=torch.uint8).pin_memory()
+        dev = torch.empty(total, dtype=torch.uint8, device="cuda")
+        outs = stmat.Outputs(plan)
+        copy = torch.cuda.Stream()
+        plan.load_files(files, dev, outs.ptrs, ring, threads=4, copy_stream=copy,
+                        compute_stream=torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        oix, obases = oracle.concat([oracle.parse_header(l.header, l.data_bytes) for l in w.files])
+        arena = np.zeros(total, np.uint8)
+        for b, d in zip(obases, datas):
+            arena[b:b + d.size] = d
+        sel = oix.select(dst=dst)
+        for i in range(len(sel)):
+            assert np.array_equal(outs.raw(i).cpu().numpy(), sel.materialize(i, arena)), sel.output(i)["name"]
