@@ -78,6 +78,7 @@ typedef enum st_dtype {
 typedef struct st_index st_index_t; /* a parsed header, or a view of one */
 typedef struct st_plan_s st_plan_t; /* a selection turned into device work */
 typedef struct st_files_s st_files_t; /* open shard files addressed as one arena */
+typedef struct st_cache_s st_cache_t; /* LRU RAM tier of host copies of file ranges */
 
 /* ---------------------------------------------------------------- header */
 
@@ -369,6 +370,57 @@ st_status st_stage_h2d(void *dst_dev, const void *src_host, uint64_t bytes, uint
  * st_materialize.  Returns without synchronizing. */
 st_status st_load(const void *data_host, void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
                   const float *scales, void *copy_stream, void *compute_stream);
+
+/* ------------------------------------------------------------ RAM tier */
+/* "Disk tier integration" (Disk tier safetensors streaming design audit):
+ * an LRU cache of host copies of tensors read from disk with a configurable
+ * maximum number of bytes; eviction drops a host copy (the index still
+ * describes the tensor, which is read again on its next use).  Thread-safe. */
+
+typedef struct st_cache_info {
+  uint64_t bytes, max_bytes;   /* bytes held by kept entries, and the bound */
+  uint64_t entries;            /* kept entries */
+  uint64_t hits, misses, evictions;
+} st_cache_info;
+
+/* pinned != 0: entries live in page-locked memory (cudaHostAlloc), so
+ * copies from them to the GPU are asynchronous; else pageable malloc. */
+st_status st_cache_create(uint64_t max_bytes, int32_t pinned, st_cache_t **out);
+/* Frees every entry, held or not: release all holds first. */
+void st_cache_free(st_cache_t *cache);
+/* The host copy of arena bytes [begin, begin + bytes) of `files`: a hit
+ * returns the kept copy (now the most recently used); a miss reads it with
+ * pread (`threads` reader threads), evicting least-recently-used entries
+ * that nobody holds until it fits the bound.  The entry is held, and *host
+ * stays valid, until st_cache_release(cache, *host).  An entry larger than
+ * the bound is read but not kept: it is freed on release.  Errors: ST_E_INVAL,
+ * ST_E_NOMEM, ST_E_IO. */
+st_status st_cache_get(st_cache_t *cache, const st_files_t *files, uint64_t begin, uint64_t bytes,
+                       uint32_t threads, const void **host);
+st_status st_cache_release(st_cache_t *cache, const void *host);
+st_status st_cache_stats(const st_cache_t *cache, st_cache_info *info);
+/* Drops every entry nobody holds. */
+st_status st_cache_clear(st_cache_t *cache);
+
+/* The lazy path for a few tensors ("Streaming safetensors mapping": a tensor
+ * is loaded when it is accessed): the selected outputs of `sel` on `index`
+ * (whose offsets are the arena of `files`), with the tensors they read
+ * (their scales and block scales), are taken from `cache` (read from the
+ * files on a miss; cache may be NULL: a plain read), copied into staging_dev
+ * (each at a 256-byte aligned offset; staging_bytes must hold them all, else
+ * ST_E_INVAL with the size needed) and materialized by one launch on
+ * `stream`, with the plan's tables in the library's static device array as
+ * for st_materialize_noalloc (no device allocation; calls whose work
+ * overlaps on the GPU race on that array: order them on one stream).
+ *   dst_host_ptrs  HOST array of one destination (device) pointer per output,
+ *                  in the selection's output order; each non-NULL and aligned
+ *                  to the output's itemsize (ST_E_INVAL otherwise).
+ * Blocks until the staging copies are done (the cache entries are then
+ * released); the kernel runs asynchronously on `stream`.  Output dtypes,
+ * errors and bit-exact results are those of st_plan + st_materialize. */
+st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_cache_t *cache,
+                          const st_selection *sel, st_dtype dst_dtype, void *const *dst_host_ptrs,
+                          void *staging_dev, uint64_t staging_bytes, uint32_t threads, void *stream);
 
 /* The disk -> pinned RAM -> device -> materialize pipeline: for each chunk of
  * the plan (its chunk_bytes; one chunk when 0) reads the chunk's arena bytes

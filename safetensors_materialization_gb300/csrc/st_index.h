@@ -41,6 +41,10 @@ struct IndexData {
 };
 
 size_t dtype_size(int dtype);
+// A root index over `core` (positions = core order), and the name lookup of
+// an index or view (ST_E_DUP_KEY on a repeated name).
+std::shared_ptr<IndexData> make_root(std::shared_ptr<const Core> core);
+st_status finish_view(IndexData *d);
 const IndexData *index_data(const st_index *ix);
 std::shared_ptr<const IndexData> index_ref(const st_index *ix);
 

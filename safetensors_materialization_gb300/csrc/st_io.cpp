@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cerrno>
+#include <cstdlib>
 #include <cstring>
 #include <memory>
 #include <new>
@@ -207,6 +208,173 @@ void st_files_close(st_files_t *files) { delete files; }
 
 st_status st_files_read(const st_files_t *files, uint64_t begin, uint64_t bytes, void *host, uint32_t threads) {
   return read_arena(files, begin, bytes, host, threads);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------ RAM tier
+//
+// "Disk tier integration": an LRU cache of host copies of tensors read from
+// disk, bounded by a configurable number of bytes; evicting an entry drops
+// the host copy (the tensor stays described by the index and is read again
+// on its next use).  An entry is keyed by (files, arena range); get() holds
+// it until release(), and held entries are never evicted.  An entry larger
+// than the bound is read but not kept (dropped on release).
+
+#include <cuda_runtime_api.h>
+
+#include <list>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+struct st_cache_s {
+  struct Entry {
+    const st_files_s *files;
+    uint64_t begin, bytes;
+    uint8_t *host = nullptr;
+    uint32_t holds = 0;
+    bool kept = true;  // counted in `bytes` and listed in the LRU order
+  };
+  using Key = std::tuple<const st_files_s *, uint64_t, uint64_t>;
+  uint64_t max_bytes = 0, bytes = 0, hits = 0, misses = 0, evictions = 0;
+  bool pinned = false;
+  std::mutex mu;
+  std::list<Entry> lru;                                  // front = most recently used
+  std::map<Key, std::list<Entry>::iterator> by_key;
+  std::map<const void *, std::list<Entry>::iterator> by_ptr;
+  std::list<Entry> transient;                            // too large to keep
+
+  uint8_t *alloc(uint64_t n) {
+    void *p = nullptr;
+    if (pinned) {
+      if (cudaHostAlloc(&p, n ? n : 1, cudaHostAllocDefault) != cudaSuccess) return nullptr;
+    } else {
+      p = std::malloc(n ? n : 1);
+    }
+    return static_cast<uint8_t *>(p);
+  }
+  void dealloc(uint8_t *p) {
+    if (!p) return;
+    if (pinned) cudaFreeHost(p);
+    else std::free(p);
+  }
+  // Evicts least-recently-used unheld entries until `need` more bytes fit.
+  void make_room(uint64_t need) {
+    for (auto it = lru.end(); bytes + need > max_bytes && it != lru.begin();) {
+      --it;
+      if (it->holds) continue;
+      bytes -= it->bytes;
+      ++evictions;
+      by_key.erase(Key(it->files, it->begin, it->bytes));
+      by_ptr.erase(it->host);
+      dealloc(it->host);
+      it = lru.erase(it);
+    }
+  }
+  ~st_cache_s() {
+    for (Entry &e : lru) dealloc(e.host);
+    for (Entry &e : transient) dealloc(e.host);
+  }
+};
+
+extern "C" {
+
+st_status st_cache_create(uint64_t max_bytes, int32_t pinned, st_cache_t **out) {
+  if (!out) return set_error(ST_E_INVAL, "NULL out");
+  st_cache_s *c = new (std::nothrow) st_cache_s;
+  if (!c) return set_error(ST_E_NOMEM, "out of host memory");
+  c->max_bytes = max_bytes;
+  c->pinned = pinned != 0;
+  *out = c;
+  return ST_OK;
+}
+
+void st_cache_free(st_cache_t *cache) { delete cache; }
+
+st_status st_cache_get(st_cache_t *c, const st_files_t *files, uint64_t begin, uint64_t bytes, uint32_t threads,
+                       const void **host) {
+  if (!c || !files || !host) return set_error(ST_E_INVAL, "NULL argument");
+  *host = nullptr;
+  std::lock_guard<std::mutex> lock(c->mu);
+  const st_cache_s::Key key(files, begin, bytes);
+  auto hit = c->by_key.find(key);
+  if (hit != c->by_key.end()) {
+    ++c->hits;
+    c->lru.splice(c->lru.begin(), c->lru, hit->second);  // most recent
+    ++hit->second->holds;
+    *host = hit->second->host;
+    return ST_OK;
+  }
+  ++c->misses;
+  st_cache_s::Entry e;
+  e.files = files;
+  e.begin = begin;
+  e.bytes = bytes;
+  e.kept = bytes <= c->max_bytes;
+  if (e.kept) c->make_room(bytes);
+  e.host = c->alloc(bytes);
+  if (!e.host) return set_error(ST_E_NOMEM, "allocating %llu bytes of %s host memory", (unsigned long long)bytes,
+                                c->pinned ? "pinned" : "pageable");
+  st_status s = read_arena(files, begin, bytes, e.host, threads);
+  if (s != ST_OK) {
+    c->dealloc(e.host);
+    return s;
+  }
+  e.holds = 1;
+  try {
+    if (e.kept) {
+      c->lru.push_front(e);
+      c->by_key[key] = c->lru.begin();
+      c->by_ptr[e.host] = c->lru.begin();
+      c->bytes += bytes;
+    } else {
+      c->transient.push_front(e);
+      c->by_ptr[e.host] = c->transient.begin();
+    }
+  } catch (const std::bad_alloc &) {
+    c->dealloc(e.host);
+    return set_error(ST_E_NOMEM, "out of host memory");
+  }
+  *host = e.host;
+  return ST_OK;
+}
+
+st_status st_cache_release(st_cache_t *c, const void *host) {
+  if (!c || !host) return set_error(ST_E_INVAL, "NULL argument");
+  std::lock_guard<std::mutex> lock(c->mu);
+  auto it = c->by_ptr.find(host);
+  if (it == c->by_ptr.end() || it->second->holds == 0)
+    return set_error(ST_E_INVAL, "%p is not a held cache entry", host);
+  auto e = it->second;
+  if (--e->holds == 0 && !e->kept) {
+    c->by_ptr.erase(it);
+    c->dealloc(e->host);
+    c->transient.erase(e);
+  }
+  return ST_OK;
+}
+
+st_status st_cache_stats(const st_cache_t *c, st_cache_info *info) {
+  if (!c || !info) return set_error(ST_E_INVAL, "NULL argument");
+  std::lock_guard<std::mutex> lock(const_cast<st_cache_s *>(c)->mu);
+  info->bytes = c->bytes;
+  info->max_bytes = c->max_bytes;
+  info->entries = c->lru.size();
+  info->hits = c->hits;
+  info->misses = c->misses;
+  info->evictions = c->evictions;
+  return ST_OK;
+}
+
+st_status st_cache_clear(st_cache_t *c) {
+  if (!c) return set_error(ST_E_INVAL, "NULL cache");
+  std::lock_guard<std::mutex> lock(c->mu);
+  const uint64_t keep = c->max_bytes;
+  c->max_bytes = 0;
+  c->make_room(0);
+  c->max_bytes = keep;
+  return ST_OK;
 }
 
 }  // extern "C"

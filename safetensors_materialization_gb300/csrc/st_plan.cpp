@@ -82,6 +82,7 @@ struct Output {
   uint32_t entry;      // core tensor
   int out_dtype;
   int64_t scale = -1;  // core tensor of the scale
+  std::vector<uint32_t> reads;  // view positions of every tensor the output reads (itself first)
   uint32_t cls;
   uint64_t numel;      // output elements (after slicing)
   uint64_t units;      // counted units (elements, or bytes for copies)
@@ -194,6 +195,7 @@ st_status check_quant(const IndexData &ix, uint32_t p, const st_block_quant &q, 
     if (g.dtype != ST_F32 || g.numel != 1)
       return set_error(ST_E_INVAL, "\"%s\": the global scale is a one-element F32 tensor", q.scale2);
     (*consumed)[it2->second] = 1;
+    o->reads.push_back(it2->second);
     o->quant.scale2 = g.begin;
     o->quant.row_units = static_cast<uint32_t>(t.shape[1]);
   }
@@ -201,6 +203,7 @@ st_status check_quant(const IndexData &ix, uint32_t p, const st_block_quant &q, 
   (*consumed)[sp] = 1;
   o->qkind = q.kind;
   o->qscale_entry = ix.ent[sp];
+  o->reads.push_back(sp);
   o->quant.scale = sc.begin;
   o->quant.scols = static_cast<uint32_t>(sc.shape[1]);
   o->quant.br_shift = log2_of(br);
@@ -299,6 +302,7 @@ st_status select_outputs(const IndexData &ix, const st_selection *sel, int req, 
     const Tensor &t = core.tensors[ix.ent[pos[i]]];
     if (qout[i].qkind != ST_QUANT_NONE) {
       Output o = std::move(qout[i]);
+      o.reads.insert(o.reads.begin(), pos[i]);
       o.name = ix.names[pos[i]];
       o.pos = pos[i];
       o.entry = ix.ent[pos[i]];
@@ -324,6 +328,8 @@ st_status select_outputs(const IndexData &ix, const st_selection *sel, int req, 
     o.entry = ix.ent[pos[i]];
     o.out_dtype = od;
     o.scale = scale[i] >= 0 ? static_cast<int64_t>(ix.ent[scale[i]]) : -1;
+    o.reads.push_back(pos[i]);
+    if (scale[i] >= 0) o.reads.push_back(static_cast<uint32_t>(scale[i]));
     int c = class_of(t.dtype, od, o.scale >= 0);
     if (c < 0) return set_error(ST_E_UNSUPPORTED_CAST, "no conversion for \"%s\"", o.name.c_str());
     o.cls = static_cast<uint32_t>(c);
@@ -570,6 +576,69 @@ void build_pieces(st_plan_s *p) {
   }
 }
 
+// Selection, kernel build, warps and pieces of a plan (host side only).
+st_status plan_host(std::shared_ptr<const IndexData> index, const st_selection *sel, st_dtype dst_dtype,
+                    const st_plan_options *opts, st_plan_s *p) {
+  p->index = std::move(index);
+  st_status s = select_outputs(*p->index, sel, dst_dtype, &p->outs);
+  if (s != ST_OK) return s;
+  const bool host_only = opts && opts->host_only;
+  uint32_t workers = opts ? opts->workers : 0;
+  p->chunk_bytes = opts ? opts->chunk_bytes : 0;
+  if (opts && opts->unit_bytes) p->unit_bytes = opts->unit_bytes;
+  const uint32_t order = opts ? opts->order : 0;
+  if (order > 2) return set_error(ST_E_INVAL, "options.order must be 0, 1 or 2");
+  uint64_t cost = 0, traffic = 0, nonempty = 0;
+  for (const Output &o : p->outs) {
+    const uint64_t t = o.units * (cls_in_size(o.cls) + cls_out_size(o.cls));
+    cost += kPieceCost + t;
+    traffic += t;
+    nonempty += t > 0;
+  }
+  // Many small tensors: the TMA build (reads staged in shared memory, so a
+  // warp keeps kilobytes in flight whatever the tensor size); else the
+  // streaming build.
+  if (opts && opts->kernel) {
+    if (opts->kernel != kKernelStream && opts->kernel != kKernelLatency && opts->kernel != kKernelTma)
+      return set_error(ST_E_INVAL, "options.kernel must be 0, 1, 2 or 3");
+    p->kernel = opts->kernel;
+  } else {
+    p->kernel = nonempty && traffic / nonempty < kSmallOutputBytes ? kKernelTma : kKernelStream;
+  }
+  // Block-scaled outputs are only in the TMA build.
+  bool has_quant = false;
+  for (const Output &o : p->outs) has_quant = has_quant || o.qkind != ST_QUANT_NONE;
+  if (has_quant) {
+    if (opts && opts->kernel && opts->kernel != kKernelTma)
+      return set_error(ST_E_INVAL, "block-scaled outputs need the TMA build (options.kernel 0 or 3)");
+    p->kernel = kKernelTma;
+  }
+  // Unit order: the register builds run one class at a time (their
+  // per-class code is large, and mixing classes stalls on instruction
+  // fetch); the TMA build's code is small, and source order keeps DRAM
+  // rows local.
+  p->class_major = order == 2 || (order == 0 && p->kernel != kKernelTma);
+  int sms = 0, blocks = 0;
+  if (!host_only || workers == 0) {
+    if (host_only) return set_error(ST_E_INVAL, "a host-only plan needs options.workers");
+    s = kernel_occupancy(p->kernel, &sms, &blocks);
+    if (s != ST_OK) return s;
+    uint32_t bps = static_cast<uint32_t>(blocks);
+    if (opts && opts->blocks_per_sm) bps = std::min(bps, opts->blocks_per_sm);
+    else if (p->kernel == kKernelStream) bps = std::min(bps, kStreamBlocksPerSm);
+    if (workers == 0) workers = static_cast<uint32_t>(sms) * bps * kWarpsPerBlock;
+  }
+  // No more warps than the work can use.
+  uint64_t cap = std::max<uint64_t>(1, cost / kMinWorkerCost);
+  p->workers = static_cast<uint32_t>(std::min<uint64_t>(workers, cap));
+  build_pieces(p);
+  if (has_quant) {
+    p->quant.resize(p->outs.size());
+    for (size_t i = 0; i < p->outs.size(); ++i) p->quant[i] = p->outs[i].quant;
+  }
+  return ST_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -580,63 +649,9 @@ st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst
   *out = nullptr;
   try {
     auto p = std::make_unique<st_plan_s>();
-    p->index = index_ref(index);
-    st_status s = select_outputs(*p->index, sel, dst_dtype, &p->outs);
+    st_status s = plan_host(index_ref(index), sel, dst_dtype, opts, p.get());
     if (s != ST_OK) return s;
     const bool host_only = opts && opts->host_only;
-    uint32_t workers = opts ? opts->workers : 0;
-    p->chunk_bytes = opts ? opts->chunk_bytes : 0;
-    if (opts && opts->unit_bytes) p->unit_bytes = opts->unit_bytes;
-    const uint32_t order = opts ? opts->order : 0;
-    if (order > 2) return set_error(ST_E_INVAL, "options.order must be 0, 1 or 2");
-    uint64_t cost = 0, traffic = 0, nonempty = 0;
-    for (const Output &o : p->outs) {
-      const uint64_t t = o.units * (cls_in_size(o.cls) + cls_out_size(o.cls));
-      cost += kPieceCost + t;
-      traffic += t;
-      nonempty += t > 0;
-    }
-    // Many small tensors: the TMA build (reads staged in shared memory, so a
-    // warp keeps kilobytes in flight whatever the tensor size); else the
-    // streaming build.
-    if (opts && opts->kernel) {
-      if (opts->kernel != kKernelStream && opts->kernel != kKernelLatency && opts->kernel != kKernelTma)
-        return set_error(ST_E_INVAL, "options.kernel must be 0, 1, 2 or 3");
-      p->kernel = opts->kernel;
-    } else {
-      p->kernel = nonempty && traffic / nonempty < kSmallOutputBytes ? kKernelTma : kKernelStream;
-    }
-    // Block-scaled outputs are only in the TMA build.
-    bool has_quant = false;
-    for (const Output &o : p->outs) has_quant = has_quant || o.qkind != ST_QUANT_NONE;
-    if (has_quant) {
-      if (opts && opts->kernel && opts->kernel != kKernelTma)
-        return set_error(ST_E_INVAL, "block-scaled outputs need the TMA build (options.kernel 0 or 3)");
-      p->kernel = kKernelTma;
-    }
-    // Unit order: the register builds run one class at a time (their
-    // per-class code is large, and mixing classes stalls on instruction
-    // fetch); the TMA build's code is small, and source order keeps DRAM
-    // rows local.
-    p->class_major = order == 2 || (order == 0 && p->kernel != kKernelTma);
-    int sms = 0, blocks = 0;
-    if (!host_only || workers == 0) {
-      if (host_only) return set_error(ST_E_INVAL, "a host-only plan needs options.workers");
-      s = kernel_occupancy(p->kernel, &sms, &blocks);
-      if (s != ST_OK) return s;
-      uint32_t bps = static_cast<uint32_t>(blocks);
-      if (opts && opts->blocks_per_sm) bps = std::min(bps, opts->blocks_per_sm);
-      else if (p->kernel == kKernelStream) bps = std::min(bps, kStreamBlocksPerSm);
-      if (workers == 0) workers = static_cast<uint32_t>(sms) * bps * kWarpsPerBlock;
-    }
-    // No more warps than the work can use.
-    uint64_t cap = std::max<uint64_t>(1, cost / kMinWorkerCost);
-    p->workers = static_cast<uint32_t>(std::min<uint64_t>(workers, cap));
-    build_pieces(p.get());
-    if (has_quant) {
-      p->quant.resize(p->outs.size());
-      for (size_t i = 0; i < p->outs.size(); ++i) p->quant[i] = p->outs[i].quant;
-    }
     if (!host_only) {
       cudaError_t e = cudaGetDevice(&p->device);
       size_t pb = p->pieces.size() * sizeof(Piece), qb = p->parts.size() * sizeof(uint32_t);
@@ -790,6 +805,56 @@ st_status launch_chunk(const st_plan_t *p, uint32_t k, const void *data_dev, voi
   return launch_materialize(a, p->kernel, stream);
 }
 
+// Launches a plan whose tables live in the library's static device array:
+// pieces | warp ranges | block-scale table | destinations (when given on the
+// host) | error word, each 256-byte aligned, filled by stream-ordered copies.
+st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *dst_dev, void *const *dst_host,
+                        const float *scales, void *stream) {
+  const size_t pieces_bytes = p->pieces.size() * sizeof(Piece);
+  const size_t parts_off = (pieces_bytes + 255) & ~size_t(255);
+  const size_t parts_bytes = p->parts.size() * sizeof(uint32_t);
+  const size_t quant_off = (parts_off + parts_bytes + 255) & ~size_t(255);
+  const size_t quant_bytes = p->quant.size() * sizeof(QuantInfo);
+  const size_t dst_off = (quant_off + quant_bytes + 255) & ~size_t(255);
+  const size_t dst_bytes = dst_host ? p->outs.size() * sizeof(void *) : 0;
+  const size_t err_off = (dst_off + dst_bytes + 255) & ~size_t(255);
+  const size_t need = err_off + sizeof(uint32_t);
+  if (need > kStaticScratchBytes)
+    return set_error(ST_E_INVAL,
+                     "the plan needs %zu bytes of static scratch (%zu pieces, %u warps, %u chunks) but the library "
+                     "holds %zu; plan with a larger unit_bytes or fewer workers",
+                     need, p->pieces.size(), p->workers, p->n_chunks, kStaticScratchBytes);
+  void *scratch = nullptr;
+  st_status s = static_scratch(&scratch);
+  if (s != ST_OK) return s;
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(base, p->pieces.data(), pieces_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(base + parts_off, p->parts.data(), parts_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && quant_bytes)
+    e = cudaMemcpyAsync(base + quant_off, p->quant.data(), quant_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && dst_bytes) e = cudaMemcpyAsync(base + dst_off, dst_host, dst_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(base + err_off, 0, sizeof(uint32_t), st);  // left over from the last call
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "filling the static scratch: %s", cuda_msg(e).c_str());
+  for (uint32_t k = 0; k < p->n_chunks; ++k) {
+    const uint32_t *parts = &p->parts[static_cast<size_t>(k) * (p->workers + 1)];
+    if (parts[0] == parts[p->workers]) continue;
+    LaunchArgs a;
+    a.data = static_cast<const uint8_t *>(data_dev);
+    a.data_bytes = p->index->core->data_bytes;
+    a.pieces = reinterpret_cast<const Piece *>(base);
+    a.parts = reinterpret_cast<const uint32_t *>(base + parts_off) + static_cast<size_t>(k) * (p->workers + 1);
+    a.workers = p->workers;
+    a.dst = dst_host ? reinterpret_cast<void *const *>(base + dst_off) : dst_dev;
+    a.scales = scales;
+    a.err = reinterpret_cast<uint32_t *>(base + err_off);
+    a.quant = quant_bytes ? reinterpret_cast<const QuantInfo *>(base + quant_off) : nullptr;
+    s = launch_materialize(a, p->kernel, stream);
+    if (s != ST_OK) return s;
+  }
+  return ST_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -929,47 +994,114 @@ st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *p, void 
   if (!data_dev || !dst_ptrs) return set_error(ST_E_INVAL, "NULL data or destination array");
   st_status s = check_tma_source(p, data_dev);
   if (s != ST_OK) return s;
-  // Layout inside the static array: pieces | warp ranges | block-scale table | error word.
-  const size_t pieces_bytes = p->pieces.size() * sizeof(Piece);
-  const size_t parts_off = (pieces_bytes + 255) & ~size_t(255);
-  const size_t parts_bytes = p->parts.size() * sizeof(uint32_t);
-  const size_t quant_off = (parts_off + parts_bytes + 255) & ~size_t(255);
-  const size_t quant_bytes = p->quant.size() * sizeof(QuantInfo);
-  const size_t err_off = (quant_off + quant_bytes + 255) & ~size_t(255);
-  const size_t need = err_off + sizeof(uint32_t);
-  if (need > kStaticScratchBytes)
-    return set_error(ST_E_INVAL,
-                     "the plan needs %zu bytes of static scratch (%zu pieces, %u warps, %u chunks) but the library "
-                     "holds %zu; plan with a larger unit_bytes or fewer workers",
-                     need, p->pieces.size(), p->workers, p->n_chunks, kStaticScratchBytes);
-  void *scratch = nullptr;
-  s = static_scratch(&scratch);
-  if (s != ST_OK) return s;
-  uint8_t *base = static_cast<uint8_t *>(scratch);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(base, p->pieces.data(), pieces_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(base + parts_off, p->parts.data(), parts_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess && quant_bytes)
-    e = cudaMemcpyAsync(base + quant_off, p->quant.data(), quant_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(base + err_off, 0, sizeof(uint32_t), st);  // left over from the last call
-  if (e != cudaSuccess) return set_error(ST_E_CUDA, "filling the static scratch: %s", cuda_msg(e).c_str());
-  for (uint32_t k = 0; k < p->n_chunks; ++k) {
-    const uint32_t *parts = &p->parts[static_cast<size_t>(k) * (p->workers + 1)];
-    if (parts[0] == parts[p->workers]) continue;
-    LaunchArgs a;
-    a.data = static_cast<const uint8_t *>(data_dev);
-    a.data_bytes = p->index->core->data_bytes;
-    a.pieces = reinterpret_cast<const Piece *>(base);
-    a.parts = reinterpret_cast<const uint32_t *>(base + parts_off) + static_cast<size_t>(k) * (p->workers + 1);
-    a.workers = p->workers;
-    a.dst = dst_ptrs;
-    a.scales = scales;
-    a.err = reinterpret_cast<uint32_t *>(base + err_off);
-    a.quant = quant_bytes ? reinterpret_cast<const QuantInfo *>(base + quant_off) : nullptr;
-    s = launch_materialize(a, p->kernel, stream);
+  return launch_static(p, data_dev, dst_ptrs, nullptr, scales, stream);
+}
+
+st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_cache_t *cache,
+                          const st_selection *sel, st_dtype dst_dtype, void *const *dst_host_ptrs,
+                          void *staging_dev, uint64_t staging_bytes, uint32_t threads, void *stream) {
+  if (!index || !files || !sel || !sel->names) return set_error(ST_E_INVAL, "NULL argument (the selection needs names)");
+  try {
+    const IndexData &ix = *index_data(index);
+    if (files_arena_bytes(files) != ix.core->data_bytes)
+      return set_error(ST_E_INVAL, "the files' arena (%llu bytes) is not the index's data section (%llu bytes)",
+                       (unsigned long long)files_arena_bytes(files), (unsigned long long)ix.core->data_bytes);
+    // The outputs on the real index, and every tensor they read.
+    std::vector<Output> outs;
+    st_status s = select_outputs(ix, sel, dst_dtype, &outs);
     if (s != ST_OK) return s;
+    if (outs.empty()) return ST_OK;
+    if (!dst_host_ptrs) return set_error(ST_E_INVAL, "NULL destinations");
+    std::vector<uint32_t> need;
+    std::vector<char> seen(ix.ent.size(), 0);
+    for (const Output &o : outs)
+      for (uint32_t q : o.reads)
+        if (!seen[q]) {
+          seen[q] = 1;
+          need.push_back(q);
+        }
+    // Those tensors staged back to back (256-byte aligned) under their view
+    // names: a small index whose data section is the staging buffer.
+    auto core = std::make_shared<Core>();
+    uint64_t at = 0;
+    for (uint32_t q : need) {
+      Tensor t = ix.core->tensors[ix.ent[q]];
+      const uint64_t n = t.end - t.begin;
+      t.name = ix.names[q];
+      at = (at + 255) & ~uint64_t(255);
+      t.begin = at;
+      t.end = at + n;
+      at += n;
+      core->tensors.push_back(std::move(t));
+    }
+    core->data_bytes = at;
+    if (at > staging_bytes)
+      return set_error(ST_E_INVAL, "staging needs %llu bytes, %llu given", (unsigned long long)at,
+                       (unsigned long long)staging_bytes);
+    if (!staging_dev) return set_error(ST_E_INVAL, "NULL staging buffer");
+    // Destinations checked on the host: non-NULL and itemsize-aligned.
+    uint64_t traffic = 0;
+    for (size_t i = 0; i < outs.size(); ++i) {
+      const Output &o = outs[i];
+      const uint64_t isz = dtype_size(o.out_dtype);
+      if (o.numel && (!dst_host_ptrs[i] || (reinterpret_cast<uintptr_t>(dst_host_ptrs[i]) & (isz - 1))))
+        return set_error(ST_E_INVAL, "destination of \"%s\" is NULL or not %llu-byte aligned", o.name.c_str(),
+                         (unsigned long long)isz);
+      traffic += o.units * (cls_in_size(o.cls) + cls_out_size(o.cls));
+    }
+    auto mini = make_root(core);
+    s = finish_view(mini.get());
+    if (s != ST_OK) return s;
+    // Units large enough that the tables fit the static array.
+    st_plan_options po{};
+    po.unit_bytes = std::max<uint64_t>(kDefaultUnitBytes, traffic / 32768 + 1);
+    st_plan_s plan;
+    s = plan_host(mini, sel, dst_dtype, &po, &plan);
+    if (s != ST_OK) return s;
+    s = check_tma_source(&plan, staging_dev);
+    if (s != ST_OK) return s;
+    // Host bytes (the RAM tier, or a plain read) -> staging, then launch.
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<const void *> held;
+    std::vector<std::vector<uint8_t>> plain;
+    auto release_all = [&]() {
+      for (const void *h : held) st_cache_release(cache, h);
+      held.clear();
+    };
+    cudaError_t e = cudaSuccess;
+    for (size_t k = 0; k < need.size(); ++k) {
+      const Tensor &src = ix.core->tensors[ix.ent[need[k]]];
+      const uint64_t n = src.end - src.begin;
+      if (!n) continue;
+      const void *host = nullptr;
+      if (cache) {
+        s = st_cache_get(cache, files, src.begin, n, threads, &host);
+        if (s != ST_OK) {
+          release_all();
+          return s;
+        }
+        held.push_back(host);
+      } else {
+        plain.emplace_back(n);
+        s = read_arena(files, src.begin, n, plain.back().data(), threads);
+        if (s != ST_OK) return s;
+        host = plain.back().data();
+      }
+      e = cudaMemcpyAsync(static_cast<uint8_t *>(staging_dev) + core->tensors[k].begin, host, n,
+                          cudaMemcpyHostToDevice, st);
+      if (e != cudaSuccess) break;
+    }
+    cudaEvent_t done = nullptr;
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(done, st);
+    if (e == cudaSuccess) e = cudaEventSynchronize(done);  // the host copies may now be evicted
+    if (done) cudaEventDestroy(done);
+    release_all();
+    if (e != cudaSuccess) return set_error(ST_E_CUDA, "staging the tensors: %s", cuda_msg(e).c_str());
+    return launch_static(&plan, staging_dev, nullptr, dst_host_ptrs, nullptr, stream);
+  } catch (const std::bad_alloc &) {
+    return set_error(ST_E_NOMEM, "out of host memory");
   }
-  return ST_OK;
 }
 
 st_status st_plan_check(const st_plan_t *p, void *stream, uint32_t *flags) {

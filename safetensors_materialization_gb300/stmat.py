@@ -32,7 +32,8 @@ EXPORTS = [
     "st_plan_free", "st_plan_count", "st_plan_output", "st_plan_arena", "st_plan_stats",
     "st_plan_piece", "st_plan_worker", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
     "st_materialize_noalloc", "st_index_open", "st_files_open", "st_files_close", "st_files_read",
-    "st_load_files",
+    "st_load_files", "st_cache_create", "st_cache_free", "st_cache_get", "st_cache_release",
+    "st_cache_stats", "st_cache_clear", "st_load_tensors",
     "st_last_error", "st_status_name", "st_dtype_size", "st_dtype_name", "st_version",
 ]
 
@@ -59,6 +60,11 @@ class OutputInfo(C.Structure):
 
 class Slice(C.Structure):
     _fields_ = [("dim", C.c_int32), ("start", C.c_int64), ("stop", C.c_int64)]
+
+
+class CacheInfo(C.Structure):
+    _fields_ = [("bytes", C.c_uint64), ("max_bytes", C.c_uint64), ("entries", C.c_uint64), ("hits", C.c_uint64),
+                ("misses", C.c_uint64), ("evictions", C.c_uint64)]
 
 
 class FilePart(C.Structure):
@@ -131,12 +137,18 @@ def lib():
             "st_files_open": [C.POINTER(FilePart), S, PP],
             "st_files_read": [P, U64, U64, P, U32],
             "st_load_files": [P, P, P, P, P, P, U64, U32, P, P],
+            "st_cache_create": [U64, C.c_int32, PP],
+            "st_cache_get": [P, P, U64, U64, U32, PP],
+            "st_cache_release": [P, P],
+            "st_cache_stats": [P, C.POINTER(CacheInfo)],
+            "st_cache_clear": [P],
+            "st_load_tensors": [P, P, P, C.POINTER(Selection), I, P, P, U64, U32, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
             f.argtypes = args
             f.restype = I
-        for name in ("st_index_free", "st_plan_free", "st_files_close"):
+        for name in ("st_index_free", "st_plan_free", "st_files_close", "st_cache_free"):
             getattr(L, name).argtypes = [P]
             getattr(L, name).restype = None
         L.st_last_error.restype = C.c_char_p
@@ -187,6 +199,39 @@ def header_size(first8: bytes) -> int:
     n = C.c_uint64()
     _check(lib().st_header_size(first8, len(first8), C.byref(n)))
     return n.value
+
+
+def _selection(names=None, scale_names=None, scale_suffix=None, part=0, n_parts=0, slices=None, quant=None):
+    """An st_selection and the ctypes objects it points into (keep them alive)."""
+    sel = Selection()
+    keep = []
+    if names is not None:
+        arr = _strs(names)
+        keep.append(arr)
+        sel.names, sel.n_names = C.cast(arr, C.POINTER(C.c_char_p)), len(names)
+    if scale_names is not None:
+        arr = _strs(scale_names)
+        keep.append(arr)
+        sel.scale_names = C.cast(arr, C.POINTER(C.c_char_p))
+    if scale_suffix:
+        sel.scale_suffix_from, sel.scale_suffix_to = scale_suffix[0].encode(), scale_suffix[1].encode()
+    sel.part, sel.n_parts = part, n_parts
+    if slices is not None:
+        arr = (Slice * max(1, len(slices)))()
+        for i, x in enumerate(slices):
+            arr[i] = Slice(*(x if x is not None else (-1, 0, 0)))
+        keep.append(arr)
+        sel.slices = C.cast(arr, C.POINTER(Slice))
+    if quant is not None:
+        arr = (BlockQuant * max(1, len(quant)))()
+        for i, q in enumerate(quant):
+            if q:
+                br, bc = q[3] if len(q) > 3 and q[3] else (0, 0)
+                arr[i] = BlockQuant(QUANT_KINDS.get(q[0], 99), q[1].encode() if q[1] else None,
+                                    q[2].encode() if q[2] else None, br, bc)
+        keep.append(arr)
+        sel.quant = C.cast(arr, C.POINTER(BlockQuant))
+    return sel, keep
 
 
 class Index:
@@ -297,40 +342,24 @@ class Index:
         _check(lib().st_index_concat(hs, n, align, bases, C.byref(out)))
         return cls(out.value), [int(b) for b in bases[:n]]
 
+    def load_tensors(self, files, dst_ptrs, staging, names, dst="BF16", cache=None, threads=8, stream=None,
+                     scale_names=None, scale_suffix=None, quant=None):
+        """st_load_tensors: the lazy path for a few named tensors (read through
+        `cache`, staged in `staging`, one launch on `stream`); dst_ptrs: one
+        device address per output, in output order."""
+        sel, keep = _selection(names, scale_names, scale_suffix, 0, 0, None, quant)
+        ptrs = (C.c_void_p * max(1, len(dst_ptrs)))(*dst_ptrs)
+        nbytes = staging.numel() if hasattr(staging, "numel") else len(staging)
+        _check(lib().st_load_tensors(self._h, files.handle, cache.handle if cache else None, C.byref(sel),
+                                     DTYPES.index(dst), ptrs, _addr(staging), nbytes, threads, _stream(stream)))
+
     def plan(self, dst="BF16", names=None, scale_names=None, scale_suffix=None, part=0, n_parts=0,
              workers=0, chunk_bytes=0, host_only=False, blocks_per_sm=0, unit_bytes=0, kernel=0, order=0,
              slices=None, quant=None):
         """st_plan: outputs and device work for a selection.  quant: per name
         None or (kind, block-scales name, global-scale name or None,
         (block rows, block cols) or None), kind "block_fp8" or "nvfp4"."""
-        sel = Selection()
-        keep = []
-        if names is not None:
-            arr = _strs(names)
-            keep.append(arr)
-            sel.names, sel.n_names = C.cast(arr, C.POINTER(C.c_char_p)), len(names)
-        if scale_names is not None:
-            arr = _strs(scale_names)
-            keep.append(arr)
-            sel.scale_names = C.cast(arr, C.POINTER(C.c_char_p))
-        if scale_suffix:
-            sel.scale_suffix_from, sel.scale_suffix_to = scale_suffix[0].encode(), scale_suffix[1].encode()
-        sel.part, sel.n_parts = part, n_parts
-        if slices is not None:
-            arr = (Slice * max(1, len(slices)))()
-            for i, x in enumerate(slices):
-                arr[i] = Slice(*(x if x is not None else (-1, 0, 0)))
-            keep.append(arr)
-            sel.slices = C.cast(arr, C.POINTER(Slice))
-        if quant is not None:
-            arr = (BlockQuant * max(1, len(quant)))()
-            for i, q in enumerate(quant):
-                if q:
-                    br, bc = q[3] if len(q) > 3 and q[3] else (0, 0)
-                    arr[i] = BlockQuant(QUANT_KINDS.get(q[0], 99), q[1].encode() if q[1] else None,
-                                        q[2].encode() if q[2] else None, br, bc)
-            keep.append(arr)
-            sel.quant = C.cast(arr, C.POINTER(BlockQuant))
+        sel, keep = _selection(names, scale_names, scale_suffix, part, n_parts, slices, quant)
         opts = PlanOptions(workers, chunk_bytes, 1 if host_only else 0, blocks_per_sm, unit_bytes, kernel, order)
         out = C.c_void_p()
         _check(lib().st_plan(self._h, C.byref(sel), DTYPES.index(dst), C.byref(opts), C.byref(out)))
@@ -371,6 +400,123 @@ class Files:
     def read(self, begin, nbytes, host, threads=4):
         """st_files_read into `host` (a numpy uint8 array or torch tensor)."""
         _check(lib().st_files_read(self._h, begin, nbytes, _addr(host), threads))
+
+
+class Cache:
+    """st_cache_t: the LRU RAM tier (host copies of file ranges, at most
+    `max_bytes`; pinned memory unless pinned=False)."""
+
+    def __init__(self, max_bytes, pinned=True):
+        out = C.c_void_p()
+        _check(lib().st_cache_create(max_bytes, 1 if pinned else 0, C.byref(out)))
+        self._h = C.c_void_p(out.value)
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value and _lib is not None:
+            _lib.st_cache_free(self._h)
+            self._h = C.c_void_p(None)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def get(self, files, begin, nbytes, threads=4):
+        """Holds the host copy of arena bytes [begin, begin + nbytes); returns
+        its address (release it with release())."""
+        out = C.c_void_p()
+        _check(lib().st_cache_get(self._h, files.handle, begin, nbytes, threads, C.byref(out)))
+        return out.value
+
+    def release(self, addr):
+        _check(lib().st_cache_release(self._h, addr))
+
+    def stats(self):
+        info = CacheInfo()
+        _check(lib().st_cache_stats(self._h, C.byref(info)))
+        return {k: getattr(info, k) for k, _ in CacheInfo._fields_}
+
+    def clear(self):
+        _check(lib().st_cache_clear(self._h))
+
+
+class StreamStateDict:
+    """A read-only mapping name -> tensor over a checkpoint's shard files, in
+    the manner of the streaming mapping of "Disk tier safetensors streaming
+    design audit (ComfyUI)": keys, shapes, dtypes and metadata come from the
+    headers alone; sd[name] reads that tensor (and its scales) through the
+    RAM tier and materializes it on the GPU with st_load_tensors; meta(name)
+    is a device='meta' stand-in (the disk reference stays in the index).
+
+    paths: shard files; dst: output float dtype; rename/prefix: views;
+    scale_suffix / quant: as for Index.plan (quant: name -> (kind, scales,
+    global scale, block))."""
+
+    def __init__(self, paths, dst="BF16", device="cuda", ram_cache_bytes=1 << 30, pinned=True, threads=8,
+                 rename=None, prefix=None, scale_suffix=None, quant=None, align=256):
+        self.files, root = Files.of_checkpoint(list(paths), align)
+        view = root
+        if rename:
+            view = view.view_rename(rename)
+        if prefix:
+            view = view.view_prefix(prefix)
+        self.index, self._root = view, root
+        self.dst, self.device, self.threads = dst, device, threads
+        self.scale_suffix, self.quant = scale_suffix, dict(quant or {})
+        self.cache = Cache(ram_cache_bytes, pinned) if ram_cache_bytes else None
+        self._staging = None
+        self._names = [e["name"] for e in view.entries()]
+        self._pos = {n: i for i, n in enumerate(self._names)}
+
+    def keys(self):
+        return list(self._names)
+
+    def __iter__(self):
+        return iter(self._names)
+
+    def __len__(self):
+        return len(self._names)
+
+    def __contains__(self, name):
+        return name in self._pos
+
+    def metadata(self):
+        return self.index.metadata()
+
+    def info(self, name):
+        """Shape and dtype of sd[name] (header only)."""
+        plan = self._plan(name, host_only=True)
+        o = plan.outputs()[0]
+        return o["shape"], o["dtype"]
+
+    def meta(self, name):
+        import torch
+        shape, dt = self.info(name)
+        return torch.empty(shape, dtype=torch_dtype(dt), device="meta")
+
+    def _sel(self, name):
+        q = self.quant.get(name)
+        return dict(names=[name], scale_suffix=self.scale_suffix, quant=[q] if q else None)
+
+    def _plan(self, name, host_only):
+        return self.index.plan(dst=self.dst, workers=1, host_only=host_only, **self._sel(name))
+
+    def __getitem__(self, name):
+        import torch
+        if name not in self._pos:
+            raise KeyError(name)
+        shape, dt = self.info(name)
+        out = torch.empty(shape, dtype=torch_dtype(dt), device=self.device)
+        e = self.index.entry(self._pos[name])
+        need = int((e["end"] - e["begin"]) * 1.25) + (1 << 16)
+        if self._staging is None or self._staging.numel() < need:
+            self._staging = torch.empty(need, dtype=torch.uint8, device=self.device)
+        self.index.load_tensors(self.files, [out.data_ptr()], self._staging, dst=self.dst, cache=self.cache,
+                                threads=self.threads, stream=torch.cuda.current_stream(), **self._sel(name))
+        return out
+
+    def items(self):
+        for n in self._names:
+            yield n, self[n]
 
 
 class Plan:

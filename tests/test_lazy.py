@@ -1,0 +1,199 @@
+"""The lazy single-tensor path and its RAM tier ("Disk tier safetensors
+streaming design audit (ComfyUI)": a streaming mapping that loads a tensor
+when it is accessed; an LRU cache of RAM-resident weights with a maximum
+number of bytes, whose eviction keeps only the disk reference).
+
+CPU: the cache's LRU rules (hits, misses, eviction order, the bound, held
+entries, entries above the bound), its bytes against the file, and the
+mapping's metadata-only side.  GPU: every tensor of a sharded checkpoint
+through StreamStateDict (st_load_tensors) against the oracle, with and
+without the cache, per-tensor scaled FP8 and block-scaled weights."""
+import os
+
+import numpy as np
+import pytest
+
+from safetensors_materialization_gb300 import synth
+
+
+def blob_file(tmp_path, n=1 << 20, seed=0):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    data = rng.integers(0, 256, size=n, dtype=np.uint8)
+    path = os.path.join(str(tmp_path), "blob.bin")
+    data.tofile(path)
+    return path, data
+
+
+def test_cache_lru_rules(stmat, tmp_path):
+    import ctypes
+    path, data = blob_file(tmp_path)
+    files = stmat.Files([(path, 0, data.size, 0)])
+    c = stmat.Cache(10_000, pinned=False)
+
+    def read(addr, n):
+        return np.ctypeslib.as_array((ctypes.c_uint8 * n).from_address(addr))
+
+    a = c.get(files, 0, 4000)
+    assert np.array_equal(read(a, 4000), data[:4000])
+    c.release(a)
+    b = c.get(files, 5000, 4000)
+    c.release(b)
+    assert c.stats() == {"bytes": 8000, "max_bytes": 10_000, "entries": 2, "hits": 0, "misses": 2, "evictions": 0}
+    a2 = c.get(files, 0, 4000)                 # a hit: the same copy, now the most recent
+    assert a2 == a and c.stats()["hits"] == 1
+    c.release(a2)
+    d = c.get(files, 20_000, 3000)             # needs room: evicts b, the least recently used
+    st = c.stats()
+    assert st["evictions"] == 1 and st["entries"] == 2 and st["bytes"] == 7000
+    assert np.array_equal(read(d, 3000), data[20_000:23_000])
+    c.release(d)
+    b2 = c.get(files, 5000, 4000)              # b was evicted: a miss, read again
+    assert c.stats()["misses"] == 4
+    assert np.array_equal(read(b2, 4000), data[5000:9000])
+    # eviction skips held entries: b2 is held, so d (the older unheld one) goes
+    e = c.get(files, 100_000, 6000)
+    st = c.stats()
+    assert st["bytes"] == 10_000 and st["entries"] == 2
+    c.release(b2)
+    c.release(e)
+    big = c.get(files, 0, 50_000)              # above the bound: read, not kept
+    assert np.array_equal(read(big, 50_000), data[:50_000])
+    assert c.stats()["entries"] == 2
+    c.release(big)
+    with pytest.raises(stmat.StmatError):
+        c.release(big)                         # freed on release
+    c.clear()
+    assert c.stats()["entries"] == 0 and c.stats()["bytes"] == 0
+    with pytest.raises(stmat.StmatError) as err:
+        c.get(files, data.size - 10, 11)
+    assert err.value.status == "ST_E_INVAL"
+
+
+def test_cache_under_held_pressure(stmat, tmp_path):
+    """When everything kept is held, a new entry is still read and kept; the
+    bound is restored as holds are released and entries age out."""
+    path, data = blob_file(tmp_path, seed=1)
+    files = stmat.Files([(path, 0, data.size, 0)])
+    c = stmat.Cache(8192, pinned=False)
+    held = [c.get(files, k * 4096, 4096) for k in range(3)]
+    assert c.stats()["bytes"] == 3 * 4096    # over the bound while held
+    for h in held:
+        c.release(h)
+    x = c.get(files, 600_000, 4096)
+    c.release(x)
+    assert c.stats()["bytes"] <= 8192
+
+
+def write_shards(tmp_path, w):
+    paths = []
+    for k, lay in enumerate(w.files):
+        path = os.path.join(str(tmp_path), f"m{k}.safetensors")
+        synth.build_workload_file(w, k).tofile(path)
+        paths.append(path)
+    return paths
+
+
+def small_llm():
+    return synth.llm8b(seed=9, layers=3, hidden=128, inter=352, vocab=400, kv=32, shards=3)
+
+
+def test_stream_state_dict_metadata_only(stmat, tmp_path):
+    torch = pytest.importorskip("torch")
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    sd = stmat.StreamStateDict(paths, dst="F16", pinned=False, ram_cache_bytes=1 << 20,
+                               rename=[("model.", "")])
+    names = [e.name.replace("model.", "", 1) if e.name.startswith("model.") else e.name
+             for lay in w.files for e in lay.entries]
+    assert sd.keys() == names and len(sd) == len(names)
+    assert "layers.0.mlp.up_proj.weight" in sd and "model.norm.weight" not in sd
+    m = sd.meta("layers.1.self_attn.q_proj.weight")
+    assert m.device.type == "meta" and tuple(m.shape) == (128, 128) and m.dtype == torch.float16
+    assert sd.metadata() == {"format": "pt"}
+    assert sd.cache.stats()["misses"] == 0     # nothing read so far
+
+
+def gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return torch
+
+
+def oracle_joined(oracle, w, paths):
+    oix, bases = oracle.concat([oracle.parse_header(l.header, l.data_bytes) for l in w.files])
+    arena = np.zeros(oix.data_bytes, np.uint8)
+    for k, (b, lay) in enumerate(zip(bases, w.files)):
+        img = synth.build_workload_file(w, k)
+        arena[b:b + lay.data_bytes] = img[lay.data_start:]
+    return oix, arena
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cache_bytes", [0, 1 << 14, 1 << 30])
+def test_stream_state_dict_loads_every_tensor(stmat, oracle, tmp_path, cache_bytes):
+    torch = gpu()
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    sd = stmat.StreamStateDict(paths, dst="BF16", ram_cache_bytes=cache_bytes)
+    oix, arena = oracle_joined(oracle, w, paths)
+    for rounds in range(2):
+        for name in sd.keys():
+            t = sd[name]
+            torch.cuda.synchronize()
+            sel = oix.select(names=[name], dst="BF16")
+            assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), name
+    if cache_bytes:
+        st = sd.cache.stats()
+        assert st["bytes"] <= cache_bytes
+        if cache_bytes == 1 << 30:
+            assert st["hits"] == len(sd) and st["misses"] == len(sd)   # the second round hit every tensor
+
+
+@pytest.mark.gpu
+def test_lazy_scaled_and_block_scaled(stmat, oracle, tmp_path):
+    torch = gpu()
+    import test_blockscale as TB
+    img, quant = TB.quant_file(50, lead=5)
+    path = os.path.join(str(tmp_path), "q.safetensors")
+    img.tofile(path)
+    oix = oracle.parse(img)
+    data = img[8 + oix.header_len:]
+    for dst in ("BF16", "F32"):
+        sd = stmat.StreamStateDict([path], dst=dst, quant=quant, ram_cache_bytes=1 << 22)
+        for name in ("a.weight", "b.weight", "mid"):
+            t = sd[name]
+            torch.cuda.synchronize()
+            sel = oix.select(names=[name], dst=dst, quant=[quant.get(name)])
+            assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, data)), name
+    # per-tensor scaled FP8 through the suffix pairing
+    w = synth.scaled_fp8(blocks=1)
+    lay = w.files[0]
+    spath = os.path.join(str(tmp_path), "s.safetensors")
+    simg = synth.build_workload_file(w, 0)
+    simg.tofile(spath)
+    sd = stmat.StreamStateDict([spath], dst="BF16", scale_suffix=w.scale_suffix)
+    soix = oracle.parse(simg)
+    name = [e.name for e in lay.entries if e.name.endswith(".weight")][3]
+    t = sd[name]
+    torch.cuda.synchronize()
+    sel = soix.select(names=[name], dst="BF16", scale_suffix=w.scale_suffix)
+    assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, simg[lay.data_start:]))
+
+
+@pytest.mark.gpu
+def test_lazy_rejects_bad_destinations(stmat, tmp_path):
+    torch = gpu()
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    files, ix = stmat.Files.of_checkpoint(paths)
+    staging = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
+    out = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    name = "model.norm.weight"
+    for bad in (0, out.data_ptr() + 1):
+        with pytest.raises(stmat.StmatError) as e:
+            ix.load_tensors(files, [bad], staging, names=[name], dst="F32")
+        assert e.value.status == "ST_E_INVAL"
+    with pytest.raises(stmat.StmatError) as e:       # staging too small
+        ix.load_tensors(files, [out.data_ptr()], staging[:16], names=[name], dst="BF16")
+    assert e.value.status == "ST_E_INVAL" and "staging needs" in str(e.value)
