@@ -199,7 +199,7 @@ typedef struct st_slice {
  *     output has shape [M, 2K].  block_rows/block_cols must be 0 (or 1/16).
  * The output dtype must be BF16, F16 or F32; a block-scaled output takes no
  * slice and no per-tensor scale; its scale tensors are consumed.  Plans with
- * block-scaled outputs run the TMA kernel build. */
+ * block-scaled outputs run a TMA kernel build (4 unless 3 is asked for). */
 typedef enum st_quant_kind { ST_QUANT_NONE = 0, ST_QUANT_BLOCK_FP8 = 2, ST_QUANT_NVFP4 = 3 } st_quant_kind;
 
 typedef struct st_block_quant {
@@ -252,7 +252,9 @@ typedef struct st_plan_options {
                              build (deep unroll); 2 = latency build (high occupancy); 3 = TMA
                              build (source bytes staged in shared memory by bulk copies; the
                              data section must then be device or managed memory, else
-                             st_materialize returns ST_E_INVAL) */
+                             st_materialize returns ST_E_INVAL); 4 = the TMA build with fewer
+                             copies in flight per warp and more warps per SM, the default for
+                             plans with block-scaled outputs */
   uint32_t order;         /* unit order within a chunk: 0 = the build's default (2 for builds 1
                              and 2, 1 for the TMA build); 1 = source order (the TMA build then
                              fetches adjacent small tensors with one bulk copy); 2 = grouped by
@@ -290,7 +292,7 @@ st_status st_plan_output(const st_plan_t *plan, size_t i, st_output_info *info);
 /* Offsets of every output in one buffer, each aligned to `align` (a power of
  * two >= 16); offsets has st_plan_count entries.  `total` is the size. */
 st_status st_plan_arena(const st_plan_t *plan, uint64_t align, uint64_t *offsets, uint64_t *total);
-/* Piece/worker layout and kernel build (1 streaming, 2 latency, 3 TMA), for tests and
+/* Piece/worker layout and kernel build (1 streaming, 2 latency, 3 TMA, 4 wide TMA), for tests and
  * tuning; any pointer may be NULL. */
 st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chunks, uint64_t *pieces,
                         uint32_t *kernel);

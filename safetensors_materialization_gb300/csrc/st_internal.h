@@ -142,6 +142,7 @@ ST_HD constexpr uint32_t cls_out_shift(uint32_t c) { return static_cast<uint32_t
 constexpr uint32_t kKernelStream = 1;
 constexpr uint32_t kKernelLatency = 2;
 constexpr uint32_t kKernelTma = 3;
+constexpr uint32_t kKernelTmaWide = 4;  // the TMA build with fewer slots per warp and more warps per SM
 
 // Resident 256-thread blocks per SM for a kernel build, and the SM count of
 // the current device.

@@ -538,12 +538,23 @@ __global__ void __launch_bounds__(kThreads, ST_LAT_MIN_BLOCKS) materialize_laten
 #ifndef ST_TMA_SEG
 #define ST_TMA_SEG 2048
 #endif
+// Two shapes of the build: many small tensors run best with 4 slots per warp
+// at 2 blocks per SM (deep per-warp queues); block-scaled weights, whose
+// consumer is busier, with 2 slots at 3 blocks per SM (more warps to issue).
 #ifndef ST_TMA_SLOTS
 #define ST_TMA_SLOTS 4
 #endif
-
+#ifndef ST_TMA_MIN_BLOCKS
+#define ST_TMA_MIN_BLOCKS 2
+#endif
+#ifndef ST_TMA_WIDE_SLOTS
+#define ST_TMA_WIDE_SLOTS 2
+#endif
+#ifndef ST_TMA_WIDE_MIN_BLOCKS
+#define ST_TMA_WIDE_MIN_BLOCKS 3
+#endif
 constexpr uint32_t kSeg = ST_TMA_SEG;
-constexpr int kSlots = ST_TMA_SLOTS;
+constexpr uint32_t kBatch = 32;  // piece descriptors fetched per bulk copy (one per lane)
 constexpr uint32_t kSlotBytes = kSeg + 32;  // a clipped window is at most kSeg + 16 bytes
 constexpr uint32_t kSpinLimit = 1u << 22;
 static_assert(kSeg % 16 == 0 && kSeg >= 64, "segment size");
@@ -574,20 +585,25 @@ constexpr uint32_t kScalePayload = 256;
 constexpr uint32_t kScaleBytes = kScalePayload + 32;
 constexpr uint32_t kQscMax = 32;
 
+template <int kSlots>
 struct alignas(128) WarpSmem {
   uint8_t buf[kSlots][kSlotBytes];
   uint8_t sbuf[kSlots][kScaleBytes];
-  Piece desc[2][32];
-  uint8_t *dstp[2][32];
-  float scl[2][32];
+  Piece desc[2][kBatch];
+  uint8_t *dstp[2][kBatch];
+  float scl[2][kBatch];
   SegMeta meta[kSlots];
   uint64_t bar[kSlots];
   uint64_t dbar[2];
   float qsc[kQscMax];  // the consumed block-FP8 segment's scales as binary32 (any alignment in the slot)
 };
-static_assert(sizeof(WarpSmem) * kWarpsPerBlock <= 113 * 1024, "two 8-warp blocks per SM");
-static_assert(offsetof(WarpSmem, sbuf) % 16 == 0 && kScaleBytes % 16 == 0, "scale bulk-copy destinations");
-static_assert(offsetof(WarpSmem, desc) % 16 == 0 && kSlotBytes % 16 == 0, "bulk-copy destinations");
+static_assert(sizeof(WarpSmem<ST_TMA_SLOTS>) * kWarpsPerBlock * ST_TMA_MIN_BLOCKS <= 226 * 1024, "blocks per SM fit");
+static_assert(sizeof(WarpSmem<ST_TMA_WIDE_SLOTS>) * kWarpsPerBlock * ST_TMA_WIDE_MIN_BLOCKS <= 226 * 1024,
+              "blocks per SM fit");
+static_assert(offsetof(WarpSmem<ST_TMA_SLOTS>, sbuf) % 16 == 0 && offsetof(WarpSmem<ST_TMA_WIDE_SLOTS>, sbuf) % 16 == 0 &&
+                  kScaleBytes % 16 == 0, "scale bulk-copy destinations");
+static_assert(offsetof(WarpSmem<ST_TMA_SLOTS>, desc) % 16 == 0 && offsetof(WarpSmem<ST_TMA_WIDE_SLOTS>, desc) % 16 == 0 &&
+                  kSlotBytes % 16 == 0, "bulk-copy destinations");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -926,21 +942,22 @@ struct Cursor {
   uint32_t e;
 };
 
-__global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs a) {
-  extern __shared__ __align__(128) uint8_t tma_smem[];
+template <int kSlots>
+__device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   const uint32_t lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const uint32_t w = blockIdx.x * kWarpsPerBlock + wib;
   if (w >= a.workers) return;
   const uint32_t p0 = a.parts[w], p1 = a.parts[w + 1];
   if (p0 >= p1) return;
-  WarpSmem &ws = reinterpret_cast<WarpSmem *>(tma_smem)[wib];
-  const uint32_t nbatch = (p1 - p0 + 31) / 32;
+  WarpSmem<kSlots> &ws = reinterpret_cast<WarpSmem<kSlots> *>(smem)[wib];
+  const uint32_t nbatch = (p1 - p0 + kBatch - 1) / kBatch;
   const uintptr_t lo16 = (reinterpret_cast<uintptr_t>(a.data) + 15) & ~uintptr_t(15);
   const uintptr_t hi16 = (reinterpret_cast<uintptr_t>(a.data) + a.data_bytes) & ~uintptr_t(15);
 
   auto issue_desc = [&](uint32_t bb) {  // lane 0
-    const uint32_t cnt = min(32u, p1 - p0 - 32 * bb);
-    bulk_load(ws.desc[bb & 1], a.pieces + p0 + 32 * bb, cnt * static_cast<uint32_t>(sizeof(Piece)), &ws.dbar[bb & 1]);
+    const uint32_t cnt = min(kBatch, p1 - p0 - kBatch * bb);
+    bulk_load(ws.desc[bb & 1], a.pieces + p0 + kBatch * bb, cnt * static_cast<uint32_t>(sizeof(Piece)),
+              &ws.dbar[bb & 1]);
   };
   if (lane == 0) {
     for (int k = 0; k < kSlots; ++k) mbar_init(&ws.bar[k]);
@@ -957,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
   auto enter_batch = [&](uint32_t b) -> bool {
     if (!mbar_wait(&ws.dbar[b & 1], (b >> 1) & 1)) return false;
     dseen = b + 1;
-    const uint32_t cnt = min(32u, p1 - p0 - 32 * b);
+    const uint32_t cnt = min(kBatch, p1 - p0 - kBatch * b);
     if (lane < cnt) {
       const Piece &pc = ws.desc[b & 1][lane];
       const uint32_t out = pc.out_cls >> kClsBits, cls = pc.out_cls & ((1u << kClsBits) - 1);
@@ -991,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
   // The piece being cut into segments: its fields are loaded once, when the
   // cursor reaches it, and the run's source/output addresses advance by the
   // pitch / run size, so a segment costs no divisions or multiplications.
-  Cursor cur{0, 0, 0, min(32u, p1 - p0), 0};
+  Cursor cur{0, 0, 0, min(kBatch, p1 - p0), 0};
   const uint8_t *run_src = nullptr;  // source of the current run's element 0
   uint8_t *run_dst = nullptr;        // output address of the current run's element 0
   uint64_t pitch = 0;
@@ -1030,7 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
         cur.i = 0;
         cur.r = 0;
         cur.e = 0;
-        cur.n = min(32u, p1 - p0 - 32 * cur.b);
+        cur.n = min(kBatch, p1 - p0 - kBatch * cur.b);
         if (!enter_batch(cur.b)) return -1;
         continue;
       }
@@ -1100,9 +1117,11 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
         m.off = off;
         m.scale = scale;
         m.cls = cls;
-        m.sptr = sptr;
-        m.col0 = col0;
-        m.bcs = qi.bc_shift;
+        if (cls_quant(cls)) {
+          m.sptr = sptr;
+          m.col0 = col0;
+          m.bcs = qi.bc_shift;
+        }
         proxy_fence();
         mbar_expect(&ws.bar[slot], bytes + sbytes);
         if (bytes) bulk_copy(ws.buf[slot], reinterpret_cast<const void *>(w0), bytes, &ws.bar[slot]);
@@ -1155,25 +1174,38 @@ __global__ void __launch_bounds__(kThreads, 2) materialize_tma(const LaunchArgs 
   }
 }
 
+__global__ void __launch_bounds__(kThreads, ST_TMA_MIN_BLOCKS) materialize_tma(const LaunchArgs a) {
+  extern __shared__ __align__(128) uint8_t tma_smem[];
+  tma_body<ST_TMA_SLOTS>(a, tma_smem);
+}
+
+__global__ void __launch_bounds__(kThreads, ST_TMA_WIDE_MIN_BLOCKS) materialize_tma_wide(const LaunchArgs a) {
+  extern __shared__ __align__(128) uint8_t tma_smem[];
+  tma_body<ST_TMA_WIDE_SLOTS>(a, tma_smem);
+}
+
 std::string cuda_msg(cudaError_t e) { return std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e); }
 
 }  // namespace
 
 namespace {
-constexpr size_t kTmaSmem = sizeof(WarpSmem) * kWarpsPerBlock;
+constexpr size_t kTmaSmem = sizeof(WarpSmem<ST_TMA_SLOTS>) * kWarpsPerBlock;
+constexpr size_t kTmaWideSmem = sizeof(WarpSmem<ST_TMA_WIDE_SLOTS>) * kWarpsPerBlock;
 constexpr int kMaxDevices = 256;
 std::mutex g_attr_mu;
-bool g_tma_attr[kMaxDevices] = {};
+bool g_tma_attr[2][kMaxDevices] = {};
 
-// The TMA build's dynamic shared memory exceeds the default 48 KiB: raise
-// the kernel's limit once per device.
-cudaError_t tma_attr(int dev) {
+// The TMA builds' dynamic shared memory exceeds the default 48 KiB: raise
+// each kernel's limit once per device.
+cudaError_t tma_attr(int dev, bool wide) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_attr_mu);
-  if (g_tma_attr[dev]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(materialize_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kTmaSmem));
-  if (e == cudaSuccess) g_tma_attr[dev] = true;
+  if (g_tma_attr[wide][dev]) return cudaSuccess;
+  cudaError_t e = wide ? cudaFuncSetAttribute(materialize_tma_wide, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(kTmaWideSmem))
+                       : cudaFuncSetAttribute(materialize_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(kTmaSmem));
+  if (e == cudaSuccess) g_tma_attr[wide][dev] = true;
   return e;
 }
 }  // namespace
@@ -1182,13 +1214,22 @@ st_status kernel_occupancy(uint32_t variant, int *sms, int *blocks_per_sm) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess && variant == kKernelTma) e = tma_attr(dev);
-  if (e == cudaSuccess)
-    e = variant == kKernelLatency
-            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_latency, kThreads, 0)
-        : variant == kKernelTma
-            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_tma, kThreads, kTmaSmem)
-            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_stream, kThreads, 0);
+  if (e == cudaSuccess && (variant == kKernelTma || variant == kKernelTmaWide)) e = tma_attr(dev, variant == kKernelTmaWide);
+  if (e == cudaSuccess) {
+    switch (variant) {
+      case kKernelLatency:
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_latency, kThreads, 0);
+        break;
+      case kKernelTma:
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_tma, kThreads, kTmaSmem);
+        break;
+      case kKernelTmaWide:
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_tma_wide, kThreads, kTmaWideSmem);
+        break;
+      default:
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, materialize_stream, kThreads, 0);
+    }
+  }
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "querying the device: %s", cuda_msg(e).c_str());
   if (*blocks_per_sm < 1) *blocks_per_sm = 1;
   return ST_OK;
@@ -1197,12 +1238,16 @@ st_status kernel_occupancy(uint32_t variant, int *sms, int *blocks_per_sm) {
 st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream) {
   const uint32_t blocks = (a.workers + kWarpsPerBlock - 1) / kWarpsPerBlock;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (variant == kKernelTma) {
+  if (variant == kKernelTma || variant == kKernelTmaWide) {
+    const bool wide = variant == kKernelTmaWide;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = tma_attr(dev);
-    if (e != cudaSuccess) return set_error(ST_E_CUDA, "enabling %zu bytes of shared memory: %s", kTmaSmem, cuda_msg(e).c_str());
-    materialize_tma<<<blocks, kThreads, kTmaSmem, st>>>(a);
+    if (e == cudaSuccess) e = tma_attr(dev, wide);
+    if (e != cudaSuccess)
+      return set_error(ST_E_CUDA, "enabling %zu bytes of shared memory: %s", wide ? kTmaWideSmem : kTmaSmem,
+                       cuda_msg(e).c_str());
+    if (wide) materialize_tma_wide<<<blocks, kThreads, kTmaWideSmem, st>>>(a);
+    else materialize_tma<<<blocks, kThreads, kTmaSmem, st>>>(a);
   } else if (variant == kKernelLatency) {
     materialize_latency<<<blocks, kThreads, 0, st>>>(a);
   } else {

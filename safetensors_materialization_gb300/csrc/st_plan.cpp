@@ -599,25 +599,25 @@ st_status plan_host(std::shared_ptr<const IndexData> index, const st_selection *
   // warp keeps kilobytes in flight whatever the tensor size); else the
   // streaming build.
   if (opts && opts->kernel) {
-    if (opts->kernel != kKernelStream && opts->kernel != kKernelLatency && opts->kernel != kKernelTma)
-      return set_error(ST_E_INVAL, "options.kernel must be 0, 1, 2 or 3");
+    if (opts->kernel < kKernelStream || opts->kernel > kKernelTmaWide)
+      return set_error(ST_E_INVAL, "options.kernel must be 0 .. 4");
     p->kernel = opts->kernel;
   } else {
     p->kernel = nonempty && traffic / nonempty < kSmallOutputBytes ? kKernelTma : kKernelStream;
   }
-  // Block-scaled outputs are only in the TMA build.
+  // Block-scaled outputs are only in the TMA builds (the wide one by default).
   bool has_quant = false;
   for (const Output &o : p->outs) has_quant = has_quant || o.qkind != ST_QUANT_NONE;
   if (has_quant) {
-    if (opts && opts->kernel && opts->kernel != kKernelTma)
-      return set_error(ST_E_INVAL, "block-scaled outputs need the TMA build (options.kernel 0 or 3)");
-    p->kernel = kKernelTma;
+    if (opts && opts->kernel && opts->kernel != kKernelTma && opts->kernel != kKernelTmaWide)
+      return set_error(ST_E_INVAL, "block-scaled outputs need a TMA build (options.kernel 0, 3 or 4)");
+    if (!(opts && opts->kernel)) p->kernel = kKernelTmaWide;
   }
   // Unit order: the register builds run one class at a time (their
   // per-class code is large, and mixing classes stalls on instruction
   // fetch); the TMA build's code is small, and source order keeps DRAM
   // rows local.
-  p->class_major = order == 2 || (order == 0 && p->kernel != kKernelTma);
+  p->class_major = order == 2 || (order == 0 && p->kernel != kKernelTma && p->kernel != kKernelTmaWide);
   int sms = 0, blocks = 0;
   if (!host_only || workers == 0) {
     if (host_only) return set_error(ST_E_INVAL, "a host-only plan needs options.workers");
@@ -778,7 +778,7 @@ st_status check_device_plan(const st_plan_t *p) {
 // The TMA build's bulk copies read the data section: it must be device (or
 // managed) memory.
 st_status check_tma_source(const st_plan_t *p, const void *data_dev) {
-  if (p->kernel != kKernelTma || !data_dev) return ST_OK;
+  if ((p->kernel != kKernelTma && p->kernel != kKernelTmaWide) || !data_dev) return ST_OK;
   cudaPointerAttributes at;
   cudaError_t e = cudaPointerGetAttributes(&at, data_dev);
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "cudaPointerGetAttributes: %s", cuda_msg(e).c_str());

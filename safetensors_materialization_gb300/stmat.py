@@ -563,7 +563,7 @@ class Plan:
         w, c, p, k = C.c_uint32(), C.c_uint32(), C.c_uint64(), C.c_uint32()
         _check(lib().st_plan_stats(self._h, C.byref(w), C.byref(c), C.byref(p), C.byref(k)))
         return {"workers": w.value, "chunks": c.value, "pieces": p.value,
-                "kernel": {1: "stream", 2: "latency", 3: "tma"}.get(k.value, str(k.value))}
+                "kernel": {1: "stream", 2: "latency", 3: "tma", 4: "tma_wide"}.get(k.value, str(k.value))}
 
     def piece(self, k):
         v = [C.c_uint64(), C.c_uint64(), C.c_uint64(), C.c_uint32(), C.c_uint32(), C.c_uint32(), C.c_uint32(),

@@ -68,7 +68,7 @@ def test_library_selection_matches_oracle(stmat, oracle, dst):
     plan = ix.plan(dst=dst, names=names, quant=q, workers=64, host_only=True)
     sel = oix.select(dst=dst, names=names, quant=q)
     assert outputs_key(plan.outputs()) == outputs_key(sel.outputs())
-    assert plan.stats()["kernel"] == "tma"
+    assert plan.stats()["kernel"] == "tma_wide"
     assert [o["name"] for o in plan.outputs()] == ["_lead", "a.weight", "mid", "b.weight"]
 
 
@@ -167,12 +167,13 @@ def assert_outputs(plan, outs, want):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("dst", ["BF16", "F16", "F32"])
-@pytest.mark.parametrize("lead,shift", [(0, 0), (3, 0), (1, 7), (13, 9)])
-def test_gpu_blockscaled_matches_oracle(stmat, oracle, dst, lead, shift):
+@pytest.mark.parametrize("lead,shift,kernel", [(0, 0, 0), (3, 0, 3), (1, 7, 0), (13, 9, 3)])
+def test_gpu_blockscaled_matches_oracle(stmat, oracle, dst, lead, shift, kernel):
     """Both formats, unaligned weight and scale offsets, the data section at
-    several device misalignments, ragged rows and blocks."""
+    several device misalignments, ragged rows and blocks, on both TMA builds."""
     img, quant = quant_file(10 + lead, lead=lead)
-    plan, outs, names, q = run_gpu(stmat, img, quant, dst, shift=shift)
+    plan, outs, names, q = run_gpu(stmat, img, quant, dst, shift=shift, kernel=kernel)
+    assert plan.stats()["kernel"] == {0: "tma_wide", 3: "tma"}[kernel]
     oix = oracle.parse(img)
     sel = oix.select(dst=dst, names=names, quant=q)
     data = img[8 + oix.header_len:]

@@ -151,12 +151,12 @@ def special_image(seed=0):
 
 @pytest.mark.parametrize("dst", ["BF16", "F16", "F32"])
 @pytest.mark.parametrize("packed", [False, True])
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 def test_every_bit_pattern(stmat, oracle, dst, packed, kernel):
     img = special_image()
     sfx = (".weight", ".scale_weight")
     plan, outs, _ = run(stmat, img, dst=dst, scale_suffix=sfx, packed=packed, kernel=kernel)
-    assert plan.stats()["kernel"] == {1: "stream", 2: "latency", 3: "tma"}[kernel]
+    assert plan.stats()["kernel"] == {1: "stream", 2: "latency", 3: "tma", 4: "tma_wide"}[kernel]
     sel, want = oracle_all(oracle, img, dst=dst, scale_suffix=sfx)
     assert_same(plan, outs, sel, want)
 
@@ -197,7 +197,7 @@ def test_alignment_sweep(stmat, oracle, residue):
     for dst in ("BF16", "F16", "F32", "KEEP"):
         sel, want = oracle_all(oracle, img, dst=dst)
         for packed in (False, True):
-            for kernel in (1, 2, 3):
+            for kernel in (1, 2, 3, 4):
                 plan, outs, _ = run(stmat, img, dst=dst, offset=residue, packed=packed,
                                     workers=[0, 7, 333][residue % 3], kernel=kernel)
                 assert_same(plan, outs, sel, want)
@@ -216,7 +216,7 @@ def test_data_section_edges(stmat, oracle):
         sel, want = oracle_all(oracle, img, dst="BF16")
         ix = stmat.Index.from_file(img)
         data = img[8 + ix.sizes()[0]:]
-        for kernel in (1, 2, 3):
+        for kernel in (1, 2, 3, 4):
             plan = ix.plan(dst="BF16", kernel=kernel)
             for shift in (1, 5, 9, 15):
                 buf = torch.zeros(data.size + 32, dtype=torch.uint8, device="cuda")
@@ -476,7 +476,7 @@ def sliced_image(seed):
     return image_of(ents, b"".join(parts), pad=5), shapes, rng
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 def test_sliced_outputs(stmat, oracle, kernel):
     """Slices on every dimension (contiguous and strided runs) at misaligned
     sources, into aligned and packed outputs."""
