@@ -561,7 +561,7 @@ static_assert(kSeg % 16 == 0 && kSeg >= 64, "segment size");
 
 // One staged segment: a run of one piece, elements [0, len); elements
 // [a, z) are in the slot, the rest are read with byte loads.
-struct SegMeta {
+struct alignas(16) SegMeta {
   uint8_t *dst;         // output address of element 0
   const uint8_t *gsrc;  // data-section address of element 0
   uint32_t len;         // elements (bytes for CLS_COPY)
@@ -572,9 +572,32 @@ struct SegMeta {
   // Block-scaled segments: the scale of the block holding element column
   // col0 is at sptr (the slot's scale area, or the data section itself when
   // the scales sit at an unaligned end of it); blocks are 1 << bcs columns.
-  const uint8_t *sptr;
   uint32_t col0, bcs;
+  const uint8_t *sptr;
+  uint64_t pad;
 };
+static_assert(sizeof(SegMeta) == 64, "segment metadata: four 16-byte words");
+
+// Segment metadata moves between the producer and the consumer as 16-byte
+// shared-memory words (the fourth only for block-scaled segments).
+__device__ __forceinline__ void put_meta(SegMeta *m, const SegMeta &v, bool quant) {
+  const uint4 *src = reinterpret_cast<const uint4 *>(&v);
+  uint4 *dst = reinterpret_cast<uint4 *>(m);
+  dst[0] = src[0];
+  dst[1] = src[1];
+  dst[2] = src[2];
+  if (quant) dst[3] = src[3];
+}
+__device__ __forceinline__ SegMeta get_meta(const SegMeta *m) {
+  SegMeta v;
+  const uint4 *src = reinterpret_cast<const uint4 *>(m);
+  uint4 *dst = reinterpret_cast<uint4 *>(&v);
+  dst[0] = src[0];
+  dst[1] = src[1];
+  dst[2] = src[2];
+  if (cls_quant(v.cls)) dst[3] = src[3];
+  return v;
+}
 
 // A segment of a block-scaled weight brings at most this many bytes of block
 // scales (the producer shortens the segment to fit), fetched with the
@@ -682,10 +705,12 @@ __device__ __forceinline__ void consume_seg(const uint8_t *buf, const SegMeta &m
   const float scale = m.scale;
   uint8_t *const dst = m.dst;
   const uint32_t len = m.len, off = m.off, a = m.a, z = m.z;
-  const uint32_t edge = a + (len - z);
-  for (uint32_t t = lane; t < edge; t += 32) {
-    const uint32_t e = t < a ? t : z + (t - a);
-    convert_one<CV>(m.gsrc + static_cast<uint64_t>(e) * SI, dst + static_cast<uint64_t>(e) * SO, scale);
+  const uint32_t edge = a + (len - z);  // elements outside the staged window: only at the data section's ends
+  if (edge) {
+    for (uint32_t t = lane; t < edge; t += 32) {
+      const uint32_t e = t < a ? t : z + (t - a);
+      convert_one<CV>(m.gsrc + static_cast<uint64_t>(e) * SI, dst + static_cast<uint64_t>(e) * SO, scale);
+    }
   }
   const uint32_t n = z - a;
   const uint8_t *sp = buf + off;
@@ -1108,7 +1133,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
         off = static_cast<uint32_t>(sa - w0);
       }
       if (lane == 0) {
-        SegMeta &m = ws.meta[slot];
+        SegMeta m;
         m.dst = run_dst + (static_cast<uint64_t>(cur.e) << sos);
         m.gsrc = s0;
         m.len = len;
@@ -1117,11 +1142,10 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
         m.off = off;
         m.scale = scale;
         m.cls = cls;
-        if (cls_quant(cls)) {
-          m.sptr = sptr;
-          m.col0 = col0;
-          m.bcs = qi.bc_shift;
-        }
+        m.col0 = col0;
+        m.bcs = qi.bc_shift;
+        m.sptr = sptr;
+        put_meta(&ws.meta[slot], m, cls_quant(cls));
         proxy_fence();
         mbar_expect(&ws.bar[slot], bytes + sbytes);
         if (bytes) bulk_copy(ws.buf[slot], reinterpret_cast<const void *>(w0), bytes, &ws.bar[slot]);
@@ -1161,7 +1185,10 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
       break;
     }
     __syncwarp();
-    consume_any(ws.buf[slot], ws.meta[slot], ws.qsc, lane);
+    {
+      const SegMeta m = get_meta(&ws.meta[slot]);
+      consume_any(ws.buf[slot], m, ws.qsc, lane);
+    }
     __syncwarp();
     ++jc;
   }
