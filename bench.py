@@ -415,6 +415,11 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     w = build_workload(args.workload, args.dst)
+    # pinned memory and reader threads on the GPU's own CPU socket
+    try:
+        host_cpus = stmat.host_affinity(local, apply=True)
+    except stmat.StmatError as e:
+        host_cpus = f"not bound: {e}"
     # source bytes in pinned host memory (the e2e source); data section on the device
     root, host, data_start = host_image(w, stmat, torch)
     ix = view_of(w)(root)
@@ -550,7 +555,7 @@ def run_ours(args, rank, world, local):
                        "shard_files": len(w.files),
                        "workers": st["workers"], "pieces": st["pieces"], "kernel_build": st["kernel"],
                        "launches_per_step": launches_per_step,
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}", "host_cpus": host_cpus},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
                          "peak_source": peak_src, "kernel": "materialize_" + st["kernel"],

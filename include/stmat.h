@@ -339,6 +339,15 @@ void st_files_close(st_files_t *files);
 st_status st_files_read(const st_files_t *files, uint64_t begin, uint64_t bytes, void *host,
                         uint32_t threads);
 
+/* The CPUs local to GPU `device` (from the PCI device's local_cpulist in
+ * sysfs), written to cpulist (len bytes, NUL-terminated, e.g. "0-71").  With
+ * apply != 0 the calling thread is also bound to them (threads it starts
+ * later inherit the binding), so that pinned host memory it allocates lands
+ * on the GPU's own socket: copies from another socket's memory cross the CPU
+ * interconnect.  Changes nothing outside the calling process.  ST_E_CUDA
+ * (no such device), ST_E_IO (sysfs unreadable), ST_E_INVAL (bad list). */
+st_status st_host_affinity(int device, int32_t apply, char *cpulist, size_t len);
+
 /* Materializes every output of the plan on `stream` (a cudaStream_t; NULL is
  * the legacy default stream), asynchronously, with no host synchronization.
  *   data_dev  device pointer to the data section (any alignment; the plan's

@@ -378,3 +378,61 @@ st_status st_cache_clear(st_cache_t *c) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ host locality
+//
+// Pinned staging memory and the threads that fill it belong on the CPU
+// socket the GPU hangs off: page-locked pages are placed where the thread
+// that allocates them runs, and copies from a remote socket's memory cross
+// the CPU interconnect.
+
+#include <sched.h>
+
+#include <cctype>
+
+#include <fstream>
+
+extern "C" {
+
+st_status st_host_affinity(int device, int32_t apply, char *cpulist, size_t len) {
+  char bus[64] = {0};
+  cudaError_t e = cudaDeviceGetPCIBusId(bus, sizeof bus, device);
+  if (e != cudaSuccess)
+    return set_error(ST_E_CUDA, "cudaDeviceGetPCIBusId(%d): %s", device, cudaGetErrorString(e));
+  for (char *c = bus; *c; ++c) *c = static_cast<char>(std::tolower(static_cast<unsigned char>(*c)));
+  std::string path = std::string("/sys/bus/pci/devices/") + bus + "/local_cpulist";
+  std::ifstream f(path);
+  std::string list;
+  if (!f || !std::getline(f, list) || list.empty())
+    return set_error(ST_E_IO, "cannot read %s", path.c_str());
+  if (cpulist && len) {
+    std::strncpy(cpulist, list.c_str(), len - 1);
+    cpulist[len - 1] = 0;
+  }
+  if (!apply) return ST_OK;
+  cpu_set_t set;
+  CPU_ZERO(&set);
+  size_t i = 0;
+  int count = 0;
+  while (i < list.size()) {  // "a-b,c,d-e"
+    size_t j = list.find(',', i);
+    if (j == std::string::npos) j = list.size();
+    const std::string item = list.substr(i, j - i);
+    const size_t dash = item.find('-');
+    char *end = nullptr;
+    const long lo = std::strtol(item.c_str(), &end, 10);
+    const long hi = dash == std::string::npos ? lo : std::strtol(item.c_str() + dash + 1, &end, 10);
+    if (lo < 0 || hi < lo || hi >= CPU_SETSIZE) return set_error(ST_E_INVAL, "cannot parse cpu list \"%s\"", list.c_str());
+    for (long c = lo; c <= hi; ++c) {
+      CPU_SET(static_cast<int>(c), &set);
+      ++count;
+    }
+    i = j + 1;
+  }
+  if (!count) return set_error(ST_E_INVAL, "empty cpu list for device %d", device);
+  if (sched_setaffinity(0, sizeof set, &set) != 0)
+    return set_error(ST_E_IO, "sched_setaffinity: %s", std::strerror(errno));
+  return ST_OK;
+}
+
+}  // extern "C"

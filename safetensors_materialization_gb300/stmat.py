@@ -33,7 +33,7 @@ EXPORTS = [
     "st_plan_piece", "st_plan_worker", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
     "st_materialize_noalloc", "st_index_open", "st_files_open", "st_files_close", "st_files_read",
     "st_load_files", "st_cache_create", "st_cache_free", "st_cache_get", "st_cache_release",
-    "st_cache_stats", "st_cache_clear", "st_load_tensors",
+    "st_cache_stats", "st_cache_clear", "st_load_tensors", "st_host_affinity",
     "st_last_error", "st_status_name", "st_dtype_size", "st_dtype_name", "st_version",
 ]
 
@@ -143,6 +143,7 @@ def lib():
             "st_cache_stats": [P, C.POINTER(CacheInfo)],
             "st_cache_clear": [P],
             "st_load_tensors": [P, P, P, C.POINTER(Selection), I, P, P, U64, U32, P],
+            "st_host_affinity": [I, C.c_int32, C.c_char_p, S],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -609,6 +610,14 @@ class Plan:
         if code not in (0, 14):
             _check(code)
         return flags.value
+
+
+def host_affinity(device=0, apply=True):
+    """st_host_affinity: the GPU's local CPU list; with apply, binds the
+    calling thread to it (do this before allocating pinned memory)."""
+    buf = C.create_string_buffer(4096)
+    _check(lib().st_host_affinity(device, 1 if apply else 0, buf, len(buf)))
+    return buf.value.decode()
 
 
 def stage_h2d(dst_dev, src_host, nbytes, chunk_bytes=0, stream=None, done_event=None):

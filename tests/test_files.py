@@ -134,3 +134,24 @@ def test_load_files_matches_oracle(stmat, oracle, tmp_path, chunk, slots):
         sel = oix.select(dst=dst)
         for i in range(len(sel)):
             assert np.array_equal(outs.raw(i).cpu().numpy(), sel.materialize(i, arena)), sel.output(i)["name"]
+
+
+@pytest.mark.gpu
+def test_host_affinity_binds_to_the_gpu_socket(stmat):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    before = os.sched_getaffinity(0)
+    try:
+        cpus = stmat.host_affinity(0, apply=False)
+        assert cpus and cpus[0].isdigit()
+        assert os.sched_getaffinity(0) == before          # apply=False changes nothing
+        stmat.host_affinity(0, apply=True)
+        now = os.sched_getaffinity(0)
+        listed = set()
+        for item in cpus.split(","):
+            a, _, b = item.partition("-")
+            listed |= set(range(int(a), int(b or a) + 1))
+        assert now == listed
+    finally:
+        os.sched_setaffinity(0, before)
