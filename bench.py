@@ -63,6 +63,19 @@ def dist_env():
     return rank, world, local
 
 
+def host_cpu_model():
+    """The host CPU's model name (lscpu's, from /proc/cpuinfo or the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -522,7 +535,18 @@ def run_ours(args, rank, world, local):
             t = torch.tensor([es], device="cuda")
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             es = float(t.item())
+        # the host link alone: st_stage_h2d of the data section, chunked like st_load
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stmat.stage_h2d(ddata, hdata, data_bytes, args.e2e_chunk_mb << 20, stream=copy)
+        copy.synchronize()
+        ev0.record(copy)
+        for _ in range(3):
+            stmat.stage_h2d(ddata, hdata, data_bytes, args.e2e_chunk_mb << 20, stream=copy)
+        ev1.record(copy)
+        copy.synchronize()
+        h2d_gbs = 3 * data_bytes / (ev0.elapsed_time(ev1) / 1e3) / 1e9
         e2e = {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "h2d_bytes_per_step": data_bytes,
+               "stage_h2d_gbs": round(h2d_gbs, 1),
                "d2h_bytes_per_step": 4, "ms_per_step": round(es * 1e3, 3),
                "chunk_bytes": args.e2e_chunk_mb << 20, "chunks": eplan.stats()["chunks"]}
 
@@ -540,7 +564,7 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, nbytes, dt = oracle_sample(w, args.cpu_seconds)
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
-               "seconds": round(dt, 2)}
+               "seconds": round(dt, 2), "host_cores": os.cpu_count(), "host_cpu": host_cpu_model()}
 
     if rank == 0:
         st = plan.stats()
@@ -560,6 +584,8 @@ def run_ours(args, rank, world, local):
                          "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
                          "peak_source": peak_src, "kernel": "materialize_" + st["kernel"],
                          "kernel_ms_mean": round(kernel_ms, 4), "kernel_ms_min": round(min(per), 4),
+                         "kernel_ms_median": round(statistics.median(per), 4),
+                         "frac_of_nominal_7900": round(achieved / 7900.0, 4),
                          "algorithmic_bytes_per_launch": src_bytes + dst_bytes},
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clk,
