@@ -1040,6 +1040,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   uint32_t count = 0, rows = 0, cls = 0, sis = 0, sos = 0;
   float scale = 1.0f;
   bool loaded = false;
+  bool interior = false;  // every byte of the piece lies in [lo16, hi16): no clipping
   // Block-scaled pieces: the output's scale table entry and the output unit
   // index of the piece's first unit.
   QuantInfo qi{};
@@ -1057,6 +1058,11 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
     run_src = a.data + pc.src;
     run_dst = dp + pc.dst;
     scale = ws.scl[cur.b & 1][cur.i];
+    {
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(run_src);
+      const uintptr_t hi = lo + static_cast<uint64_t>(rows - 1) * pitch + (static_cast<uint64_t>(count) << sis);
+      interior = lo >= lo16 && hi <= hi16;
+    }
     if (cls_quant(cls)) {
       qi = a.quant[pc.out_cls >> kClsBits];
       const uint64_t unit0 = pc.dst >> sos;  // one division per piece
@@ -1120,17 +1126,25 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
       const uint8_t *s0 = run_src + (static_cast<uint64_t>(cur.e) << sis);
       const uintptr_t s = reinterpret_cast<uintptr_t>(s0);
       const uintptr_t send = s + (static_cast<uint64_t>(len) << sis);
-      uint32_t A = 0, Z = len;
-      if (s < lo16) A = min(len, static_cast<uint32_t>((lo16 - s + (1u << sis) - 1) >> sis));
-      if (send > hi16) Z = hi16 > s ? static_cast<uint32_t>((hi16 - s) >> sis) : 0;
-      if (Z < A) Z = A;
-      uint32_t bytes = 0, off = 0;
-      uintptr_t w0 = 0;
-      if (Z > A) {
-        const uintptr_t sa = s + (static_cast<uint64_t>(A) << sis);
-        w0 = sa & ~uintptr_t(15);
-        bytes = static_cast<uint32_t>(((s + (static_cast<uint64_t>(Z) << sis) + 15) & ~uintptr_t(15)) - w0);
-        off = static_cast<uint32_t>(sa - w0);
+      uint32_t A = 0, Z = len, bytes, off;
+      uintptr_t w0;
+      if (interior) {
+        w0 = s & ~uintptr_t(15);
+        bytes = static_cast<uint32_t>(((send + 15) & ~uintptr_t(15)) - w0);
+        off = static_cast<uint32_t>(s - w0);
+      } else {  // the first or last piece of the data section: clip to [lo16, hi16)
+        if (s < lo16) A = min(len, static_cast<uint32_t>((lo16 - s + (1u << sis) - 1) >> sis));
+        if (send > hi16) Z = hi16 > s ? static_cast<uint32_t>((hi16 - s) >> sis) : 0;
+        if (Z < A) Z = A;
+        bytes = 0;
+        off = 0;
+        w0 = 0;
+        if (Z > A) {
+          const uintptr_t sa = s + (static_cast<uint64_t>(A) << sis);
+          w0 = sa & ~uintptr_t(15);
+          bytes = static_cast<uint32_t>(((s + (static_cast<uint64_t>(Z) << sis) + 15) & ~uintptr_t(15)) - w0);
+          off = static_cast<uint32_t>(sa - w0);
+        }
       }
       if (lane == 0) {
         SegMeta m;
