@@ -967,7 +967,11 @@ struct Cursor {
   uint32_t e;
 };
 
-template <int kSlots>
+// kInterior: compute per piece whether it lies inside the data section's
+// aligned interior, so its segments skip the clipping arithmetic (measured:
+// +2 % on many small tensors with the 4-slot shape; -1..3 % on the
+// register-capped wide shape, which keeps the general path).
+template <int kSlots, bool kInterior>
 __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   const uint32_t lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const uint32_t w = blockIdx.x * kWarpsPerBlock + wib;
@@ -1058,7 +1062,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
     run_src = a.data + pc.src;
     run_dst = dp + pc.dst;
     scale = ws.scl[cur.b & 1][cur.i];
-    {
+    if constexpr (kInterior) {
       const uintptr_t lo = reinterpret_cast<uintptr_t>(run_src);
       const uintptr_t hi = lo + static_cast<uint64_t>(rows - 1) * pitch + (static_cast<uint64_t>(count) << sis);
       interior = lo >= lo16 && hi <= hi16;
@@ -1128,7 +1132,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
       const uintptr_t send = s + (static_cast<uint64_t>(len) << sis);
       uint32_t A = 0, Z = len, bytes, off;
       uintptr_t w0;
-      if (interior) {
+      if (kInterior && interior) {
         w0 = s & ~uintptr_t(15);
         bytes = static_cast<uint32_t>(((send + 15) & ~uintptr_t(15)) - w0);
         off = static_cast<uint32_t>(s - w0);
@@ -1217,12 +1221,12 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
 
 __global__ void __launch_bounds__(kThreads, ST_TMA_MIN_BLOCKS) materialize_tma(const LaunchArgs a) {
   extern __shared__ __align__(128) uint8_t tma_smem[];
-  tma_body<ST_TMA_SLOTS>(a, tma_smem);
+  tma_body<ST_TMA_SLOTS, true>(a, tma_smem);
 }
 
 __global__ void __launch_bounds__(kThreads, ST_TMA_WIDE_MIN_BLOCKS) materialize_tma_wide(const LaunchArgs a) {
   extern __shared__ __align__(128) uint8_t tma_smem[];
-  tma_body<ST_TMA_WIDE_SLOTS>(a, tma_smem);
+  tma_body<ST_TMA_WIDE_SLOTS, false>(a, tma_smem);
 }
 
 std::string cuda_msg(cudaError_t e) { return std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e); }
