@@ -245,7 +245,9 @@ typedef struct st_plan_options {
   uint64_t chunk_bytes;   /* 0 = one launch over the whole data section; otherwise the data
                              section is split in chunks of this size for st_load's pipeline */
   int32_t host_only;      /* nonzero: build the plan without touching the GPU (requires workers) */
-  uint32_t blocks_per_sm; /* 0 = 3 for the streaming build, the most that fit for the latency build */
+  uint32_t blocks_per_sm; /* 0 = for the streaming build 2 when the outputs' contiguous runs
+                             average >= 64 KiB of traffic, else 3; the most that fit for the
+                             other builds */
   uint64_t unit_bytes;    /* traffic per interleaved unit; 0 = 32768 */
   uint32_t kernel;        /* 0 = choose: the TMA build when outputs average under 64 KiB of
                              traffic (many small tensors), else the streaming build; 1 = streaming

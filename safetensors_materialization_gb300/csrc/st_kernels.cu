@@ -188,8 +188,17 @@ struct CopyBytes {
 //  - LatencyCfg: half the depth, <= 40 registers (6 blocks per SM); for
 //    many small tensors, where per-piece latency dominates and more resident
 //    warps hide it.
+#ifndef ST_STREAM_U16
+#define ST_STREAM_U16 4
+#endif
+#ifndef ST_STREAM_U8
+#define ST_STREAM_U8 8
+#endif
+#ifndef ST_STREAM_U4
+#define ST_STREAM_U4 16
+#endif
 struct StreamCfg {
-  static constexpr int kU16 = 4, kU8 = 8, kU4 = 16;
+  static constexpr int kU16 = ST_STREAM_U16, kU8 = ST_STREAM_U8, kU4 = ST_STREAM_U4;
 };
 // Compile-time tuning knobs for the latency build (defaults measured best).
 #ifndef ST_LAT_U16
