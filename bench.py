@@ -338,8 +338,9 @@ def write_shards(w, host, data_start, stmat, tmp):
 def time_lazy(args, w, host, data_start, stmat, torch):
     """The lazy path: every output loaded alone through StreamStateDict
     (st_load_tensors) from the workload's files in the page cache; a cold
-    pass (every tensor read into the RAM tier) and a warm pass (every tensor
-    a RAM-tier hit).  Reports tensors/s and dst GB/s per pass."""
+    pass (every tensor read into the RAM tier), a warm pass (every tensor a
+    RAM-tier hit) and a pass without a RAM tier (each tensor copied straight
+    from the files' mappings).  Reports tensors/s and dst GB/s per pass."""
     import shutil
     import tempfile
     tmp = tempfile.mkdtemp(prefix="stmat_lazy_")
@@ -353,13 +354,16 @@ def time_lazy(args, w, host, data_start, stmat, torch):
             names = [n for n in names if not n.endswith(w.scale_suffix[1])]
         if w.quant:
             names = [n for n in names if n in w.quant]
+        sd0 = stmat.StreamStateDict(paths, dst=w.dst[0], ram_cache_bytes=0, threads=args.io_threads,
+                                    rename=w.rename or None, prefix=w.prefix, scale_suffix=w.scale_suffix,
+                                    quant=w.quant)
         res = {}
-        for label in ("cold", "warm"):
+        for label, d in (("cold", sd), ("warm", sd), ("no_ram_tier", sd0)):
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             nbytes = 0
             for n in names:
-                t = sd[n]
+                t = d[n]
                 nbytes += t.numel() * t.element_size()
                 del t
             torch.cuda.synchronize()
@@ -370,7 +374,8 @@ def time_lazy(args, w, host, data_start, stmat, torch):
         res.update({"tensors": len(names), "ram_tier": {"hits": st["hits"], "misses": st["misses"],
                                                          "bytes": st["bytes"]},
                     "source": "one st_load_tensors per tensor (header-only index, pread into the pinned RAM "
-                              "tier, staged copy, one launch); files in the page cache"})
+                              "tier or, without it, a copy from the files' mappings; staged copy, one launch); "
+                              "files in the page cache"})
         return res
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
@@ -378,13 +383,21 @@ def time_lazy(args, w, host, data_start, stmat, torch):
 
 def time_load_files(args, w, host, data_start, data_bytes, dev, outs, sel, stream, dist, world, gb_dst, stmat, torch):
     """st_load_files from the workload's shard files, written to a temp dir
-    just before (so they are read from the page cache): dst GB/s per step."""
+    just before (so they are read from the page cache): dst GB/s per step.
+    Ring-less (copies straight from the files' mappings) where the GPU reads
+    pageable memory through the host's page tables, else through a pinned
+    ring filled by pread threads; the other mode and a first load (files
+    opened, loaded once and closed inside each step: fresh mappings) are
+    listed beside it."""
     import shutil
     import tempfile
     tmp = tempfile.mkdtemp(prefix="stmat_bench_")
     try:
         paths = write_shards(w, host, data_start, stmat, tmp)
         files, fix = stmat.Files.of_checkpoint(paths)
+        opened = [stmat.Index.open(p) for p in paths]
+        _, bases = stmat.Index.concat([o[0] for o in opened])
+        parts = [(p, off, o.sizes()[1], b) for p, (o, off), b in zip(paths, opened, bases)]
         chunk = args.e2e_chunk_mb << 20
         fplan = view_of(w)(fix).plan(dst=w.dst[0], scale_suffix=w.scale_suffix, chunk_bytes=chunk,
                                      blocks_per_sm=args.blocks_per_sm, unit_bytes=args.unit_bytes,
@@ -392,33 +405,57 @@ def time_load_files(args, w, host, data_start, data_bytes, dev, outs, sel, strea
         ring = torch.empty(3 * chunk, dtype=torch.uint8).pin_memory()
         copy = torch.cuda.Stream()
         ddata = dev[:data_bytes]
-        for _ in range(2):
-            fplan.load_files(files, ddata, outs.ptrs, ring, threads=args.io_threads, copy_stream=copy,
+        direct = stmat.reads_pageable(torch.cuda.current_device())
+
+        def load(fl, r):
+            fplan.load_files(fl, ddata, outs.ptrs, r, threads=args.io_threads, copy_stream=copy,
                              compute_stream=stream)
-            fplan.check(stream)
-        if dist:
-            dist.barrier()
+            if fplan.check(stream) != 0:
+                raise RuntimeError("st_load_files flagged a bad destination")
+
+        def first_load(r):
+            fl = stmat.Files(parts)
+            load(fl, r)
+            fl.close()
+
         steps = max(3, min(args.steps, 5))
-        reps = []
-        for _ in range(3):
-            t0 = time.perf_counter()
-            for _ in range(steps):
-                fplan.load_files(files, ddata, outs.ptrs, ring, threads=args.io_threads, copy_stream=copy,
-                                 compute_stream=stream)
-                if fplan.check(stream) != 0:
-                    raise RuntimeError("st_load_files flagged a bad destination")
-            reps.append((time.perf_counter() - t0) / steps)
-        es = statistics.median(reps)
-        if dist:
-            t = torch.tensor([es], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            es = float(t.item())
+
+        def timed(step):
+            for _ in range(2):
+                step()
+            if dist:
+                dist.barrier()
+            reps = []
+            for _ in range(3):
+                t0 = time.perf_counter()
+                for _ in range(steps):
+                    step()
+                reps.append((time.perf_counter() - t0) / steps)
+            es = statistics.median(reps)
+            if dist:
+                t = torch.tensor([es], device="cuda")
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                es = float(t.item())
+            return es, reps
+
+        main_ring = None if direct else ring
+        es, reps = timed(lambda: load(files, main_ring))
+        other, _ = timed(lambda: load(files, ring if direct else None))
+        first, _ = timed(lambda: first_load(main_ring))
+        gbs = lambda t: round(gb_dst * world / t, 1)
         return {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "ms_per_step": round(es * 1e3, 3),
-                "repeats_gbs": [round(gb_dst * world / r, 1) for r in reps], "files": len(paths), "file_bytes_per_step": data_bytes, "chunk_bytes": chunk,
-                "ring_bytes": 3 * chunk, "io_threads": args.io_threads,
-                "source": "shard files in the page cache (written just before), pread into a pinned ring"}
+                "repeats_gbs": [gbs(r) for r in reps], "files": len(paths), "file_bytes_per_step": data_bytes,
+                "chunk_bytes": chunk,
+                "mode": "ring-less: copies from the files' mappings" if direct else
+                        f"pinned ring of {3 * chunk} bytes, {args.io_threads} pread threads",
+                "gpu_reads_pageable": direct,
+                ("ring_gbs" if direct else "ringless_gbs"): gbs(other),
+                "first_load_gbs": gbs(first),
+                "source": "shard files in the page cache (written just before); first_load opens, loads and "
+                          "closes the files inside each step"}
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
+
 
 def run_ours(args, rank, world, local):
     import torch

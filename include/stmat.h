@@ -330,8 +330,11 @@ typedef struct st_file_part {
 } st_file_part;
 
 /* Opens the files of `n` parts (read-only) and checks each holds its range;
- * the parts must not overlap in the arena.  ST_E_IO on open/stat failures or
- * a file too short, ST_E_INVAL on overlap.  The paths are copied. */
+ * the parts must not overlap in the arena.  Each file is also mapped
+ * read-only (shared) for ring-less st_load_files; a file that cannot be
+ * mapped is still opened (only ring-less loads of its bytes then fail).
+ * ST_E_IO on open/stat failures or a file too short, ST_E_INVAL on overlap.
+ * The paths are copied.  A file must not shrink while it is open. */
 st_status st_files_open(const st_file_part *parts, size_t n, st_files_t **out);
 void st_files_close(st_files_t *files);
 /* Reads arena bytes [begin, begin + bytes) into host[0, bytes) with up to
@@ -349,6 +352,25 @@ st_status st_files_read(const st_files_t *files, uint64_t begin, uint64_t bytes,
  * interconnect.  Changes nothing outside the calling process.  ST_E_CUDA
  * (no such device), ST_E_IO (sysfs unreadable), ST_E_INVAL (bad list). */
 st_status st_host_affinity(int device, int32_t apply, char *cpulist, size_t len);
+
+/* Faults arena bytes [begin, begin + bytes) into the page tables of the
+ * files' read-only mappings, reading pages that are not in the page cache
+ * from disk (madvise MADV_POPULATE_READ), on up to `threads` host threads
+ * (0: the calling thread); synchronous.  A prefetch: ring-less st_load_files does the same per chunk
+ * ahead of its copies.  ST_E_INVAL when the range leaves the arena, ST_E_IO
+ * when a page cannot be read (a file that shrank after it was opened, an I/O
+ * error); ST_OK without effect where the kernel lacks MADV_POPULATE_READ or a
+ * file could not be mapped. */
+st_status st_files_prefetch(const st_files_t *files, uint64_t begin, uint64_t bytes, uint32_t threads);
+
+/* *yes = 1 when GPU `device` reads pageable host memory through the host's
+ * page tables (cudaDevAttrPageableMemoryAccessUsesHostPageTables, e.g. a GPU
+ * attached to its CPU by a coherent link): copies from mapped files then go
+ * from the page cache to the device with no CPU copy, and ring-less
+ * st_load_files is the fast path.  Otherwise 0 (ring-less loads still work;
+ * the driver then stages each copy through its own buffers).  ST_E_CUDA when
+ * the device cannot be queried. */
+st_status st_device_reads_pageable(int device, int32_t *yes);
 
 /* Materializes every output of the plan on `stream` (a cudaStream_t; NULL is
  * the legacy default stream), asynchronously, with no host synchronization.
@@ -419,7 +441,9 @@ st_status st_cache_clear(st_cache_t *cache);
  * is loaded when it is accessed): the selected outputs of `sel` on `index`
  * (whose offsets are the arena of `files`), with the tensors they read
  * (their scales and block scales), are taken from `cache` (read from the
- * files on a miss; cache may be NULL: a plain read), copied into staging_dev
+ * files on a miss; cache may be NULL: then copied straight from the files'
+ * read-only mappings after st_files_prefetch of their bytes, or read when a
+ * file could not be mapped), copied into staging_dev
  * (each at a 256-byte aligned offset; staging_bytes must hold them all, else
  * ST_E_INVAL with the size needed) and materialized by one launch on
  * `stream`, with the plan's tables in the library's static device array as
@@ -443,12 +467,24 @@ st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_c
  * copy and kernel of chunk k.  ring_host: ring_bytes of host memory, pinned
  * for the copies to be asynchronous, holding at least one chunk (two or more
  * for overlap); a slot is reused only after its previous copy finished.
+ * Ring-less (ring_host NULL and ring_bytes 0): each chunk is copied to
+ * data_dev straight from the files' read-only mappings (cudaMemcpyAsync from
+ * pageable memory).  One host thread faults the chunks' pages into the page
+ * tables ahead of the copies (madvise MADV_POPULATE_READ, which reads pages
+ * not in the page cache from disk; `threads` is unused), and a page that
+ * cannot be read (a file that shrank, an I/O error) ends the load with
+ * ST_E_IO before that chunk's copy is queued.  On a GPU for which
+ * st_device_reads_pageable reports 1 the copy engine then reads the page
+ * cache directly.  Bytes of the arena that no file covers (gaps between
+ * joined shards) get no defined value in either mode.
  * The first copy waits for work already queued on compute_stream.  Blocks
  * the calling thread until every chunk is read and its copy finished (the
- * ring is then free); the kernels may still be running on compute_stream.
- * The plan's index must describe the files' arena (data_bytes = the arena
- * size).  Errors: ST_E_INVAL (arguments, ring too small, arena size),
- * ST_E_IO (reads), ST_E_CUDA. */
+ * ring is then free, the mappings no longer read: the files may be closed),
+ * also when it returns an error after queueing copies; the kernels may still
+ * be running on compute_stream.  The plan's index must describe the files'
+ * arena (data_bytes = the arena size).  Errors: ST_E_INVAL (arguments, ring
+ * too small, arena size), ST_E_IO (reads; a file that could not be mapped,
+ * ring-less), ST_E_CUDA. */
 st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t *plan,
                         void *const *dst_ptrs, const float *scales, void *ring_host, uint64_t ring_bytes,
                         uint32_t threads, void *copy_stream, void *compute_stream);

@@ -158,6 +158,23 @@ st_status static_scratch(void **addr);
 // Shard-file reads (st_io.cpp): arena bytes [begin, begin + bytes) into host.
 st_status read_arena(const st_files_s *f, uint64_t begin, uint64_t bytes, void *host, uint32_t threads);
 uint64_t files_arena_bytes(const st_files_s *f);
+bool files_mapped(const st_files_s *f);  // every non-empty part has its read-only mapping
+// Arena bytes [begin, begin + bytes) from the files' read-only mappings to
+// device memory dev[0, bytes) with cudaMemcpyAsync on `stream` (a
+// cudaStream_t); bytes no part covers are not written.
+st_status copy_arena_direct(const st_files_s *f, uint64_t begin, uint64_t bytes, void *dev, void *stream);
+// Populate threads for a load from the files' mappings: `threads` workers
+// fault the arena's pages into the page tables (MADV_POPULATE_READ, which
+// reads uncached pages from disk) in chunk order, ahead of the copies;
+// chunk k is arena bytes [begin + k * chunk, ...) (one chunk when chunk is 0).
+// populate_wait(k) blocks until chunk k's bytes are in (ST_E_IO when a page
+// could not be read: the file shrank or an I/O error; ST_OK at once where the
+// kernel lacks the call); populate_stop ends the workers and frees.
+struct Populator;
+Populator *populate_start(const st_files_s *f, uint64_t begin, uint64_t bytes, uint64_t chunk,
+                          uint32_t threads);
+st_status populate_wait(Populator *p, uint64_t k);
+void populate_stop(Populator *p);
 
 // Error reporting shared by the host files.
 st_status set_error(st_status s, const char *fmt, ...);

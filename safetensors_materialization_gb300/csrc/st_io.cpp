@@ -6,14 +6,21 @@
 // set of shard files is addressed as one arena (the layout st_index_concat
 // gives): arena byte x of part k lives at file offset offset_k + (x - base_k).
 // Reads use pread on host threads; the disk -> pinned -> device -> materialize
-// pipeline built on them is st_load_files (st_plan.cpp).
+// pipeline built on them is st_load_files (st_plan.cpp).  Each file is also
+// mapped read-only, so that on hosts whose GPU reads pageable memory through
+// the host's page tables a chunk can be copied to the device straight from
+// the page cache, with no CPU copy (st_load_files without a ring).
+#include <cuda_runtime_api.h>
 #include <fcntl.h>
+#include <sys/mman.h>
 #include <sys/stat.h>
 #include <unistd.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cerrno>
+#include <condition_variable>
+#include <mutex>
 #include <cstdlib>
 #include <cstring>
 #include <memory>
@@ -29,12 +36,16 @@ struct st_files_s {
     std::string path;
     int fd = -1;
     uint64_t offset = 0, bytes = 0, base = 0;
+    const uint8_t *map = nullptr;  // the whole file, PROT_READ / MAP_SHARED; NULL if mapping failed
+    uint64_t map_bytes = 0;
   };
   std::vector<Part> parts;  // sorted by base, non-overlapping
   uint64_t arena_bytes = 0;
   ~st_files_s() {
-    for (Part &p : parts)
+    for (Part &p : parts) {
+      if (p.map) munmap(const_cast<uint8_t *>(p.map), p.map_bytes);
       if (p.fd >= 0) close(p.fd);
+    }
   }
 };
 
@@ -121,6 +132,141 @@ st_status read_arena(const st_files_s *f, uint64_t begin, uint64_t bytes, void *
 
 uint64_t files_arena_bytes(const st_files_s *f) { return f->arena_bytes; }
 
+bool files_mapped(const st_files_s *f) {
+  for (const auto &p : f->parts)
+    if (!p.map && p.bytes) return false;
+  return true;
+}
+
+namespace {
+
+#ifndef MADV_POPULATE_READ
+#define MADV_POPULATE_READ 22  // Linux 5.14
+#endif
+
+// Faults arena bytes [begin, end) of the files' mappings into the process's
+// page tables, reading pages that are not cached.  1 = done, 0 = the kernel
+// lacks MADV_POPULATE_READ (nothing done), -1 = a page could not be read.
+int populate_range(const st_files_s &f, uint64_t begin, uint64_t end, std::string *msg) {
+  static const uint64_t page = static_cast<uint64_t>(sysconf(_SC_PAGESIZE));
+  for (const auto &p : f.parts) {
+    const uint64_t a = std::max(begin, p.base), b = std::min(end, p.base + p.bytes);
+    if (a >= b || !p.map) continue;
+    const uint64_t lo = (p.offset + (a - p.base)) / page * page;
+    const uint64_t hi = std::min(p.map_bytes, p.offset + (b - p.base));
+    if (madvise(const_cast<uint8_t *>(p.map) + lo, hi - lo, MADV_POPULATE_READ) != 0) {
+      if (errno == EINVAL) return 0;
+      *msg = "reading bytes " + std::to_string(lo) + ".." + std::to_string(hi) + " of " + p.path + " (mapped): " +
+             std::strerror(errno) + " (did the file shrink?)";
+      return -1;
+    }
+  }
+  return 1;
+}
+
+}  // namespace
+
+// Populate threads: jobs of at most kJob arena bytes in arena order, taken by
+// `threads` workers; the job list of chunk k is [first[k], first[k + 1]).
+struct Populator {
+  static constexpr uint64_t kJob = 32ull << 20;
+  const st_files_s *files;
+  std::vector<uint64_t> lo, hi;
+  std::vector<size_t> first;
+  std::vector<int8_t> state;  // 0 pending, 1 done, -1 failed (guarded by m)
+  std::vector<std::string> msg;
+  std::atomic<size_t> next{0};
+  std::atomic<bool> stop{false};
+  std::mutex m;
+  std::condition_variable cv;
+  std::vector<std::thread> pool;
+};
+
+Populator *populate_start(const st_files_s *f, uint64_t begin, uint64_t bytes, uint64_t chunk,
+                          uint32_t threads) try {
+  auto *P = new Populator;
+  P->files = f;
+  const uint64_t C = chunk ? chunk : (bytes ? bytes : 1), end = begin + bytes;
+  for (uint64_t c0 = begin; c0 < end; c0 += C) {
+    P->first.push_back(P->lo.size());
+    const uint64_t c1 = std::min(end, c0 + C);
+    for (uint64_t x = c0; x < c1; x += Populator::kJob) {
+      P->lo.push_back(x);
+      P->hi.push_back(std::min(c1, x + Populator::kJob));
+    }
+  }
+  P->first.push_back(P->lo.size());
+  P->state.assign(P->lo.size(), 0);
+  P->msg.resize(P->lo.size());
+  const uint32_t t = std::min<uint32_t>(threads, 16);  // 0: populate_wait does the jobs on the calling thread
+  try {
+    for (uint32_t i = 0; i < t && i < P->lo.size(); ++i)
+      P->pool.emplace_back([P] {
+        bool supported = true;
+        for (;;) {
+          const size_t j = P->next.fetch_add(1);
+          if (j >= P->lo.size() || P->stop.load()) break;
+          std::string msg;
+          const int r = supported ? populate_range(*P->files, P->lo[j], P->hi[j], &msg) : 0;
+          if (r == 0) supported = false;
+          {
+            std::lock_guard<std::mutex> g(P->m);
+            P->state[j] = r < 0 ? -1 : 1;
+            if (r < 0) P->msg[j] = std::move(msg);
+          }
+          P->cv.notify_all();
+        }
+      });
+  } catch (const std::exception &) {
+    // Fewer workers (or none): populate_wait then does the missing jobs itself.
+  }
+  return P;
+} catch (const std::bad_alloc &) {
+  return nullptr;
+}
+
+st_status populate_wait(Populator *P, uint64_t k) {
+  if (k + 1 >= P->first.size()) return ST_OK;
+  std::unique_lock<std::mutex> g(P->m);
+  for (size_t j = P->first[k]; j < P->first[k + 1]; ++j) {
+    if (P->pool.empty() && P->state[j] == 0) {  // no workers: populate here
+      g.unlock();
+      std::string msg;
+      const int r = populate_range(*P->files, P->lo[j], P->hi[j], &msg);
+      g.lock();
+      P->state[j] = r < 0 ? -1 : 1;
+      if (r < 0) P->msg[j] = std::move(msg);
+    }
+    P->cv.wait(g, [&] { return P->state[j] != 0; });
+    if (P->state[j] < 0) return set_error(ST_E_IO, "%s", P->msg[j].c_str());
+  }
+  return ST_OK;
+}
+
+void populate_stop(Populator *P) {
+  if (!P) return;
+  P->stop = true;
+  for (auto &th : P->pool) th.join();
+  delete P;
+}
+
+st_status copy_arena_direct(const st_files_s *f, uint64_t begin, uint64_t bytes, void *dev, void *stream) {
+  if (begin > f->arena_bytes || bytes > f->arena_bytes - begin)
+    return set_error(ST_E_INVAL, "range %llu + %llu is beyond the %llu-byte arena", (unsigned long long)begin,
+                     (unsigned long long)bytes, (unsigned long long)f->arena_bytes);
+  for (const auto &p : f->parts) {
+    const uint64_t a = std::max(begin, p.base), b = std::min(begin + bytes, p.base + p.bytes);
+    if (a >= b) continue;
+    if (!p.map) return set_error(ST_E_IO, "%s could not be mapped: pass a pinned ring instead", p.path.c_str());
+    const cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t *>(dev) + (a - begin), p.map + p.offset + (a - p.base),
+                                          b - a, cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+      return set_error(ST_E_CUDA, "copy of %llu bytes of %s: %s", (unsigned long long)(b - a), p.path.c_str(),
+                       cudaGetErrorString(e));
+  }
+  return ST_OK;
+}
+
 }  // namespace stmat
 
 using namespace stmat;
@@ -188,6 +334,13 @@ st_status st_files_open(const st_file_part *parts, size_t n, st_files_t **out) {
       if (static_cast<uint64_t>(sb.st_size) < p.offset + p.bytes)
         return set_error(ST_E_IO, "%s holds %llu bytes; part %zu needs %llu", p.path, (unsigned long long)sb.st_size,
                          k, (unsigned long long)(p.offset + p.bytes));
+      if (sb.st_size > 0) {  // a failed mapping only rules out ring-less loads
+        void *m = mmap(nullptr, static_cast<size_t>(sb.st_size), PROT_READ, MAP_SHARED, f->parts.back().fd, 0);
+        if (m != MAP_FAILED) {
+          f->parts.back().map = static_cast<const uint8_t *>(m);
+          f->parts.back().map_bytes = static_cast<uint64_t>(sb.st_size);
+        }
+      }
     }
     std::sort(f->parts.begin(), f->parts.end(),
               [](const st_files_s::Part &a, const st_files_s::Part &b) { return a.base < b.base; });
@@ -210,6 +363,28 @@ st_status st_files_read(const st_files_t *files, uint64_t begin, uint64_t bytes,
   return read_arena(files, begin, bytes, host, threads);
 }
 
+st_status st_files_prefetch(const st_files_t *files, uint64_t begin, uint64_t bytes, uint32_t threads) {
+  if (!files) return set_error(ST_E_INVAL, "NULL files");
+  if (begin > files->arena_bytes || bytes > files->arena_bytes - begin)
+    return set_error(ST_E_INVAL, "range %llu + %llu is beyond the %llu-byte arena", (unsigned long long)begin,
+                     (unsigned long long)bytes, (unsigned long long)files->arena_bytes);
+  if (!bytes) return ST_OK;
+  Populator *P = populate_start(files, begin, bytes, 0, threads);
+  if (!P) return set_error(ST_E_NOMEM, "starting the populate threads");
+  const st_status s = populate_wait(P, 0);
+  populate_stop(P);
+  return s;
+}
+
+st_status st_device_reads_pageable(int device, int32_t *yes) {
+  if (!yes) return set_error(ST_E_INVAL, "NULL argument");
+  int v = 0;
+  const cudaError_t e = cudaDeviceGetAttribute(&v, cudaDevAttrPageableMemoryAccessUsesHostPageTables, device);
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "device %d: %s", device, cudaGetErrorString(e));
+  *yes = v ? 1 : 0;
+  return ST_OK;
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------ RAM tier
@@ -220,8 +395,6 @@ st_status st_files_read(const st_files_t *files, uint64_t begin, uint64_t bytes,
 // on its next use).  An entry is keyed by (files, arena range); get() holds
 // it until release(), and held entries are never evicted.  An entry larger
 // than the bound is read but not kept (dropped on release).
-
-#include <cuda_runtime_api.h>
 
 #include <list>
 #include <map>

@@ -33,7 +33,8 @@ EXPORTS = [
     "st_plan_piece", "st_plan_worker", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
     "st_materialize_noalloc", "st_index_open", "st_files_open", "st_files_close", "st_files_read",
     "st_load_files", "st_cache_create", "st_cache_free", "st_cache_get", "st_cache_release",
-    "st_cache_stats", "st_cache_clear", "st_load_tensors", "st_host_affinity",
+    "st_cache_stats", "st_cache_clear", "st_load_tensors", "st_host_affinity", "st_device_reads_pageable",
+    "st_files_prefetch",
     "st_last_error", "st_status_name", "st_dtype_size", "st_dtype_name", "st_version",
 ]
 
@@ -144,6 +145,8 @@ def lib():
             "st_cache_clear": [P],
             "st_load_tensors": [P, P, P, C.POINTER(Selection), I, P, P, U64, U32, P],
             "st_host_affinity": [I, C.c_int32, C.c_char_p, S],
+            "st_device_reads_pageable": [I, C.POINTER(C.c_int32)],
+            "st_files_prefetch": [P, U64, U64, U32],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -379,6 +382,7 @@ class Files:
         out = C.c_void_p()
         _check(lib().st_files_open(arr, len(parts), C.byref(out)))
         self._h = C.c_void_p(out.value)
+        self.arena_bytes = max((base + n for _, _, n, base in parts), default=0)
 
     @classmethod
     def of_checkpoint(cls, paths, align=256):
@@ -389,18 +393,31 @@ class Files:
         parts = [(p, off, o.sizes()[1], b) for p, (o, off), b in zip(paths, opened, bases)]
         return cls(parts), ix
 
-    def __del__(self):
+    def close(self):
+        """st_files_close (also on garbage collection)."""
         if getattr(self, "_h", None) and self._h.value and _lib is not None:
             _lib.st_files_close(self._h)
             self._h = C.c_void_p(None)
 
+    def __del__(self):
+        self.close()
+
     @property
     def handle(self):
+        if not self._h.value:
+            raise StmatError(1, "the files are closed")
         return self._h
+
+    def prefetch(self, begin=0, nbytes=None, threads=4):
+        """st_files_prefetch: fault arena bytes into the mappings' page tables
+        (reads uncached pages from disk); default the whole arena."""
+        if nbytes is None:
+            nbytes = self.arena_bytes - begin
+        _check(lib().st_files_prefetch(self.handle, begin, nbytes, threads))
 
     def read(self, begin, nbytes, host, threads=4):
         """st_files_read into `host` (a numpy uint8 array or torch tensor)."""
-        _check(lib().st_files_read(self._h, begin, nbytes, _addr(host), threads))
+        _check(lib().st_files_read(self.handle, begin, nbytes, _addr(host), threads))
 
 
 class Cache:
@@ -594,11 +611,14 @@ class Plan:
         _check(lib().st_load(_addr(data_host), _addr(data_dev), self._h, _addr(dst_ptrs), _addr(scales),
                              _stream(copy_stream), _stream(compute_stream)))
 
-    def load_files(self, files, data_dev, dst_ptrs, ring_host, ring_bytes=None, threads=8, scales=None,
+    def load_files(self, files, data_dev, dst_ptrs, ring_host=None, ring_bytes=None, threads=8, scales=None,
                    copy_stream=None, compute_stream=None):
         """st_load_files: disk -> pinned ring -> device, each chunk materialized
-        as soon as it lands."""
-        if ring_bytes is None:
+        as soon as it lands; with ring_host None, each chunk is copied straight
+        from the files' mappings (the fast path where reads_pageable() holds)."""
+        if ring_bytes is None and ring_host is None:
+            ring_bytes = 0
+        elif ring_bytes is None:
             ring_bytes = ring_host.numel() if hasattr(ring_host, "numel") else len(ring_host)
         _check(lib().st_load_files(files.handle, _addr(data_dev), self._h, _addr(dst_ptrs), _addr(scales),
                                    _addr(ring_host), ring_bytes, threads, _stream(copy_stream),
@@ -618,6 +638,15 @@ def host_affinity(device=0, apply=True):
     buf = C.create_string_buffer(4096)
     _check(lib().st_host_affinity(device, 1 if apply else 0, buf, len(buf)))
     return buf.value.decode()
+
+
+def reads_pageable(device=0):
+    """st_device_reads_pageable: whether the GPU reads pageable host memory
+    through the host's page tables (ring-less file loads are then copy-engine
+    reads of the page cache)."""
+    yes = C.c_int32()
+    _check(lib().st_device_reads_pageable(device, C.byref(yes)))
+    return bool(yes.value)
 
 
 def stage_h2d(dst_dev, src_host, nbytes, chunk_bytes=0, stream=None, done_event=None):

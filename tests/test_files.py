@@ -106,9 +106,41 @@ def test_file_errors(stmat, tmp_path):
     assert e.value.status == "ST_E_IO"
 
 
+@pytest.mark.parametrize("threads", [0, 1, 3])
+def test_prefetch_and_its_guard(stmat, tmp_path, threads):
+    """st_files_prefetch faults the mappings in (the step ring-less loads take
+    before each copy); a file that shrank after opening is ST_E_IO there, so a
+    ring-less load stops before queueing a copy of missing pages."""
+    w = small_llm()
+    paths, datas = write_shards(str(tmp_path), w)
+    files, ix = stmat.Files.of_checkpoint(paths)
+    total = ix.sizes()[1]
+    files.prefetch(threads=threads)
+    files.prefetch(total // 3, total // 3, threads=threads)
+    files.prefetch(total, 0)
+    got = np.zeros(total, np.uint8)
+    files.read(0, total, got, threads=2)                  # unchanged by the prefetch
+    with pytest.raises(stmat.StmatError) as e:
+        files.prefetch(total - 10, 11)
+    assert e.value.status == "ST_E_INVAL"
+    files.close()
+    blob = os.path.join(str(tmp_path), "blob.bin")
+    np.arange(3 << 20, dtype=np.uint32).astype(np.uint8).tofile(blob)
+    bf = stmat.Files([(blob, 4096, (3 << 20) - 4096, 0)])
+    bf.prefetch(threads=threads)
+    os.truncate(blob, 1 << 20)                            # drops 2 MiB: many whole pages of any size
+    with pytest.raises(stmat.StmatError) as e:
+        bf.prefetch(threads=threads)
+    assert e.value.status == "ST_E_IO" and "shrink" in str(e.value)
+    bf.prefetch(0, (1 << 19), threads=threads)            # the part still in the file is fine
+    bf.close()
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("chunk,slots", [(0, 1), (1 << 16, 2), (1 << 20, 3), (3 << 20, 2)])
+@pytest.mark.parametrize("chunk,slots", [(0, 1), (1 << 16, 2), (1 << 20, 3), (3 << 20, 2),
+                                         (0, 0), (1 << 16, 0), (3 << 20, 0)])
 def test_load_files_matches_oracle(stmat, oracle, tmp_path, chunk, slots):
+    """slots == 0: ring-less, every chunk copied from the files' mappings."""
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
@@ -119,8 +151,8 @@ def test_load_files_matches_oracle(stmat, oracle, tmp_path, chunk, slots):
     for dst in ("BF16", "F16"):
         plan = ix.plan(dst=dst, chunk_bytes=chunk)
         C = chunk or total
-        ring = torch.empty(C * slots, dtype=torch.uint8).pin_memory()
-        dev = torch.empty(total, dtype=torch.uint8, device="cuda")
+        ring = torch.empty(C * slots, dtype=torch.uint8).pin_memory() if slots else None
+        dev = torch.full((total,), 0xA5, dtype=torch.uint8, device="cuda")
         outs = stmat.Outputs(plan)
         copy = torch.cuda.Stream()
         plan.load_files(files, dev, outs.ptrs, ring, threads=4, copy_stream=copy,
@@ -134,6 +166,47 @@ def test_load_files_matches_oracle(stmat, oracle, tmp_path, chunk, slots):
         sel = oix.select(dst=dst)
         for i in range(len(sel)):
             assert np.array_equal(outs.raw(i).cpu().numpy(), sel.materialize(i, arena)), sel.output(i)["name"]
+
+
+@pytest.mark.gpu
+def test_load_files_ringless_block_scaled_and_errors(stmat, oracle, tmp_path):
+    """Ring-less loads of block-scaled weights through a view (scales read by
+    the kernel from chunks landed earlier), a ring pointer without a size and
+    the reverse, and the files closed right after a load returns."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    assert isinstance(stmat.reads_pageable(0), bool)
+    import test_blockscale as TB
+    img, quant = TB.quant_file(70, lead=3)
+    path = os.path.join(str(tmp_path), "q.safetensors")
+    img.tofile(path)
+    oix = oracle.parse(img)
+    data = img[8 + oix.header_len:]
+    for chunk in (0, 1 << 12, 5000):
+        files, ix = stmat.Files.of_checkpoint([path])
+        names, q = TB.selection(ix, quant)
+        plan = ix.plan(dst="BF16", names=names, quant=q, chunk_bytes=chunk)
+        dev = torch.empty(data.size, dtype=torch.uint8, device="cuda")
+        outs = stmat.Outputs(plan)
+        plan.load_files(files, dev, outs.ptrs, None, copy_stream=torch.cuda.Stream(),
+                        compute_stream=torch.cuda.current_stream())
+        files.close()                                      # the copies are done when load_files returns
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        sel = oix.select(names=names, dst="BF16", quant=q)
+        for i in range(len(sel)):
+            assert np.array_equal(outs.raw(i).cpu().numpy(), sel.materialize(i, data)), sel.output(i)["name"]
+    files, ix = stmat.Files.of_checkpoint([path])
+    plan = ix.plan(dst="F32")
+    dev = torch.empty(data.size, dtype=torch.uint8, device="cuda")
+    outs = stmat.Outputs(plan)
+    ring = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
+    for args in ((None, 4096), (ring, 0)):
+        with pytest.raises(stmat.StmatError) as e:
+            plan.load_files(files, dev, outs.ptrs, args[0], ring_bytes=args[1])
+        assert e.value.status == "ST_E_INVAL"
+    torch.cuda.synchronize()
 
 
 @pytest.mark.gpu
