@@ -39,6 +39,8 @@ constexpr uint64_t kPieceCost = 1024;       // fixed cost of a piece, in bytes o
 constexpr uint64_t kMinWorkerCost = 4096;   // no more warps than total cost / this
 constexpr uint64_t kMaxPieceUnits = 1ull << 30;
 constexpr uint64_t kDefaultUnitBytes = 32768;  // cost of one interleaved unit
+constexpr uint64_t kLazyBytesPerWarp = 16384;  // st_load_tensors: traffic per warp
+constexpr uint64_t kLazyMaxWarps = 2432;        // ... and at most this many warps (2 blocks on each of 152 SMs)
 constexpr uint32_t kStreamBlocksPerSm = 3;     // streaming build: fewer, deeper warps ...
 constexpr uint32_t kStreamBlocksPerSmLong = 2;  // ... and fewer still when the contiguous runs are long
 constexpr uint64_t kLongRunBytes = 65536;       // mean traffic per contiguous run that counts as long
@@ -1100,9 +1102,13 @@ st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_c
     auto mini = make_root(core);
     s = finish_view(mini.get());
     if (s != ST_OK) return s;
-    // Units large enough that the tables fit the static array.
+    // Units large enough that the tables fit the static array, and warps in
+    // proportion to the traffic: the host plan and its tables grow with the
+    // warp count, and one tensor's launch needs few warps (its GPU time
+    // overlaps the next call's host work).
     st_plan_options po{};
     po.unit_bytes = std::max<uint64_t>(kDefaultUnitBytes, traffic / 32768 + 1);
+    po.workers = static_cast<uint32_t>(std::min<uint64_t>(kLazyMaxWarps, (traffic / kLazyBytesPerWarp + 8) & ~7ull));
     st_plan_s plan;
     s = plan_host(mini, sel, dst_dtype, &po, &plan);
     if (s != ST_OK) return s;

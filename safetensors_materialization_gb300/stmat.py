@@ -484,6 +484,7 @@ class StreamStateDict:
         self._staging = None
         self._names = [e["name"] for e in view.entries()]
         self._pos = {n: i for i, n in enumerate(self._names)}
+        self._info = {}  # name -> (shape, dtype, staging bytes), filled on first use
 
     def keys(self):
         return list(self._names)
@@ -500,11 +501,19 @@ class StreamStateDict:
     def metadata(self):
         return self.index.metadata()
 
+    def _lookup(self, name):
+        got = self._info.get(name)
+        if got is None:
+            o = self._plan(name, host_only=True).outputs()[0]
+            e = self.index.entry(self._pos[name])
+            got = (o["shape"], o["dtype"], int((e["end"] - e["begin"]) * 1.25) + (1 << 16))
+            self._info[name] = got
+        return got
+
     def info(self, name):
         """Shape and dtype of sd[name] (header only)."""
-        plan = self._plan(name, host_only=True)
-        o = plan.outputs()[0]
-        return o["shape"], o["dtype"]
+        shape, dt, _ = self._lookup(name)
+        return shape, dt
 
     def meta(self, name):
         import torch
@@ -522,10 +531,8 @@ class StreamStateDict:
         import torch
         if name not in self._pos:
             raise KeyError(name)
-        shape, dt = self.info(name)
+        shape, dt, need = self._lookup(name)
         out = torch.empty(shape, dtype=torch_dtype(dt), device=self.device)
-        e = self.index.entry(self._pos[name])
-        need = int((e["end"] - e["begin"]) * 1.25) + (1 << 16)
         if self._staging is None or self._staging.numel() < need:
             self._staging = torch.empty(need, dtype=torch.uint8, device=self.device)
         self.index.load_tensors(self.files, [out.data_ptr()], self._staging, dst=self.dst, cache=self.cache,
