@@ -421,7 +421,8 @@ typedef struct st_cache_info {
 /* pinned != 0: entries live in page-locked memory (cudaHostAlloc), so
  * copies from them to the GPU are asynchronous; else pageable malloc. */
 st_status st_cache_create(uint64_t max_bytes, int32_t pinned, st_cache_t **out);
-/* Frees every entry, held or not: release all holds first. */
+/* Waits for the copies of st_load_tensors calls that still read entries,
+ * then frees every entry, held or not: release all holds first. */
 void st_cache_free(st_cache_t *cache);
 /* The host copy of arena bytes [begin, begin + bytes) of `files`: a hit
  * returns the kept copy (now the most recently used); a miss reads it with
@@ -434,7 +435,8 @@ st_status st_cache_get(st_cache_t *cache, const st_files_t *files, uint64_t begi
                        uint32_t threads, const void **host);
 st_status st_cache_release(st_cache_t *cache, const void *host);
 st_status st_cache_stats(const st_cache_t *cache, st_cache_info *info);
-/* Drops every entry nobody holds. */
+/* Waits for the copies of st_load_tensors calls that still read entries
+ * (releasing their holds), then drops every entry nobody holds. */
 st_status st_cache_clear(st_cache_t *cache);
 
 /* The lazy path for a few tensors ("Streaming safetensors mapping": a tensor
@@ -452,8 +454,13 @@ st_status st_cache_clear(st_cache_t *cache);
  *   dst_host_ptrs  HOST array of one destination (device) pointer per output,
  *                  in the selection's output order; each non-NULL and aligned
  *                  to the output's itemsize (ST_E_INVAL otherwise).
- * Blocks until the staging copies are done (the cache entries are then
- * released); the kernel runs asynchronously on `stream`.  Output dtypes,
+ * With a cache: returns once the staging copies are queued; the entries
+ * they read stay held until the copies finish and are released by the next
+ * st_cache_get or st_cache_stats on that cache that finds them finished
+ * (st_cache_clear and st_cache_free wait for them), so the bound may be
+ * exceeded meanwhile.  Without a cache: blocks until the copies are done
+ * (the files may then be closed).  The kernel runs asynchronously on
+ * `stream`; staging_dev is in use until it has run.  Output dtypes,
  * errors and bit-exact results are those of st_plan + st_materialize. */
 st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_cache_t *cache,
                           const st_selection *sel, st_dtype dst_dtype, void *const *dst_host_ptrs,

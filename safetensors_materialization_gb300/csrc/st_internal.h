@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <vector>
 
 #include "stmat.h"
 
@@ -171,6 +172,12 @@ st_status copy_arena_direct(const st_files_s *f, uint64_t begin, uint64_t bytes,
 // could not be read: the file shrank or an I/O error; ST_OK at once where the
 // kernel lacks the call); populate_stop ends the workers and frees.
 struct Populator;
+// Hands one hold on each of `hosts` (entries of `cache`) over to be dropped
+// once `event` (a cudaEvent_t recorded after the copies that read them; the
+// cache destroys it) has completed: the next st_cache_get or st_cache_stats
+// that finds it complete drops them, st_cache_clear and st_cache_free wait
+// for it.  False (nothing handed over) when out of host memory.
+bool cache_release_after(st_cache_s *cache, void *event, const std::vector<const void *> &hosts);
 Populator *populate_start(const st_files_s *f, uint64_t begin, uint64_t bytes, uint64_t chunk,
                           uint32_t threads);
 st_status populate_wait(Populator *p, uint64_t k);

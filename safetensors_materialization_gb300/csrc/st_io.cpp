@@ -417,6 +417,13 @@ struct st_cache_s {
   std::map<Key, std::list<Entry>::iterator> by_key;
   std::map<const void *, std::list<Entry>::iterator> by_ptr;
   std::list<Entry> transient;                            // too large to keep
+  // Holds handed over by st_load_tensors: released once the event (recorded
+  // after the copies that read those entries) has completed.
+  struct Pending {
+    cudaEvent_t ev;
+    std::vector<const void *> hosts;
+  };
+  std::vector<Pending> pending;
 
   uint8_t *alloc(uint64_t n) {
     void *p = nullptr;
@@ -445,11 +452,56 @@ struct st_cache_s {
       it = lru.erase(it);
     }
   }
+  // Drops one hold (mu held); an entry too large to keep is freed with its last hold.
+  bool release_locked(const void *host) {
+    auto it = by_ptr.find(host);
+    if (it == by_ptr.end() || it->second->holds == 0) return false;
+    auto e = it->second;
+    if (--e->holds == 0 && !e->kept) {
+      by_ptr.erase(it);
+      dealloc(e->host);
+      transient.erase(e);
+    }
+    return true;
+  }
+  // Releases the pending holds whose copies have finished (mu held); with
+  // `wait`, waits for all of them first.
+  void reap(bool wait) {
+    size_t kept = 0;
+    for (size_t i = 0; i < pending.size(); ++i) {
+      Pending &p = pending[i];
+      cudaError_t e = wait ? cudaEventSynchronize(p.ev) : cudaEventQuery(p.ev);
+      if (e == cudaErrorNotReady) {
+        (void)cudaGetLastError();  // not-ready is recorded as the last error: clear it
+        pending[kept++] = std::move(p);
+        continue;
+      }
+      // Done, or the context failed (then no copy reads the entries any more).
+      for (const void *h : p.hosts) release_locked(h);
+      cudaEventDestroy(p.ev);
+    }
+    pending.resize(kept);
+  }
   ~st_cache_s() {
+    reap(true);
     for (Entry &e : lru) dealloc(e.host);
     for (Entry &e : transient) dealloc(e.host);
   }
 };
+
+namespace stmat {
+
+bool cache_release_after(st_cache_s *c, void *event, const std::vector<const void *> &hosts) {
+  std::lock_guard<std::mutex> lock(c->mu);
+  try {
+    c->pending.push_back({static_cast<cudaEvent_t>(event), hosts});
+  } catch (const std::bad_alloc &) {
+    return false;
+  }
+  return true;
+}
+
+}  // namespace stmat
 
 extern "C" {
 
@@ -470,6 +522,7 @@ st_status st_cache_get(st_cache_t *c, const st_files_t *files, uint64_t begin, u
   if (!c || !files || !host) return set_error(ST_E_INVAL, "NULL argument");
   *host = nullptr;
   std::lock_guard<std::mutex> lock(c->mu);
+  c->reap(false);
   const st_cache_s::Key key(files, begin, bytes);
   auto hit = c->by_key.find(key);
   if (hit != c->by_key.end()) {
@@ -516,21 +569,14 @@ st_status st_cache_get(st_cache_t *c, const st_files_t *files, uint64_t begin, u
 st_status st_cache_release(st_cache_t *c, const void *host) {
   if (!c || !host) return set_error(ST_E_INVAL, "NULL argument");
   std::lock_guard<std::mutex> lock(c->mu);
-  auto it = c->by_ptr.find(host);
-  if (it == c->by_ptr.end() || it->second->holds == 0)
-    return set_error(ST_E_INVAL, "%p is not a held cache entry", host);
-  auto e = it->second;
-  if (--e->holds == 0 && !e->kept) {
-    c->by_ptr.erase(it);
-    c->dealloc(e->host);
-    c->transient.erase(e);
-  }
+  if (!c->release_locked(host)) return set_error(ST_E_INVAL, "%p is not a held cache entry", host);
   return ST_OK;
 }
 
 st_status st_cache_stats(const st_cache_t *c, st_cache_info *info) {
   if (!c || !info) return set_error(ST_E_INVAL, "NULL argument");
   std::lock_guard<std::mutex> lock(const_cast<st_cache_s *>(c)->mu);
+  const_cast<st_cache_s *>(c)->reap(false);
   info->bytes = c->bytes;
   info->max_bytes = c->max_bytes;
   info->entries = c->lru.size();
@@ -543,6 +589,7 @@ st_status st_cache_stats(const st_cache_t *c, st_cache_info *info) {
 st_status st_cache_clear(st_cache_t *c) {
   if (!c) return set_error(ST_E_INVAL, "NULL cache");
   std::lock_guard<std::mutex> lock(c->mu);
+  c->reap(true);
   const uint64_t keep = c->max_bytes;
   c->max_bytes = 0;
   c->make_room(0);

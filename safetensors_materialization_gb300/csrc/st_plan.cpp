@@ -1159,7 +1159,13 @@ st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_c
     cudaEvent_t done = nullptr;
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventRecord(done, st);
-    if (e == cudaSuccess) e = cudaEventSynchronize(done);  // the host copies may now be evicted
+    // RAM-tier entries: held until the copies that read them finish, then
+    // dropped by a later cache call (no wait here); other sources: wait.
+    if (e == cudaSuccess && cache && !held.empty() && cache_release_after(cache, done, held)) {
+      held.clear();
+      done = nullptr;  // the cache owns the event now
+    }
+    if (e == cudaSuccess && done) e = cudaEventSynchronize(done);
     if (done) cudaEventDestroy(done);
     release_all();
     if (e != cudaSuccess) return set_error(ST_E_CUDA, "staging the tensors: %s", cuda_msg(e).c_str());

@@ -197,3 +197,28 @@ def test_lazy_rejects_bad_destinations(stmat, tmp_path):
     with pytest.raises(stmat.StmatError) as e:       # staging too small
         ix.load_tensors(files, [out.data_ptr()], staging[:16], names=[name], dst="BF16")
     assert e.value.status == "ST_E_INVAL" and "staging needs" in str(e.value)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cache_kind", ["one_tensor", "none_kept", "all"])
+def test_back_to_back_loads_keep_entries_until_copied(stmat, oracle, tmp_path, cache_kind):
+    """Loads every tensor without synchronizing in between: a RAM-tier entry
+    stays held until the staging copy that reads it has finished, so a small
+    tier cannot evict (or free) bytes still in flight; the holds are dropped
+    by later cache calls."""
+    torch = gpu()
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    largest = max(e.nbytes for lay in w.files for e in lay.entries)
+    bound = {"one_tensor": largest + largest // 2, "none_kept": 64, "all": 1 << 30}[cache_kind]
+    sd = stmat.StreamStateDict(paths, dst="F16", ram_cache_bytes=bound)
+    oix, arena = oracle_joined(oracle, w, paths)
+    got = {name: sd[name] for name in sd.keys()}          # no synchronization between loads
+    torch.cuda.synchronize()
+    for name, t in got.items():
+        sel = oix.select(names=[name], dst="F16")
+        assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), name
+    st = sd.cache.stats()                                 # finds every copy finished: no holds left
+    assert st["misses"] == len(got)
+    sd.cache.clear()
+    assert sd.cache.stats()["entries"] == 0 and sd.cache.stats()["bytes"] == 0
