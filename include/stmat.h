@@ -450,7 +450,10 @@ st_status st_cache_clear(st_cache_t *cache);
  * ST_E_INVAL with the size needed) and materialized by one launch on
  * `stream`, with the plan's tables in the library's static device array as
  * for st_materialize_noalloc (no device allocation; calls whose work
- * overlaps on the GPU race on that array: order them on one stream).
+ * overlaps on the GPU race on that array: order them on one stream).  The
+ * tables go up in one asynchronous copy from a 4 MiB page-locked host mirror
+ * of that array, allocated by the first call on each device and kept until
+ * the process exits.
  *   dst_host_ptrs  HOST array of one destination (device) pointer per output,
  *                  in the selection's output order; each non-NULL and aligned
  *                  to the output's itemsize (ST_E_INVAL otherwise).
@@ -514,7 +517,9 @@ st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t
  *     fewer workers to shrink it.
  *   - Set-up: the first call on a device, with that device current, looks up
  *     the array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
+ *     before any stream capture.  Under a capture, the table copies read the
+ *     plan's host memory when the graph runs: keep the plan alive while the
+ *     graph can run.
  *   - Sharing: every call, on every stream, uses the same array, and it keeps
  *     the last call's contents; the error word is cleared by each call.  Calls
  *     whose work overlaps on the GPU (different streams, or threads) race on

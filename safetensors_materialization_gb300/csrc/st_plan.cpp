@@ -21,7 +21,9 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <memory>
+#include <mutex>
 #include <new>
 #include <string>
 #include <string_view>
@@ -817,11 +819,24 @@ st_status launch_chunk(const st_plan_t *p, uint32_t k, const void *data_dev, voi
   return launch_materialize(a, p->kernel, stream);
 }
 
+// A page-locked mirror of the static array, one per device, allocated on first
+// use: st_load_tensors packs its tables there and uploads them in one
+// asynchronous copy (a copy from pageable memory first waits for the stream,
+// which would hold each lazy call until the previous call's kernel is done).
+// Reused once the event recorded after its last copy has completed.
+struct TableMirror {
+  uint8_t *host = nullptr;
+  cudaEvent_t done = nullptr;
+};
+std::mutex g_mirror_mu;
+std::map<int, TableMirror> g_mirrors;
+
 // Launches a plan whose tables live in the library's static device array:
 // pieces | warp ranges | block-scale table | destinations (when given on the
-// host) | error word, each 256-byte aligned, filled by stream-ordered copies.
+// host) | error word, each 256-byte aligned, filled by stream-ordered copies
+// (with `mirror`, one copy from the device's page-locked mirror).
 st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *dst_dev, void *const *dst_host,
-                        const float *scales, void *stream) {
+                        const float *scales, void *stream, bool mirror = false) {
   const size_t pieces_bytes = p->pieces.size() * sizeof(Piece);
   const size_t parts_off = (pieces_bytes + 255) & ~size_t(255);
   const size_t parts_bytes = p->parts.size() * sizeof(uint32_t);
@@ -841,12 +856,41 @@ st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *d
   if (s != ST_OK) return s;
   uint8_t *base = static_cast<uint8_t *>(scratch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(base, p->pieces.data(), pieces_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(base + parts_off, p->parts.data(), parts_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess && quant_bytes)
-    e = cudaMemcpyAsync(base + quant_off, p->quant.data(), quant_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess && dst_bytes) e = cudaMemcpyAsync(base + dst_off, dst_host, dst_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(base + err_off, 0, sizeof(uint32_t), st);  // left over from the last call
+  cudaError_t e = cudaSuccess;
+  if (mirror) {
+    std::lock_guard<std::mutex> lock(g_mirror_mu);
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    TableMirror &m = g_mirrors[dev];
+    if (e == cudaSuccess && !m.host) {
+      void *h = nullptr;
+      e = cudaHostAlloc(&h, kStaticScratchBytes, cudaHostAllocDefault);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m.done, cudaEventDisableTiming);
+      if (e == cudaSuccess) {
+        m.host = static_cast<uint8_t *>(h);
+        e = cudaEventRecord(m.done, st);
+      } else if (h) {
+        cudaFreeHost(h);
+      }
+    }
+    if (e == cudaSuccess) e = cudaEventSynchronize(m.done);  // its last copy has left the mirror
+    if (e == cudaSuccess) {
+      std::memcpy(m.host, p->pieces.data(), pieces_bytes);
+      std::memcpy(m.host + parts_off, p->parts.data(), parts_bytes);
+      if (quant_bytes) std::memcpy(m.host + quant_off, p->quant.data(), quant_bytes);
+      if (dst_bytes) std::memcpy(m.host + dst_off, dst_host, dst_bytes);
+      std::memset(m.host + err_off, 0, sizeof(uint32_t));
+      e = cudaMemcpyAsync(base, m.host, need, cudaMemcpyHostToDevice, st);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(m.done, st);
+  } else {
+    e = cudaMemcpyAsync(base, p->pieces.data(), pieces_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(base + parts_off, p->parts.data(), parts_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && quant_bytes)
+      e = cudaMemcpyAsync(base + quant_off, p->quant.data(), quant_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && dst_bytes) e = cudaMemcpyAsync(base + dst_off, dst_host, dst_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + err_off, 0, sizeof(uint32_t), st);  // left over from the last call
+  }
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "filling the static scratch: %s", cuda_msg(e).c_str());
   for (uint32_t k = 0; k < p->n_chunks; ++k) {
     const uint32_t *parts = &p->parts[static_cast<size_t>(k) * (p->workers + 1)];
@@ -1169,7 +1213,7 @@ st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_c
     if (done) cudaEventDestroy(done);
     release_all();
     if (e != cudaSuccess) return set_error(ST_E_CUDA, "staging the tensors: %s", cuda_msg(e).c_str());
-    return launch_static(&plan, staging_dev, nullptr, dst_host_ptrs, nullptr, stream);
+    return launch_static(&plan, staging_dev, nullptr, dst_host_ptrs, nullptr, stream, /*mirror=*/true);
   } catch (const std::bad_alloc &) {
     return set_error(ST_E_NOMEM, "out of host memory");
   }

@@ -96,3 +96,28 @@ def test_noalloc_rejects_a_plan_larger_than_its_scratch(stmat):
         big.materialize_noalloc(data, ptrs)
     assert e.value.status == "ST_E_INVAL"
     assert "static scratch" in str(e.value)
+
+
+def test_noalloc_under_stream_capture(stmat):
+    """Captured into a CUDA graph (after a first call outside the capture, as
+    the header asks) and replayed: the outputs equal st_materialize's.  The
+    captured table copies read the plan's host memory when the graph runs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    buf, data, host_plan, dev_plan = case(stmat, mixed_image(4, 250), "BF16", sms * 3 * 8)
+    outs = stmat.Outputs(host_plan)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        host_plan.materialize_noalloc(data, outs.ptrs, stream=side)
+    torch.cuda.synchronize()
+    ref = stmat.Outputs(dev_plan)
+    dev_plan.materialize(data, ref.ptrs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        host_plan.materialize_noalloc(data, outs.ptrs, stream=torch.cuda.current_stream())
+    for _ in range(2):
+        outs.arena.fill_(0x5A)
+        graph.replay()
+        torch.cuda.synchronize()
+        for i in range(len(ref.infos)):
+            assert torch.equal(outs.raw(i), ref.raw(i)), host_plan.output(i)["name"]
