@@ -898,7 +898,10 @@ __device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta 
   const uint8_t *sp = buf + off;
   uint8_t *dp = dst + static_cast<uint64_t>(a) * SO;
   uint32_t h = static_cast<uint32_t>(((OS - (reinterpret_cast<uintptr_t>(dp) & (OS - 1))) & (OS - 1)) / SO);
-  if (h > n) h = n;
+  // NVFP4 to F32 writes 8-byte units to a destination aligned to 4 only:
+  // whole units then never reach vector alignment, so every unit is written
+  // element by element.
+  if (h > n || (reinterpret_cast<uintptr_t>(dp) & (SO - 1))) h = n;
   const uint32_t nst = (n - h) / KS, t0 = h + nst * KS;
   const uint32_t ends = h + (n - t0);
   for (uint32_t t = lane; t < ends; t += 32) {

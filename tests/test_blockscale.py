@@ -114,9 +114,10 @@ def test_library_errors_match_oracle(stmat, oracle):
     for kw in cases:
         assert lib(**kw) == orc(**kw), kw
     # the register builds refuse block-scaled outputs
-    with pytest.raises(stmat.StmatError) as e:
-        ix.plan(names=["w"], quant=[("block_fp8", "s", None, (128, 128))], workers=8, host_only=True, kernel=1)
-    assert e.value.status == "ST_E_INVAL"
+    for kernel in (1, 2):
+        with pytest.raises(stmat.StmatError) as e:
+            ix.plan(names=["w"], quant=[("block_fp8", "s", None, (128, 128))], workers=8, host_only=True, kernel=kernel)
+        assert e.value.status == "ST_E_INVAL"
 
 
 def test_synthetic_workloads_select_like_the_oracle(stmat, oracle):
@@ -182,7 +183,8 @@ def test_gpu_blockscaled_matches_oracle(stmat, oracle, dst, lead, shift, kernel)
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("fp8", [("F8_E5M2", 64, 48, (16, 16)), ("F8_E4M3", 3, 2000, (1, 16)),
-                                 ("F8_E4M3", 1000, 17, (256, 16)), ("F8_E4M3", 130, 1030, (64, 512))])
+                                 ("F8_E4M3", 1000, 17, (256, 16)), ("F8_E4M3", 130, 1030, (64, 512)),
+                                 ("F8_E4M3", 9, 40000, (1, 16))])
 def test_gpu_block_shapes(stmat, oracle, fp8):
     img, quant = quant_file(20, lead=5, fp8=fp8, nv=(7, 2064))
     for dst in ("BF16", "F32"):
@@ -191,6 +193,37 @@ def test_gpu_block_shapes(stmat, oracle, fp8):
         sel = oix.select(dst=dst, names=names, quant=q)
         data = img[8 + oix.header_len:]
         assert_outputs(plan, outs, [sel.materialize(i, data) for i in range(len(sel))])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_gpu_f32_outputs_at_4_mod_8(stmat, oracle, kernel):
+    """F32 outputs aligned to their itemsize only (4 mod 8): an NVFP4 output's
+    8-byte units then never reach vector alignment, so every unit is written
+    element by element; the bytes equal the oracle's."""
+    torch = _gpu()
+    img, quant = quant_file(60, lead=3)
+    ix = stmat.Index.from_file(img)
+    names, q = selection(ix, quant)
+    plan = ix.plan(dst="F32", names=names, quant=q, kernel=kernel)
+    data = img[8 + ix.sizes()[0]:]
+    dbuf = torch.from_numpy(data.copy()).cuda()
+    infos = plan.outputs()
+    at, offs = 0, []
+    for o in infos:
+        at = (at + 255) // 256 * 256 + 4
+        offs.append(at)
+        at += o["bytes"]
+    arena = torch.full((at + 256,), 0xA5, dtype=torch.uint8, device="cuda")
+    ptrs = torch.tensor([arena.data_ptr() + x for x in offs], dtype=torch.int64, device="cuda")
+    plan.materialize(dbuf, ptrs)
+    torch.cuda.synchronize()
+    assert plan.check() == 0
+    oix = oracle.parse(img)
+    sel = oix.select(dst="F32", names=names, quant=q)
+    host = arena.cpu().numpy()
+    for i, o in enumerate(infos):
+        assert np.array_equal(host[offs[i]:offs[i] + o["bytes"]], sel.materialize(i, data)), o["name"]
 
 
 @pytest.mark.gpu
