@@ -898,9 +898,10 @@ __device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta 
   const uint8_t *sp = buf + off;
   uint8_t *dp = dst + static_cast<uint64_t>(a) * SO;
   uint32_t h = static_cast<uint32_t>(((OS - (reinterpret_cast<uintptr_t>(dp) & (OS - 1))) & (OS - 1)) / SO);
-  // NVFP4 to F32 writes 8-byte units to a destination aligned to 4 only:
-  // whole units then never reach vector alignment, so every unit is written
-  // element by element.
+  // An NVFP4 unit is two elements (4 bytes of BF16/F16, 8 of F32) and a
+  // destination is only aligned to the itemsize: at 2 mod 4 (4 mod 8) whole
+  // units never reach vector alignment, so every unit is written element by
+  // element.
   if (h > n || (reinterpret_cast<uintptr_t>(dp) & (SO - 1))) h = n;
   const uint32_t nst = (n - h) / KS, t0 = h + nst * KS;
   const uint32_t ends = h + (n - t0);

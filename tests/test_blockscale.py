@@ -197,21 +197,23 @@ def test_gpu_block_shapes(stmat, oracle, fp8):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("kernel", [0, 3])
-def test_gpu_f32_outputs_at_4_mod_8(stmat, oracle, kernel):
-    """F32 outputs aligned to their itemsize only (4 mod 8): an NVFP4 output's
-    8-byte units then never reach vector alignment, so every unit is written
-    element by element; the bytes equal the oracle's."""
+@pytest.mark.parametrize("dst", ["F32", "BF16", "F16"])
+def test_gpu_outputs_at_itemsize_alignment(stmat, oracle, kernel, dst):
+    """Outputs aligned to their itemsize only (4 mod 8 for F32, 2 mod 4 for
+    BF16/F16): an NVFP4 output's two-element units then never reach vector
+    alignment, so every unit is written element by element; the bytes equal
+    the oracle's."""
     torch = _gpu()
     img, quant = quant_file(60, lead=3)
     ix = stmat.Index.from_file(img)
     names, q = selection(ix, quant)
-    plan = ix.plan(dst="F32", names=names, quant=q, kernel=kernel)
+    plan = ix.plan(dst=dst, names=names, quant=q, kernel=kernel)
     data = img[8 + ix.sizes()[0]:]
     dbuf = torch.from_numpy(data.copy()).cuda()
     infos = plan.outputs()
     at, offs = 0, []
     for o in infos:
-        at = (at + 255) // 256 * 256 + 4
+        at = (at + 255) // 256 * 256 + (4 if dst == "F32" else 2)
         offs.append(at)
         at += o["bytes"]
     arena = torch.full((at + 256,), 0xA5, dtype=torch.uint8, device="cuda")
@@ -220,7 +222,7 @@ def test_gpu_f32_outputs_at_4_mod_8(stmat, oracle, kernel):
     torch.cuda.synchronize()
     assert plan.check() == 0
     oix = oracle.parse(img)
-    sel = oix.select(dst="F32", names=names, quant=q)
+    sel = oix.select(dst=dst, names=names, quant=q)
     host = arena.cpu().numpy()
     for i, o in enumerate(infos):
         assert np.array_equal(host[offs[i]:offs[i] + o["bytes"]], sel.materialize(i, data)), o["name"]
