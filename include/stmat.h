@@ -429,8 +429,10 @@ void st_cache_free(st_cache_t *cache);
  * pread (`threads` reader threads), evicting least-recently-used entries
  * that nobody holds until it fits the bound.  The entry is held, and *host
  * stays valid, until st_cache_release(cache, *host).  An entry larger than
- * the bound is read but not kept: it is freed on release.  Errors: ST_E_INVAL,
- * ST_E_NOMEM, ST_E_IO. */
+ * the bound is read but not kept: it is freed on release.  Entries belong
+ * to the st_files_t they were read from (each open gets an id of its own):
+ * files opened again, even at the same address, never hit them; entries of
+ * closed files age out.  Errors: ST_E_INVAL, ST_E_NOMEM, ST_E_IO. */
 st_status st_cache_get(st_cache_t *cache, const st_files_t *files, uint64_t begin, uint64_t bytes,
                        uint32_t threads, const void **host);
 st_status st_cache_release(st_cache_t *cache, const void *host);

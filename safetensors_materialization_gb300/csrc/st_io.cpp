@@ -41,6 +41,7 @@ struct st_files_s {
   };
   std::vector<Part> parts;  // sorted by base, non-overlapping
   uint64_t arena_bytes = 0;
+  uint64_t uid = 0;  // unique in the process: RAM-tier entries are keyed by it, not by the address
   ~st_files_s() {
     for (Part &p : parts) {
       if (p.map) munmap(const_cast<uint8_t *>(p.map), p.map_bytes);
@@ -313,8 +314,10 @@ st_status st_index_open(const char *path, st_index_t **out, uint64_t *data_offse
 st_status st_files_open(const st_file_part *parts, size_t n, st_files_t **out) {
   if (!out || (n && !parts)) return set_error(ST_E_INVAL, "NULL argument");
   *out = nullptr;
+  static std::atomic<uint64_t> next_uid{1};
   std::unique_ptr<st_files_s> f(new (std::nothrow) st_files_s);
   if (!f) return set_error(ST_E_NOMEM, "out of host memory");
+  f->uid = next_uid.fetch_add(1);
   try {
     for (size_t k = 0; k < n; ++k) {
       const st_file_part &p = parts[k];
@@ -403,13 +406,13 @@ st_status st_device_reads_pageable(int device, int32_t *yes) {
 
 struct st_cache_s {
   struct Entry {
-    const st_files_s *files;
+    uint64_t files;  // the files' uid
     uint64_t begin, bytes;
     uint8_t *host = nullptr;
     uint32_t holds = 0;
     bool kept = true;  // counted in `bytes` and listed in the LRU order
   };
-  using Key = std::tuple<const st_files_s *, uint64_t, uint64_t>;
+  using Key = std::tuple<uint64_t, uint64_t, uint64_t>;  // (files uid, begin, bytes)
   uint64_t max_bytes = 0, bytes = 0, hits = 0, misses = 0, evictions = 0;
   bool pinned = false;
   std::mutex mu;
@@ -523,7 +526,7 @@ st_status st_cache_get(st_cache_t *c, const st_files_t *files, uint64_t begin, u
   *host = nullptr;
   std::lock_guard<std::mutex> lock(c->mu);
   c->reap(false);
-  const st_cache_s::Key key(files, begin, bytes);
+  const st_cache_s::Key key(files->uid, begin, bytes);
   auto hit = c->by_key.find(key);
   if (hit != c->by_key.end()) {
     ++c->hits;
@@ -534,7 +537,7 @@ st_status st_cache_get(st_cache_t *c, const st_files_t *files, uint64_t begin, u
   }
   ++c->misses;
   st_cache_s::Entry e;
-  e.files = files;
+  e.files = files->uid;
   e.begin = begin;
   e.bytes = bytes;
   e.kept = bytes <= c->max_bytes;

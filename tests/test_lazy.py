@@ -222,3 +222,27 @@ def test_back_to_back_loads_keep_entries_until_copied(stmat, oracle, tmp_path, c
     assert st["misses"] == len(got)
     sd.cache.clear()
     assert sd.cache.stats()["entries"] == 0 and sd.cache.stats()["bytes"] == 0
+
+
+def test_cache_entries_belong_to_their_files_object(stmat, tmp_path):
+    """Entries are keyed by the files object's own id, not its address: a
+    files object opened after another was closed (the allocator often hands
+    out the same address again) never hits the closed one's entries."""
+    import ctypes
+    rng = np.random.Generator(np.random.PCG64(10))
+    paths, datas = [], []
+    for k in range(2):
+        data = rng.integers(0, 256, size=1 << 16, dtype=np.uint8)
+        path = os.path.join(str(tmp_path), f"blob{k}.bin")
+        data.tofile(path)
+        paths.append(path)
+        datas.append(data)
+    c = stmat.Cache(1 << 20, pinned=False)
+    for k in range(8):
+        files = stmat.Files([(paths[k % 2], 0, 1 << 16, 0)])
+        h = c.get(files, 100, 4000)
+        got = np.ctypeslib.as_array((ctypes.c_uint8 * 4000).from_address(h)).copy()
+        c.release(h)
+        assert np.array_equal(got, datas[k % 2][100:4100]), k
+        files.close()
+    assert c.stats()["misses"] == 8 and c.stats()["hits"] == 0
