@@ -185,7 +185,8 @@ struct Populator {
 
 Populator *populate_start(const st_files_s *f, uint64_t begin, uint64_t bytes, uint64_t chunk,
                           uint32_t threads) try {
-  auto *P = new Populator;
+  std::unique_ptr<Populator> own(new Populator);
+  Populator *P = own.get();
   P->files = f;
   const uint64_t C = chunk ? chunk : (bytes ? bytes : 1), end = begin + bytes;
   for (uint64_t c0 = begin; c0 < end; c0 += C) {
@@ -221,7 +222,7 @@ Populator *populate_start(const st_files_s *f, uint64_t begin, uint64_t bytes, u
   } catch (const std::exception &) {
     // Fewer workers (or none): populate_wait then does the missing jobs itself.
   }
-  return P;
+  return own.release();
 } catch (const std::bad_alloc &) {
   return nullptr;
 }
@@ -476,7 +477,8 @@ struct st_cache_s {
       cudaError_t e = wait ? cudaEventSynchronize(p.ev) : cudaEventQuery(p.ev);
       if (e == cudaErrorNotReady) {
         (void)cudaGetLastError();  // not-ready is recorded as the last error: clear it
-        pending[kept++] = std::move(p);
+        if (kept != i) pending[kept] = std::move(p);  // never onto itself: that would empty `hosts`
+        ++kept;
         continue;
       }
       // Done, or the context failed (then no copy reads the entries any more).

@@ -857,23 +857,32 @@ st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *d
   uint8_t *base = static_cast<uint8_t *>(scratch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (mirror) {
-    std::lock_guard<std::mutex> lock(g_mirror_mu);
+  std::unique_lock<std::mutex> lock(g_mirror_mu, std::defer_lock);
+  TableMirror *mp = nullptr;
+  if (mirror) {  // the page-locked mirror, or (if it cannot be had) the pageable copies below
+    lock.lock();
     int dev = 0;
     e = cudaGetDevice(&dev);
     TableMirror &m = g_mirrors[dev];
     if (e == cudaSuccess && !m.host) {
       void *h = nullptr;
-      e = cudaHostAlloc(&h, kStaticScratchBytes, cudaHostAllocDefault);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m.done, cudaEventDisableTiming);
-      if (e == cudaSuccess) {
+      cudaEvent_t ev = nullptr;
+      if (cudaHostAlloc(&h, kStaticScratchBytes, cudaHostAllocDefault) == cudaSuccess &&
+          cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) == cudaSuccess &&
+          cudaEventRecord(ev, st) == cudaSuccess) {
         m.host = static_cast<uint8_t *>(h);
-        e = cudaEventRecord(m.done, st);
-      } else if (h) {
-        cudaFreeHost(h);
+        m.done = ev;
+      } else {
+        if (ev) cudaEventDestroy(ev);
+        if (h) cudaFreeHost(h);
+        (void)cudaGetLastError();  // not sticky: fall back to pageable copies
       }
     }
-    if (e == cudaSuccess) e = cudaEventSynchronize(m.done);  // its last copy has left the mirror
+    if (e == cudaSuccess && m.host) mp = &m;
+  }
+  if (mp) {
+    TableMirror &m = *mp;
+    e = cudaEventSynchronize(m.done);  // its last copy has left the mirror
     if (e == cudaSuccess) {
       std::memcpy(m.host, p->pieces.data(), pieces_bytes);
       std::memcpy(m.host + parts_off, p->parts.data(), parts_bytes);
@@ -883,7 +892,7 @@ st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *d
       e = cudaMemcpyAsync(base, m.host, need, cudaMemcpyHostToDevice, st);
     }
     if (e == cudaSuccess) e = cudaEventRecord(m.done, st);
-  } else {
+  } else if (e == cudaSuccess) {
     e = cudaMemcpyAsync(base, p->pieces.data(), pieces_bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(base + parts_off, p->parts.data(), parts_bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess && quant_bytes)

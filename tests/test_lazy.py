@@ -246,3 +246,30 @@ def test_cache_entries_belong_to_their_files_object(stmat, tmp_path):
         assert np.array_equal(got, datas[k % 2][100:4100]), k
         files.close()
     assert c.stats()["misses"] == 8 and c.stats()["hits"] == 0
+
+
+@pytest.mark.gpu
+def test_holds_released_when_copies_finish_late(stmat, oracle, tmp_path):
+    """RAM-tier hits queued behind a long kernel: the next call finds the
+    previous call's copies still in flight (their holds must be kept, not
+    lost) and the holds are dropped once the copies are done, so clear() then
+    empties the tier."""
+    torch = gpu()
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    sd = stmat.StreamStateDict(paths, dst="BF16", ram_cache_bytes=1 << 30)
+    oix, arena = oracle_joined(oracle, w, paths)
+    names = sd.keys()[:6]
+    for n in names:                            # misses: each allocates its page-locked entry
+        sd[n]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)             # about 0.1 s of a bounded spin on the current stream
+    got = [sd[n] for n in names]              # hits (nothing allocated): their copies queue behind it
+    torch.cuda.synchronize()
+    st = sd.cache.stats()
+    assert st["misses"] == len(names) and st["hits"] == len(names) and st["entries"] == len(names)
+    sd.cache.clear()
+    assert sd.cache.stats()["entries"] == 0 and sd.cache.stats()["bytes"] == 0
+    for n, t in zip(names, got):
+        sel = oix.select(names=[n], dst="BF16")
+        assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), n
