@@ -453,9 +453,9 @@ st_status st_cache_clear(st_cache_t *cache);
  * `stream`, with the plan's tables in the library's static device array as
  * for st_materialize_noalloc (no device allocation; calls whose work
  * overlaps on the GPU race on that array: order them on one stream).  The
- * tables go up in one asynchronous copy from a 4 MiB page-locked host mirror
- * of that array, allocated by the first call on each device and kept until
- * the process exits.
+ * tables go up in one asynchronous copy from a page-locked host mirror of
+ * that array (two 4 MiB halves used in turn), allocated by the first call on
+ * each device and kept until the process exits.
  *   dst_host_ptrs  HOST array of one destination (device) pointer per output,
  *                  in the selection's output order; each non-NULL and aligned
  *                  to the output's itemsize (ST_E_INVAL otherwise).

@@ -823,10 +823,14 @@ st_status launch_chunk(const st_plan_t *p, uint32_t k, const void *data_dev, voi
 // use: st_load_tensors packs its tables there and uploads them in one
 // asynchronous copy (a copy from pageable memory first waits for the stream,
 // which would hold each lazy call until the previous call's kernel is done).
-// Reused once the event recorded after its last copy has completed.
+// Two halves used in turn, each reused once the event recorded after its
+// last copy has completed: a call then waits for the call before the
+// previous one, not for the previous one's staging copy.  (The device array
+// itself is single: its reuse is ordered by the stream.)
 struct TableMirror {
-  uint8_t *host = nullptr;
-  cudaEvent_t done = nullptr;
+  uint8_t *host[2] = {nullptr, nullptr};
+  cudaEvent_t done[2] = {nullptr, nullptr};
+  uint32_t next = 0;
 };
 std::mutex g_mirror_mu;
 std::map<int, TableMirror> g_mirrors;
@@ -864,34 +868,41 @@ st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *d
     int dev = 0;
     e = cudaGetDevice(&dev);
     TableMirror &m = g_mirrors[dev];
-    if (e == cudaSuccess && !m.host) {
+    if (e == cudaSuccess && !m.host[0]) {
       void *h = nullptr;
-      cudaEvent_t ev = nullptr;
-      if (cudaHostAlloc(&h, kStaticScratchBytes, cudaHostAllocDefault) == cudaSuccess &&
-          cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) == cudaSuccess &&
-          cudaEventRecord(ev, st) == cudaSuccess) {
-        m.host = static_cast<uint8_t *>(h);
-        m.done = ev;
+      cudaEvent_t ev[2] = {nullptr, nullptr};
+      if (cudaHostAlloc(&h, 2 * kStaticScratchBytes, cudaHostAllocDefault) == cudaSuccess &&
+          cudaEventCreateWithFlags(&ev[0], cudaEventDisableTiming) == cudaSuccess &&
+          cudaEventCreateWithFlags(&ev[1], cudaEventDisableTiming) == cudaSuccess &&
+          cudaEventRecord(ev[0], st) == cudaSuccess && cudaEventRecord(ev[1], st) == cudaSuccess) {
+        for (int k = 0; k < 2; ++k) {
+          m.host[k] = static_cast<uint8_t *>(h) + k * kStaticScratchBytes;
+          m.done[k] = ev[k];
+        }
       } else {
-        if (ev) cudaEventDestroy(ev);
+        for (cudaEvent_t x : ev)
+          if (x) cudaEventDestroy(x);
         if (h) cudaFreeHost(h);
         (void)cudaGetLastError();  // not sticky: fall back to pageable copies
       }
     }
-    if (e == cudaSuccess && m.host) mp = &m;
+    if (e == cudaSuccess && m.host[0]) mp = &m;
   }
   if (mp) {
     TableMirror &m = *mp;
-    e = cudaEventSynchronize(m.done);  // its last copy has left the mirror
+    const uint32_t k = m.next;
+    m.next ^= 1u;
+    uint8_t *h = m.host[k];
+    e = cudaEventSynchronize(m.done[k]);  // this half's last copy has left it
     if (e == cudaSuccess) {
-      std::memcpy(m.host, p->pieces.data(), pieces_bytes);
-      std::memcpy(m.host + parts_off, p->parts.data(), parts_bytes);
-      if (quant_bytes) std::memcpy(m.host + quant_off, p->quant.data(), quant_bytes);
-      if (dst_bytes) std::memcpy(m.host + dst_off, dst_host, dst_bytes);
-      std::memset(m.host + err_off, 0, sizeof(uint32_t));
-      e = cudaMemcpyAsync(base, m.host, need, cudaMemcpyHostToDevice, st);
+      std::memcpy(h, p->pieces.data(), pieces_bytes);
+      std::memcpy(h + parts_off, p->parts.data(), parts_bytes);
+      if (quant_bytes) std::memcpy(h + quant_off, p->quant.data(), quant_bytes);
+      if (dst_bytes) std::memcpy(h + dst_off, dst_host, dst_bytes);
+      std::memset(h + err_off, 0, sizeof(uint32_t));
+      e = cudaMemcpyAsync(base, h, need, cudaMemcpyHostToDevice, st);
     }
-    if (e == cudaSuccess) e = cudaEventRecord(m.done, st);
+    if (e == cudaSuccess) e = cudaEventRecord(m.done[k], st);
   } else if (e == cudaSuccess) {
     e = cudaMemcpyAsync(base, p->pieces.data(), pieces_bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(base + parts_off, p->parts.data(), parts_bytes, cudaMemcpyHostToDevice, st);
