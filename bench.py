@@ -48,7 +48,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-files", choices=["auto", "on", "off"], default="auto",
                     help="also time st_load_files from shard files written to a temp dir (auto: below 8 GB)")
-    ap.add_argument("--io-threads", type=int, default=8)
+    ap.add_argument("--io-threads", type=int, default=16)
     ap.add_argument("--lazy", choices=["auto", "on", "off"], default="auto",
                     help="also time the lazy one-tensor-at-a-time path (auto: up to 2000 tensors, below 8 GB)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -20,6 +20,8 @@
 #include <atomic>
 #include <cerrno>
 #include <condition_variable>
+#include <deque>
+#include <functional>
 #include <mutex>
 #include <cstdlib>
 #include <cstring>
@@ -30,6 +32,85 @@
 #include <vector>
 
 #include "st_internal.h"
+
+// Reader threads kept for the lifetime of a files object (started on first
+// use, at most kMaxReaders): a range read hands each thread one span and
+// waits for all of them.  Starting threads for every read cost a third of
+// the page-cache read rate.
+struct ReaderPool {
+  static constexpr uint32_t kMaxReaders = 32;
+  std::mutex m;
+  std::condition_variable cv;
+  std::deque<std::function<void()>> jobs;
+  std::vector<std::thread> threads;
+  bool stop = false;
+  // Grows to n threads (fewer if threads cannot be started).
+  void ensure(uint32_t n) {
+    std::lock_guard<std::mutex> g(m);
+    n = std::min(n, kMaxReaders);
+    try {
+      while (threads.size() < n)
+        threads.emplace_back([this] {
+          for (;;) {
+            std::function<void()> job;
+            {
+              std::unique_lock<std::mutex> lk(m);
+              cv.wait(lk, [this] { return stop || !jobs.empty(); });
+              if (jobs.empty()) return;  // stop, nothing left
+              job = std::move(jobs.front());
+              jobs.pop_front();
+            }
+            job();
+          }
+        });
+    } catch (const std::exception &) {
+    }
+  }
+  // Runs every job of the batch (on the pool, or here when it has no
+  // threads) and returns when all are done.
+  void run(std::vector<std::function<void()>> &batch) {
+    bool pooled;
+    {
+      std::lock_guard<std::mutex> g(m);
+      pooled = !threads.empty();
+    }
+    if (!pooled) {
+      for (auto &job : batch) job();
+      return;
+    }
+    std::mutex dm;
+    std::condition_variable dcv;
+    size_t left = batch.size(), queued = 0;
+    {
+      std::lock_guard<std::mutex> g(m);
+      try {
+        for (auto &job : batch) {
+          jobs.emplace_back([&dm, &dcv, &left, job] {
+            job();
+            std::lock_guard<std::mutex> dg(dm);  // notify under the lock: the waiter
+            if (--left == 0) dcv.notify_all();   // cannot return (and drop dm/dcv) before
+          });
+          ++queued;
+        }
+      } catch (const std::bad_alloc &) {
+        // the jobs not queued run here, below
+      }
+    }
+    cv.notify_all();
+    for (size_t i = queued; i < batch.size(); ++i) batch[i]();
+    std::unique_lock<std::mutex> lk(dm);
+    left -= batch.size() - queued;
+    dcv.wait(lk, [&] { return left == 0; });
+  }
+  ~ReaderPool() {
+    {
+      std::lock_guard<std::mutex> g(m);
+      stop = true;
+    }
+    cv.notify_all();
+    for (auto &t : threads) t.join();
+  }
+};
 
 struct st_files_s {
   struct Part {
@@ -42,6 +123,7 @@ struct st_files_s {
   std::vector<Part> parts;  // sorted by base, non-overlapping
   uint64_t arena_bytes = 0;
   uint64_t uid = 0;  // unique in the process: RAM-tier entries are keyed by it, not by the address
+  mutable ReaderPool readers;
   ~st_files_s() {
     for (Part &p : parts) {
       if (p.map) munmap(const_cast<uint8_t *>(p.map), p.map_bytes);
@@ -110,20 +192,20 @@ st_status read_arena(const st_files_s *f, uint64_t begin, uint64_t bytes, void *
   }
   std::vector<std::string> msgs(t);
   std::atomic<bool> ok{true};
-  std::vector<std::thread> pool;
   try {
+    std::vector<std::function<void()>> batch;
     for (uint32_t i = 0; i < t; ++i) {
       const uint64_t lo = begin + std::min(bytes, blocks * i / t * kBlock);
       const uint64_t hi = begin + std::min(bytes, blocks * (i + 1) / t * kBlock);
-      pool.emplace_back([&, i, lo, hi] {
+      batch.emplace_back([&, i, lo, hi] {
         if (!read_span(*f, begin, lo, hi, dst, &msgs[i])) ok = false;
       });
     }
-  } catch (const std::exception &) {
-    for (auto &th : pool) th.join();
-    return set_error(ST_E_NOMEM, "starting %u reader threads", t);
+    f->readers.ensure(t);
+    f->readers.run(batch);
+  } catch (const std::bad_alloc &) {
+    return set_error(ST_E_NOMEM, "queueing %u reads", t);
   }
-  for (auto &th : pool) th.join();
   if (!ok) {
     for (const auto &m : msgs)
       if (!m.empty()) return set_error(ST_E_IO, "%s", m.c_str());

@@ -346,7 +346,7 @@ class Index:
         _check(lib().st_index_concat(hs, n, align, bases, C.byref(out)))
         return cls(out.value), [int(b) for b in bases[:n]]
 
-    def load_tensors(self, files, dst_ptrs, staging, names, dst="BF16", cache=None, threads=8, stream=None,
+    def load_tensors(self, files, dst_ptrs, staging, names, dst="BF16", cache=None, threads=16, stream=None,
                      scale_names=None, scale_suffix=None, quant=None):
         """st_load_tensors: the lazy path for a few named tensors (read through
         `cache`, staged in `staging`, one launch on `stream`); dst_ptrs: one
@@ -469,7 +469,7 @@ class StreamStateDict:
     scale_suffix / quant: as for Index.plan (quant: name -> (kind, scales,
     global scale, block))."""
 
-    def __init__(self, paths, dst="BF16", device="cuda", ram_cache_bytes=1 << 30, pinned=True, threads=8,
+    def __init__(self, paths, dst="BF16", device="cuda", ram_cache_bytes=1 << 30, pinned=True, threads=16,
                  rename=None, prefix=None, scale_suffix=None, quant=None, align=256):
         self.files, root = Files.of_checkpoint(list(paths), align)
         view = root

@@ -68,6 +68,37 @@ def test_files_read_the_joined_arena(stmat, tmp_path, threads):
         assert np.array_equal(part, ref)
 
 
+def test_concurrent_reads_share_the_reader_pool(stmat, tmp_path):
+    """Several host threads read different ranges of one files object at
+    once (each read split over the object's reader threads); every read gets
+    its own bytes."""
+    import threading
+    rng = np.random.Generator(np.random.PCG64(3))
+    data = rng.integers(0, 256, size=24 << 20, dtype=np.uint8)
+    path = os.path.join(str(tmp_path), "big.bin")
+    data.tofile(path)
+    files = stmat.Files([(path, 0, data.size, 0)])
+    errors = []
+
+    def worker(seed):
+        r = np.random.Generator(np.random.PCG64(seed))
+        for _ in range(12):
+            begin = int(r.integers(0, data.size - 1))
+            n = int(r.integers(1, min(data.size - begin, 5 << 20) + 1))
+            got = np.empty(n, np.uint8)
+            files.read(begin, n, got, threads=int(r.integers(1, 9)))
+            if not np.array_equal(got, data[begin:begin + n]):
+                errors.append((seed, begin, n))
+
+    ts = [threading.Thread(target=worker, args=(s,)) for s in range(6)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors
+    files.close()
+
+
 def test_file_errors(stmat, tmp_path):
     w = small_llm()
     paths, datas = write_shards(str(tmp_path), w)
