@@ -339,8 +339,9 @@ def time_lazy(args, w, host, data_start, stmat, torch):
     """The lazy path: every output loaded alone through StreamStateDict
     (st_load_tensors) from the workload's files in the page cache; a cold
     pass (every tensor read into the RAM tier), a warm pass (every tensor a
-    RAM-tier hit) and a pass without a RAM tier (each tensor copied straight
-    from the files' mappings).  Reports tensors/s and dst GB/s per pass."""
+    RAM-tier hit), a pass without a RAM tier (each tensor copied straight
+    from the files' mappings) and a warm pass in batches (StreamStateDict.
+    load_many).  Reports tensors/s and dst GB/s per pass."""
     import shutil
     import tempfile
     tmp = tempfile.mkdtemp(prefix="stmat_lazy_")
@@ -370,6 +371,16 @@ def time_lazy(args, w, host, data_start, stmat, torch):
             dt = time.perf_counter() - t0
             res[label] = {"tensors_per_s": round(len(names) / dt, 1), "gbs_dst": round(nbytes / dt / 1e9, 3),
                           "ms": round(dt * 1e3, 1)}
+        # the same tensors in batches (one copy and one launch per batch), RAM tier warm
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        got = sd.load_many(names)
+        nbytes = sum(t.numel() * t.element_size() for t in got.values())
+        del got
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        res["warm_batched"] = {"tensors_per_s": round(len(names) / dt, 1), "gbs_dst": round(nbytes / dt / 1e9, 3),
+                               "ms": round(dt * 1e3, 1)}
         st = sd.cache.stats()
         res.update({"tensors": len(names), "ram_tier": {"hits": st["hits"], "misses": st["misses"],
                                                          "bytes": st["bytes"]},

@@ -539,6 +539,51 @@ class StreamStateDict:
                                 threads=self.threads, stream=torch.cuda.current_stream(), **self._sel(name))
         return out
 
+    def load_many(self, names, max_batch_bytes=256 << 20, max_batch=1024, alone_bytes=32 << 20):
+        """Several tensors at once: one st_load_tensors (one staging copy, one
+        launch) per batch of at most max_batch tensors or max_batch_bytes of
+        staged bytes; a tensor of alone_bytes or more is loaded on its own
+        (large tensors already fill the host link one at a time, and batching
+        them only loses the overlap).  Returns {name: tensor}."""
+        import torch
+        out, batch, staged = {}, [], 0
+
+        def flush():
+            if not batch:
+                return
+            quant = [self.quant.get(n) for n in batch]
+            kw = dict(names=list(batch), scale_suffix=self.scale_suffix, quant=quant if any(quant) else None)
+            # A name that another name of the batch consumes (its scale) is no
+            # output of the batch: then the destinations would not line up.
+            got = [o["name"] for o in self.index.plan(dst=self.dst, workers=1, host_only=True, **kw).outputs()]
+            if got != batch:
+                for n in batch:
+                    out[n] = self[n]
+                return
+            need = sum(self._lookup(n)[2] for n in batch)
+            if self._staging is None or self._staging.numel() < need:
+                self._staging = torch.empty(need, dtype=torch.uint8, device=self.device)
+            ts = [torch.empty(self._lookup(n)[0], dtype=torch_dtype(self._lookup(n)[1]), device=self.device)
+                  for n in batch]
+            self.index.load_tensors(self.files, [t.data_ptr() for t in ts], self._staging, dst=self.dst,
+                                    cache=self.cache, threads=self.threads, stream=torch.cuda.current_stream(), **kw)
+            out.update(zip(batch, ts))
+
+        for n in names:
+            if n not in self._pos:
+                raise KeyError(n)
+            need = self._lookup(n)[2]
+            if need >= alone_bytes:
+                out[n] = self[n]
+                continue
+            if batch and (len(batch) >= max_batch or staged + need > max_batch_bytes):
+                flush()
+                batch, staged = [], 0
+            batch.append(n)
+            staged += need
+        flush()
+        return {n: out[n] for n in names}
+
     def items(self):
         for n in self._names:
             yield n, self[n]

@@ -273,3 +273,53 @@ def test_holds_released_when_copies_finish_late(stmat, oracle, tmp_path):
     for n, t in zip(names, got):
         sel = oix.select(names=[n], dst="BF16")
         assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), n
+
+
+def test_load_many_batches_check_their_outputs(stmat, tmp_path):
+    """A batch whose names include a scale that another name of the batch
+    consumes has fewer outputs than names: load_many sees it (host-only plan)
+    and loads those names one by one (here: the fallback is taken without a
+    GPU, so only the check itself runs)."""
+    w = synth.scaled_fp8(blocks=1)
+    lay = w.files[0]
+    path = os.path.join(str(tmp_path), "s.safetensors")
+    synth.build_workload_file(w, 0).tofile(path)
+    sd = stmat.StreamStateDict([path], dst="BF16", scale_suffix=w.scale_suffix, pinned=False)
+    weight = [e.name for e in lay.entries if e.name.endswith(".weight")][0]
+    scale = weight[: -len(w.scale_suffix[0])] + w.scale_suffix[1]
+    outs = sd.index.plan(dst="BF16", names=[weight, scale], workers=1, host_only=True,
+                         scale_suffix=w.scale_suffix).outputs()
+    assert [o["name"] for o in outs] == [weight]          # the scale is consumed: one output for two names
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cache_bytes", [0, 1 << 30])
+def test_load_many_matches_oracle(stmat, oracle, tmp_path, cache_bytes):
+    """load_many over every tensor (batches split by count and bytes) equals
+    the oracle; with a scale suffix, a batch holding a weight and its scale
+    falls back to one name at a time."""
+    torch = gpu()
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    sd = stmat.StreamStateDict(paths, dst="F16", ram_cache_bytes=cache_bytes)
+    oix, arena = oracle_joined(oracle, w, paths)
+    for kw in (dict(), dict(max_batch=5), dict(max_batch_bytes=1 << 16)):
+        got = sd.load_many(sd.keys(), **kw)
+        torch.cuda.synchronize()
+        assert list(got) == sd.keys()
+        for name, t in got.items():
+            sel = oix.select(names=[name], dst="F16")
+            assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), name
+    s = synth.scaled_fp8(blocks=1)
+    spath = os.path.join(str(tmp_path), "s.safetensors")
+    simg = synth.build_workload_file(s, 0)
+    simg.tofile(spath)
+    sds = stmat.StreamStateDict([spath], dst="BF16", scale_suffix=s.scale_suffix)
+    soix = oracle.parse(simg)
+    names = sds.keys()[:6]                                 # weights and their scales together
+    got = sds.load_many(names)
+    torch.cuda.synchronize()
+    for name in names:
+        sel = soix.select(names=[name], dst="BF16", scale_suffix=s.scale_suffix)
+        want = sel.materialize(0, simg[s.files[0].data_start:])
+        assert np.array_equal(got[name].reshape(-1).view(torch.uint8).cpu().numpy(), want), name
