@@ -275,21 +275,33 @@ def test_holds_released_when_copies_finish_late(stmat, oracle, tmp_path):
         assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), n
 
 
+def scaled_fp8_file(tmp_path):
+    """Two E4M3 weights with their one-element F32 scales and an F16 tensor."""
+    import test_blockscale as TB
+    rng = np.random.Generator(np.random.PCG64(12))
+    ents = []
+    for k in range(2):
+        ents.append((f"l{k}.weight", "F8_E4M3", [24, 40], rng.integers(0, 0x7F, size=960, dtype=np.uint8).tobytes()))
+        ents.append((f"l{k}.scale_weight", "F32", [], np.float32(rng.uniform(1e-3, 1e-1)).tobytes()))
+    ents.append(("norm", "F16", [40], rng.standard_normal(40).astype(np.float16).tobytes()))
+    img = TB.image(ents, lead=3)
+    path = os.path.join(str(tmp_path), "s.safetensors")
+    img.tofile(path)
+    return path, img, (".weight", ".scale_weight")
+
+
 def test_load_many_batches_check_their_outputs(stmat, tmp_path):
     """A batch whose names include a scale that another name of the batch
-    consumes has fewer outputs than names: load_many sees it (host-only plan)
-    and loads those names one by one (here: the fallback is taken without a
-    GPU, so only the check itself runs)."""
-    w = synth.scaled_fp8(blocks=1)
-    lay = w.files[0]
-    path = os.path.join(str(tmp_path), "s.safetensors")
-    synth.build_workload_file(w, 0).tofile(path)
-    sd = stmat.StreamStateDict([path], dst="BF16", scale_suffix=w.scale_suffix, pinned=False)
-    weight = [e.name for e in lay.entries if e.name.endswith(".weight")][0]
-    scale = weight[: -len(w.scale_suffix[0])] + w.scale_suffix[1]
-    outs = sd.index.plan(dst="BF16", names=[weight, scale], workers=1, host_only=True,
-                         scale_suffix=w.scale_suffix).outputs()
-    assert [o["name"] for o in outs] == [weight]          # the scale is consumed: one output for two names
+    consumes has fewer outputs than names: the host-only plan load_many
+    checks each batch with shows it (the batch is then loaded name by name)."""
+    path, img, suffix = scaled_fp8_file(tmp_path)
+    sd = stmat.StreamStateDict([path], dst="BF16", scale_suffix=suffix, pinned=False)
+    outs = sd.index.plan(dst="BF16", names=["l0.weight", "l0.scale_weight"], workers=1, host_only=True,
+                         scale_suffix=suffix).outputs()
+    assert [o["name"] for o in outs] == ["l0.weight"]       # the scale is consumed: one output for two names
+    outs = sd.index.plan(dst="BF16", names=["l0.weight", "norm"], workers=1, host_only=True,
+                         scale_suffix=suffix).outputs()
+    assert [o["name"] for o in outs] == ["l0.weight", "norm"]
 
 
 @pytest.mark.gpu
@@ -310,16 +322,13 @@ def test_load_many_matches_oracle(stmat, oracle, tmp_path, cache_bytes):
         for name, t in got.items():
             sel = oix.select(names=[name], dst="F16")
             assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), name
-    s = synth.scaled_fp8(blocks=1)
-    spath = os.path.join(str(tmp_path), "s.safetensors")
-    simg = synth.build_workload_file(s, 0)
-    simg.tofile(spath)
-    sds = stmat.StreamStateDict([spath], dst="BF16", scale_suffix=s.scale_suffix)
+    spath, simg, suffix = scaled_fp8_file(tmp_path)
+    sds = stmat.StreamStateDict([spath], dst="BF16", scale_suffix=suffix)
     soix = oracle.parse(simg)
-    names = sds.keys()[:6]                                 # weights and their scales together
+    names = sds.keys()                                     # weights and their scales together
     got = sds.load_many(names)
     torch.cuda.synchronize()
+    data = simg[8 + soix.header_len:]
     for name in names:
-        sel = soix.select(names=[name], dst="BF16", scale_suffix=s.scale_suffix)
-        want = sel.materialize(0, simg[s.files[0].data_start:])
-        assert np.array_equal(got[name].reshape(-1).view(torch.uint8).cpu().numpy(), want), name
+        sel = soix.select(names=[name], dst="BF16", scale_suffix=suffix)
+        assert np.array_equal(got[name].reshape(-1).view(torch.uint8).cpu().numpy(), sel.materialize(0, data)), name
