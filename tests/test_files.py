@@ -241,6 +241,33 @@ def test_load_files_ringless_block_scaled_and_errors(stmat, oracle, tmp_path):
 
 
 @pytest.mark.gpu
+def test_load_files_empty_data_sections(stmat, tmp_path):
+    """Checkpoints whose data sections are empty (a header alone; zero-size
+    tensors): both load modes queue nothing and succeed."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import json
+    import struct
+    for k, ents in enumerate(({}, {"z": {"dtype": "F16", "shape": [0, 4], "data_offsets": [0, 0]}})):
+        h = json.dumps(ents).encode()
+        path = os.path.join(str(tmp_path), f"e{k}.safetensors")
+        with open(path, "wb") as f:
+            f.write(struct.pack("<Q", len(h)) + h)
+        files, ix = stmat.Files.of_checkpoint([path])
+        assert ix.sizes()[1] == 0
+        plan = ix.plan(dst="BF16", chunk_bytes=1 << 20)
+        outs = stmat.Outputs(plan)
+        dev = torch.empty(16, dtype=torch.uint8, device="cuda")
+        ring = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
+        plan.load_files(files, dev, outs.ptrs)
+        plan.load_files(files, dev, outs.ptrs, ring)
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        files.close()
+
+
+@pytest.mark.gpu
 def test_host_affinity_binds_to_the_gpu_socket(stmat):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
