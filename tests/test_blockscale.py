@@ -317,3 +317,41 @@ def test_gpu_special_scales(stmat, oracle, dst):
             sel = oix.select(dst=dst, names=names, quant=q)
             data = img[8 + oix.header_len:]
             assert_outputs(plan, outs, [sel.materialize(i, data) for i in range(len(sel))])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("chunk", [4096, 5000, 1 << 16])
+def test_gpu_chunked_loads_wait_for_block_scales(stmat, oracle, tmp_path, chunk):
+    """Block-scaled weights through the chunked pipelines, st_load from pinned
+    memory and st_load_files through a pinned ring: a chunk's pieces run only
+    once the chunk holding their block scales has landed; the bytes equal
+    the oracle's."""
+    import os
+    torch = _gpu()
+    img, quant = quant_file(77, lead=9)
+    path = os.path.join(str(tmp_path), "q.safetensors")
+    img.tofile(path)
+    oix = oracle.parse(img)
+    data = img[8 + oix.header_len:]
+    files, ix = stmat.Files.of_checkpoint([path])
+    names, q = selection(ix, quant)
+    sel = oix.select(dst="BF16", names=names, quant=q)
+    want = [sel.materialize(i, data) for i in range(len(sel))]
+    for mode in ("pinned", "ring"):
+        plan = ix.plan(dst="BF16", names=names, quant=q, chunk_bytes=chunk)
+        assert plan.stats()["chunks"] > 1
+        dev = torch.full((data.size,), 0xA5, dtype=torch.uint8, device="cuda")
+        outs = stmat.Outputs(plan)
+        outs.arena.fill_(0x5A)
+        copy = torch.cuda.Stream()
+        if mode == "pinned":
+            host = torch.from_numpy(data.copy()).pin_memory()
+            plan.load(host, dev, outs.ptrs, copy_stream=copy, compute_stream=torch.cuda.current_stream())
+        else:
+            ring = torch.empty(3 * chunk, dtype=torch.uint8).pin_memory()
+            plan.load_files(files, dev, outs.ptrs, ring, threads=3, copy_stream=copy,
+                            compute_stream=torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        assert_outputs(plan, outs, want)
+    files.close()
