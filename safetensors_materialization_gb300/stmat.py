@@ -347,11 +347,11 @@ class Index:
         return cls(out.value), [int(b) for b in bases[:n]]
 
     def load_tensors(self, files, dst_ptrs, staging, names, dst="BF16", cache=None, threads=16, stream=None,
-                     scale_names=None, scale_suffix=None, quant=None):
+                     scale_names=None, scale_suffix=None, quant=None, slices=None):
         """st_load_tensors: the lazy path for a few named tensors (read through
         `cache`, staged in `staging`, one launch on `stream`); dst_ptrs: one
-        device address per output, in output order."""
-        sel, keep = _selection(names, scale_names, scale_suffix, 0, 0, None, quant)
+        device address per output, in output order; slices as for plan()."""
+        sel, keep = _selection(names, scale_names, scale_suffix, 0, 0, slices, quant)
         ptrs = (C.c_void_p * max(1, len(dst_ptrs)))(*dst_ptrs)
         nbytes = staging.numel() if hasattr(staging, "numel") else len(staging)
         _check(lib().st_load_tensors(self._h, files.handle, cache.handle if cache else None, C.byref(sel),
@@ -537,6 +537,25 @@ class StreamStateDict:
             self._staging = torch.empty(need, dtype=torch.uint8, device=self.device)
         self.index.load_tensors(self.files, [out.data_ptr()], self._staging, dst=self.dst, cache=self.cache,
                                 threads=self.threads, stream=torch.cuda.current_stream(), **self._sel(name))
+        return out
+
+    def slice(self, name, dim, start, stop):
+        """sd[name][..., start:stop, ...] along `dim`, read and cast on access
+        (a tensor-parallel rank's rows or columns): one st_load_tensors with a
+        slice, the gather done by the kernel."""
+        import torch
+        if name not in self._pos:
+            raise KeyError(name)
+        q = self.quant.get(name)
+        kw = dict(names=[name], scale_suffix=self.scale_suffix, quant=[q] if q else None,
+                  slices=[(dim, start, stop)])
+        o = self.index.plan(dst=self.dst, workers=1, host_only=True, **kw).outputs()[0]
+        out = torch.empty(o["shape"], dtype=torch_dtype(o["dtype"]), device=self.device)
+        need = self._lookup(name)[2]
+        if self._staging is None or self._staging.numel() < need:
+            self._staging = torch.empty(need, dtype=torch.uint8, device=self.device)
+        self.index.load_tensors(self.files, [out.data_ptr()], self._staging, dst=self.dst, cache=self.cache,
+                                threads=self.threads, stream=torch.cuda.current_stream(), **kw)
         return out
 
     def load_many(self, names, max_batch_bytes=256 << 20, max_batch=1024, alone_bytes=32 << 20):

@@ -332,3 +332,33 @@ def test_load_many_matches_oracle(stmat, oracle, tmp_path, cache_bytes):
     for name in names:
         sel = soix.select(names=[name], dst="BF16", scale_suffix=suffix)
         assert np.array_equal(got[name].reshape(-1).view(torch.uint8).cpu().numpy(), sel.materialize(0, data)), name
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cache_bytes", [0, 1 << 30])
+def test_lazy_slices_match_oracle(stmat, oracle, tmp_path, cache_bytes):
+    """sd.slice(name, dim, start, stop): one tensor-parallel rank's rows or
+    columns read and gathered on access, on every 2-D tensor of a sharded
+    checkpoint along both dimensions, against the oracle's sliced outputs."""
+    torch = gpu()
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    sd = stmat.StreamStateDict(paths, dst="BF16", ram_cache_bytes=cache_bytes)
+    oix, arena = oracle_joined(oracle, w, paths)
+    checked = 0
+    for name in sd.keys():
+        shape, _ = sd.info(name)
+        if len(shape) != 2:
+            continue
+        for dim in (0, 1):
+            n = shape[dim]
+            start, stop = n // 4, n // 4 + max(1, n // 3)
+            t = sd.slice(name, dim, start, stop)
+            torch.cuda.synchronize()
+            want_shape = list(shape)
+            want_shape[dim] = stop - start
+            assert list(t.shape) == want_shape
+            sel = oix.select(names=[name], dst="BF16", slices=[(dim, start, stop)])
+            assert np.array_equal(t.reshape(-1).view(torch.uint8).cpu().numpy(), sel.materialize(0, arena)), (name, dim)
+            checked += 1
+    assert checked >= 20
