@@ -449,7 +449,9 @@ st_status st_cache_clear(st_cache_t *cache);
  * read-only mappings after st_files_prefetch of their bytes, or read when a
  * file could not be mapped), copied into staging_dev
  * (each at a 256-byte aligned offset; staging_bytes must hold them all, else
- * ST_E_INVAL with the size needed) and materialized by one launch on
+ * ST_E_INVAL with the size needed; an output that is a dim-0 slice of a
+ * tensor no other output reads stages only its rows) and materialized by one
+ * launch on
  * `stream`, with the plan's tables in the library's static device array as
  * for st_materialize_noalloc (no device allocation; calls whose work
  * overlaps on the GPU race on that array: order them on one stream).  The

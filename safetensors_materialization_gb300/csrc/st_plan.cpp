@@ -1134,13 +1134,53 @@ st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_c
           seen[q] = 1;
           need.push_back(q);
         }
+    // An output that is a dim-0 slice of a tensor no other output reads
+    // stages only its rows (a tensor-parallel rank reads its share of the
+    // file, not the whole tensor); the staged tensor is then those rows, and
+    // the output reads it unsliced.
+    std::vector<uint32_t> readers(ix.ent.size(), 0), need_at(ix.ent.size(), 0);
+    for (const Output &o : outs)
+      for (uint32_t q : o.reads) ++readers[q];
+    for (size_t k = 0; k < need.size(); ++k) need_at[need[k]] = static_cast<uint32_t>(k);
+    std::vector<uint64_t> sub_lo(need.size(), 0);  // staged range: source bytes [begin + sub_lo, ...)
+    std::vector<int64_t> sub_rows(need.size(), -1);  // rows staged, or -1: the whole tensor
+    std::vector<st_slice> slices2;                  // the selection's slices, those outputs unsliced
+    if (sel->slices) {
+      std::vector<int64_t> sel_of(ix.ent.size(), -1);  // view position -> selection entry
+      for (size_t j = 0; j < sel->n_names; ++j) {
+        auto it = ix.pos.find(std::string_view(sel->names[j]));
+        if (it != ix.pos.end()) sel_of[it->second] = static_cast<int64_t>(j);
+      }
+      for (const Output &o : outs) {
+        const uint32_t q = o.reads[0];
+        const Tensor &t = ix.core->tensors[ix.ent[q]];
+        if (o.sdim != 0 || o.qkind != ST_QUANT_NONE || readers[q] != 1 || sel_of[o.pos] < 0 || t.shape.empty() ||
+            t.shape[0] <= 0)
+          continue;
+        const uint64_t row_bytes = (t.end - t.begin) / static_cast<uint64_t>(t.shape[0]);
+        const uint32_t k = need_at[q];
+        sub_lo[k] = static_cast<uint64_t>(o.start) * row_bytes;
+        sub_rows[k] = o.stop - o.start;
+        if (slices2.empty()) slices2.assign(sel->slices, sel->slices + sel->n_names);
+        slices2[sel_of[o.pos]].dim = -1;
+      }
+    }
+    st_selection sel2 = *sel;
+    if (!slices2.empty()) sel2.slices = slices2.data();
     // Those tensors staged back to back (256-byte aligned) under their view
     // names: a small index whose data section is the staging buffer.
     auto core = std::make_shared<Core>();
     uint64_t at = 0;
-    for (uint32_t q : need) {
+    for (size_t k = 0; k < need.size(); ++k) {
+      const uint32_t q = need[k];
       Tensor t = ix.core->tensors[ix.ent[q]];
-      const uint64_t n = t.end - t.begin;
+      uint64_t n = t.end - t.begin;
+      if (sub_rows[k] >= 0) {
+        const uint64_t rows = static_cast<uint64_t>(t.shape[0]);
+        n = static_cast<uint64_t>(sub_rows[k]) * (n / rows);
+        t.numel = static_cast<uint64_t>(sub_rows[k]) * (t.numel / rows);
+        t.shape[0] = sub_rows[k];
+      }
       t.name = ix.names[q];
       at = (at + 255) & ~uint64_t(255);
       t.begin = at;
@@ -1174,7 +1214,7 @@ st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_c
     po.unit_bytes = std::max<uint64_t>(kDefaultUnitBytes, traffic / 32768 + 1);
     po.workers = static_cast<uint32_t>(std::min<uint64_t>(kLazyMaxWarps, (traffic / kLazyBytesPerWarp + 8) & ~7ull));
     st_plan_s plan;
-    s = plan_host(mini, sel, dst_dtype, &po, &plan);
+    s = plan_host(mini, &sel2, dst_dtype, &po, &plan);
     if (s != ST_OK) return s;
     s = check_tma_source(&plan, staging_dev);
     if (s != ST_OK) return s;
@@ -1192,23 +1232,23 @@ st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_c
     const bool direct = !cache && files_mapped(files);
     cudaError_t e = cudaSuccess;
     for (size_t k = 0; k < need.size() && s == ST_OK; ++k) {
-      const Tensor &src = ix.core->tensors[ix.ent[need[k]]];
-      const uint64_t n = src.end - src.begin;
+      const uint64_t from = ix.core->tensors[ix.ent[need[k]]].begin + sub_lo[k];  // arena byte
+      const uint64_t n = core->tensors[k].end - core->tensors[k].begin;
       if (!n) continue;
       uint8_t *to = static_cast<uint8_t *>(staging_dev) + core->tensors[k].begin;
       const void *host = nullptr;
       if (direct) {
-        s = st_files_prefetch(files, src.begin, n, 0);
-        if (s == ST_OK) s = copy_arena_direct(files, src.begin, n, to, st);
+        s = st_files_prefetch(files, from, n, 0);
+        if (s == ST_OK) s = copy_arena_direct(files, from, n, to, st);
         continue;
       }
       if (cache) {
-        s = st_cache_get(cache, files, src.begin, n, threads, &host);
+        s = st_cache_get(cache, files, from, n, threads, &host);
         if (s != ST_OK) break;
         held.push_back(host);
       } else {
         plain.emplace_back(n);
-        s = read_arena(files, src.begin, n, plain.back().data(), threads);
+        s = read_arena(files, from, n, plain.back().data(), threads);
         if (s != ST_OK) break;
         host = plain.back().data();
       }

@@ -362,3 +362,25 @@ def test_lazy_slices_match_oracle(stmat, oracle, tmp_path, cache_bytes):
             assert np.array_equal(t.reshape(-1).view(torch.uint8).cpu().numpy(), sel.materialize(0, arena)), (name, dim)
             checked += 1
     assert checked >= 20
+
+
+@pytest.mark.gpu
+def test_lazy_row_slice_reads_only_its_rows(stmat, oracle, tmp_path):
+    """A dim-0 slice stages only its rows: the RAM tier then holds exactly
+    those bytes (a tensor-parallel rank reads its share of the file), and the
+    output still equals the oracle's."""
+    torch = gpu()
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    sd = stmat.StreamStateDict(paths, dst="BF16", ram_cache_bytes=1 << 30)
+    oix, arena = oracle_joined(oracle, w, paths)
+    name = "model.layers.1.mlp.up_proj.weight"
+    shape, _ = sd.info(name)
+    rows = shape[0]
+    t = sd.slice(name, 0, rows // 4, rows // 2)
+    torch.cuda.synchronize()
+    e = sd.index.entry(sd._pos[name])
+    row_bytes = (e["end"] - e["begin"]) // rows
+    assert sd.cache.stats()["bytes"] == (rows // 2 - rows // 4) * row_bytes
+    sel = oix.select(names=[name], dst="BF16", slices=[(0, rows // 4, rows // 2)])
+    assert np.array_equal(t.reshape(-1).view(torch.uint8).cpu().numpy(), sel.materialize(0, arena))
