@@ -459,7 +459,8 @@ def time_load_files(args, w, host, data_start, data_bytes, dev, outs, sel, strea
         first, _ = timed(lambda: first_load(main_ring))
         gbs = lambda t: round(gb_dst * world / t, 1)
         return {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "ms_per_step": round(es * 1e3, 3),
-                "repeats_gbs": [gbs(r) for r in reps], "files": len(paths), "file_bytes_per_step": data_bytes,
+                "repeats_gbs": [gbs(r) for r in reps], "files": len(paths),
+                "file_bytes_per_step": fplan.copy_bytes()[0],
                 "chunk_bytes": chunk,
                 "mode": "ring-less: copies from the files' mappings" if direct else
                         f"pinned ring of {3 * chunk} bytes, {args.io_threads} pread threads",
@@ -605,8 +606,9 @@ def run_ours(args, rank, world, local):
         ev1.record(copy)
         copy.synchronize()
         h2d_gbs = 3 * data_bytes / (ev0.elapsed_time(ev1) / 1e3) / 1e9
-        e2e = {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "h2d_bytes_per_step": data_bytes,
-               "stage_h2d_gbs": round(h2d_gbs, 1),
+        copied, n_ranges = eplan.copy_bytes()   # a sparse plan copies only the ranges it reads
+        e2e = {"value": round(gb_dst * world / es, 3), "unit": "GB/s", "h2d_bytes_per_step": copied,
+               "copy_ranges": n_ranges, "stage_h2d_gbs": round(h2d_gbs, 1),
                "d2h_bytes_per_step": 4, "ms_per_step": round(es * 1e3, 3),
                "repeats_gbs": [round(gb_dst * world / r, 1) for r in reps],
                "chunk_bytes": args.e2e_chunk_mb << 20, "chunks": eplan.stats()["chunks"]}

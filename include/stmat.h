@@ -298,6 +298,12 @@ st_status st_plan_arena(const st_plan_t *plan, uint64_t align, uint64_t *offsets
  * tuning; any pointer may be NULL. */
 st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chunks, uint64_t *pieces,
                         uint32_t *kernel);
+/* The data-section bytes st_load and st_load_files copy for this plan: all of
+ * it, or, when the outputs read under three quarters of it (a
+ * tensor-parallel rank's slices), only the byte ranges they read (each
+ * output's source extent and its scales, merged across gaps under 64 KiB),
+ * in *ranges pieces (may be NULL). */
+st_status st_plan_copy_bytes(const st_plan_t *plan, uint64_t *bytes, uint32_t *ranges);
 /* Piece k (host copy): `rows` runs of `count` counted units; run r reads
  * from data-section offset src + r * pitch and writes output bytes from
  * dst + r * count * out_itemsize; scale offset (or ~0), output, class. */
@@ -400,9 +406,11 @@ st_status st_stage_h2d(void *dst_dev, const void *src_host, uint64_t bytes, uint
 /* Stages the data section from host memory (pinned, data_bytes long) into
  * data_dev on `copy_stream` chunk by chunk (the plan's chunk_bytes) and
  * materializes each chunk's pieces on `compute_stream` as soon as that
- * chunk's copy completes, so copies and kernels overlap.  The first copy
- * waits for work already queued on compute_stream.  Arguments as for
- * st_materialize.  Returns without synchronizing. */
+ * chunk's copy completes, so copies and kernels overlap.  A plan whose
+ * outputs read under three quarters of the data section copies only the
+ * ranges they read (st_plan_copy_bytes); data_dev's other bytes are left as
+ * they are.  The first copy waits for work already queued on compute_stream.
+ * Arguments as for st_materialize.  Returns without synchronizing. */
 st_status st_load(const void *data_host, void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
                   const float *scales, void *copy_stream, void *compute_stream);
 
@@ -490,7 +498,10 @@ st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_c
  * ST_E_IO before that chunk's copy is queued.  On a GPU for which
  * st_device_reads_pageable reports 1 the copy engine then reads the page
  * cache directly.  Bytes of the arena that no file covers (gaps between
- * joined shards) get no defined value in either mode.
+ * joined shards) get no defined value in either mode.  A plan whose outputs
+ * read under three quarters of the arena (a tensor-parallel rank) reads and
+ * copies only those ranges (st_plan_copy_bytes), in both modes; ring-less,
+ * each range is then faulted in right before its copy.
  * The first copy waits for work already queued on compute_stream.  Blocks
  * the calling thread until every chunk is read and its copy finished (the
  * ring is then free, the mappings no longer read: the files may be closed),

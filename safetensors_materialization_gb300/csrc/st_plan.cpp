@@ -122,6 +122,11 @@ struct st_plan_s {
   uint64_t unit_bytes = kDefaultUnitBytes;
   bool class_major = false;
   uint32_t n_chunks = 1;
+  // Data-section byte ranges the plan reads (sorted, merged); `sparse` when
+  // they cover under three quarters of it (a tensor-parallel rank's load):
+  // the loaders then copy only these.
+  std::vector<std::pair<uint64_t, uint64_t>> ranges;
+  bool sparse = false;
   std::vector<Piece> pieces;
   std::vector<uint32_t> parts;  // n_chunks * (workers + 1)
   // device side
@@ -582,6 +587,60 @@ void build_pieces(st_plan_s *p) {
   }
 }
 
+// The data-section bytes a plan's outputs read: each output's source extent
+// (its runs from the first to the last), its per-tensor scale, its block
+// scales and global scale; sorted, and merged across gaps under 64 KiB.
+void compute_ranges(st_plan_s *p) {
+  const Core &core = *p->index->core;
+  std::vector<std::pair<uint64_t, uint64_t>> r;
+  r.reserve(p->outs.size() * 2);
+  auto whole = [&](int64_t entry) {
+    if (entry >= 0) r.push_back({core.tensors[entry].begin, core.tensors[entry].end});
+  };
+  for (const Output &o : p->outs) {
+    if (o.units == 0) continue;
+    const uint64_t si = cls_in_size(o.cls);
+    r.push_back({o.src0, o.src0 + (o.runs - 1) * o.pitch + (o.runs > 1 ? o.run : o.units) * si});
+    whole(o.scale);
+    if (o.qkind != ST_QUANT_NONE) {
+      whole(o.qscale_entry);
+      if (o.quant.scale2 != kNoScale) r.push_back({o.quant.scale2, o.quant.scale2 + 4});
+    }
+  }
+  std::sort(r.begin(), r.end());
+  constexpr uint64_t kGap = 65536;
+  p->ranges.clear();
+  uint64_t covered = 0;
+  for (const auto &x : r) {
+    if (!p->ranges.empty() && x.first <= p->ranges.back().second + kGap)
+      p->ranges.back().second = std::max(p->ranges.back().second, x.second);
+    else
+      p->ranges.push_back(x);
+  }
+  for (const auto &x : p->ranges) covered += x.second - x.first;
+  p->sparse = covered < core.data_bytes / 4 * 3;
+}
+
+// Calls fn(lo, hi) for the plan's read ranges within [off, off + n): all of
+// it when the plan is not sparse.
+template <class F>
+st_status for_each_range(const st_plan_s *p, uint64_t off, uint64_t n, F fn) {
+  if (!n) return ST_OK;
+  if (!p->sparse) return fn(off, off + n);
+  auto it = std::lower_bound(p->ranges.begin(), p->ranges.end(), std::make_pair(off, uint64_t(0)),
+                             [](const std::pair<uint64_t, uint64_t> &a, const std::pair<uint64_t, uint64_t> &b) {
+                               return a.second <= b.first;
+                             });
+  for (; it != p->ranges.end() && it->first < off + n; ++it) {
+    const uint64_t lo = std::max(off, it->first), hi = std::min(off + n, it->second);
+    if (lo < hi) {
+      const st_status s = fn(lo, hi);
+      if (s != ST_OK) return s;
+    }
+  }
+  return ST_OK;
+}
+
 // Selection, kernel build, warps and pieces of a plan (host side only).
 st_status plan_host(std::shared_ptr<const IndexData> index, const st_selection *sel, st_dtype dst_dtype,
                     const st_plan_options *opts, st_plan_s *p) {
@@ -646,6 +705,7 @@ st_status plan_host(std::shared_ptr<const IndexData> index, const st_selection *
   uint64_t cap = std::max<uint64_t>(1, cost / kMinWorkerCost);
   p->workers = static_cast<uint32_t>(std::min<uint64_t>(workers, cap));
   build_pieces(p);
+  compute_ranges(p);
   if (has_quant) {
     p->quant.resize(p->outs.size());
     for (size_t i = 0; i < p->outs.size(); ++i) p->quant[i] = p->outs[i].quant;
@@ -737,6 +797,20 @@ st_status st_plan_arena(const st_plan_t *p, uint64_t align, uint64_t *offsets, u
     at += p->outs[i].numel * dtype_size(p->outs[i].out_dtype);
   }
   *total = at;
+  return ST_OK;
+}
+
+st_status st_plan_copy_bytes(const st_plan_t *p, uint64_t *bytes, uint32_t *ranges) {
+  if (!p || !bytes) return set_error(ST_E_INVAL, "NULL argument");
+  if (!p->sparse) {
+    *bytes = p->index->core->data_bytes;
+    if (ranges) *ranges = 1;
+    return ST_OK;
+  }
+  uint64_t b = 0;
+  for (const auto &x : p->ranges) b += x.second - x.first;
+  *bytes = b;
+  if (ranges) *ranges = static_cast<uint32_t>(p->ranges.size());
   return ST_OK;
 }
 
@@ -990,12 +1064,17 @@ st_status st_load(const void *data_host, void *data_dev, const st_plan_t *p, voi
   for (uint32_t k = 0; k < p->n_chunks; ++k) {
     uint64_t off = static_cast<uint64_t>(k) * C;
     uint64_t n = off < data ? std::min(C, data - off) : 0;
-    if (n) {
-      e = cudaMemcpyAsync(static_cast<uint8_t *>(data_dev) + off, static_cast<const uint8_t *>(data_host) + off, n,
-                          cudaMemcpyHostToDevice, cs);
-      if (e != cudaSuccess)
-        return set_error(ST_E_CUDA, "copy of chunk %u (%llu bytes): %s", k, (unsigned long long)n, cuda_msg(e).c_str());
-    }
+    // The whole chunk, or (sparse plan) only the byte ranges the plan reads.
+    s = for_each_range(p, off, n, [&](uint64_t lo, uint64_t hi) -> st_status {
+      const cudaError_t ce = cudaMemcpyAsync(static_cast<uint8_t *>(data_dev) + lo,
+                                             static_cast<const uint8_t *>(data_host) + lo, hi - lo,
+                                             cudaMemcpyHostToDevice, cs);
+      if (ce != cudaSuccess)
+        return set_error(ST_E_CUDA, "copy of chunk %u (%llu bytes): %s", k, (unsigned long long)(hi - lo),
+                         cuda_msg(ce).c_str());
+      return ST_OK;
+    });
+    if (s != ST_OK) return s;
     e = cudaEventRecord(p->events[k], cs);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ks, p->events[k], 0);
     if (e != cudaSuccess) return set_error(ST_E_CUDA, "chunk %u event: %s", k, cuda_msg(e).c_str());
@@ -1041,7 +1120,7 @@ st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t
     Populator *p = nullptr;
     ~PopGuard() { populate_stop(p); }
   } pop;
-  if (direct && data) {
+  if (direct && data && !p->sparse) {  // a sparse plan faults in each range it copies, right before the copy
     pop.p = populate_start(files, 0, data, C, 1);
     if (!pop.p) return set_error(ST_E_NOMEM, "starting the populate threads");
   }
@@ -1051,8 +1130,13 @@ st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t
     if (direct) {
       // On an error the copies already queued still read the mappings: wait
       // for them, so that closing the files afterwards is safe.
-      if (n) s = populate_wait(pop.p, k);
-      if (n && s == ST_OK) s = copy_arena_direct(files, off, n, static_cast<uint8_t *>(data_dev) + off, cs);
+      if (n && pop.p) s = populate_wait(pop.p, k);
+      if (s == ST_OK)
+        s = for_each_range(p, off, n, [&](uint64_t lo, uint64_t hi) -> st_status {
+          st_status r = pop.p ? ST_OK : st_files_prefetch(files, lo, hi - lo, 0);
+          if (r == ST_OK) r = copy_arena_direct(files, lo, hi - lo, static_cast<uint8_t *>(data_dev) + lo, cs);
+          return r;
+        });
       if (s == ST_OK) {
         e = cudaEventRecord(p->events[k], cs);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(ks, p->events[k], 0);
@@ -1071,17 +1155,19 @@ st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t
       if (e != cudaSuccess) return set_error(ST_E_CUDA, "waiting for chunk %llu: %s", (unsigned long long)(k - slots),
                                              cuda_msg(e).c_str());
     }
-    if (n) {
-      const uint64_t arena = files_arena_bytes(files);
-      const uint64_t rn = off < arena ? std::min(n, arena - off) : 0;
-      if (rn) {
-        s = read_arena(files, off, rn, slot, threads);
-        if (s != ST_OK) return s;
-      }
-      e = cudaMemcpyAsync(static_cast<uint8_t *>(data_dev) + off, slot, n, cudaMemcpyHostToDevice, cs);
-      if (e != cudaSuccess)
-        return set_error(ST_E_CUDA, "copy of chunk %u (%llu bytes): %s", k, (unsigned long long)n, cuda_msg(e).c_str());
-    }
+    // The whole chunk, or (sparse plan) only the byte ranges the plan reads,
+    // each read into the slot at its place and copied.
+    s = for_each_range(p, off, n, [&](uint64_t lo, uint64_t hi) -> st_status {
+      st_status r = read_arena(files, lo, hi - lo, slot + (lo - off), threads);
+      if (r != ST_OK) return r;
+      const cudaError_t ce = cudaMemcpyAsync(static_cast<uint8_t *>(data_dev) + lo, slot + (lo - off), hi - lo,
+                                             cudaMemcpyHostToDevice, cs);
+      if (ce != cudaSuccess)
+        return set_error(ST_E_CUDA, "copy of chunk %u (%llu bytes): %s", k, (unsigned long long)(hi - lo),
+                         cuda_msg(ce).c_str());
+      return ST_OK;
+    });
+    if (s != ST_OK) return s;
     e = cudaEventRecord(p->events[k], cs);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ks, p->events[k], 0);
     if (e != cudaSuccess) return set_error(ST_E_CUDA, "chunk %u event: %s", k, cuda_msg(e).c_str());

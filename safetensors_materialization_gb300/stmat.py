@@ -30,7 +30,7 @@ EXPORTS = [
     "st_index_metadata_get", "st_view_prefix", "st_view_filter", "st_view_rename", "st_index_concat",
     "st_plan",
     "st_plan_free", "st_plan_count", "st_plan_output", "st_plan_arena", "st_plan_stats",
-    "st_plan_piece", "st_plan_worker", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
+    "st_plan_piece", "st_plan_worker", "st_plan_copy_bytes", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
     "st_materialize_noalloc", "st_index_open", "st_files_open", "st_files_close", "st_files_read",
     "st_load_files", "st_cache_create", "st_cache_free", "st_cache_get", "st_cache_release",
     "st_cache_stats", "st_cache_clear", "st_load_tensors", "st_host_affinity", "st_device_reads_pageable",
@@ -129,6 +129,7 @@ def lib():
             "st_plan_piece": [P, U64, C.POINTER(U64), C.POINTER(U64), C.POINTER(U64), C.POINTER(U32),
                               C.POINTER(U32), C.POINTER(U32), C.POINTER(U32), C.POINTER(U64)],
             "st_plan_worker": [P, U32, U32, C.POINTER(U64), C.POINTER(U64)],
+            "st_plan_copy_bytes": [P, C.POINTER(U64), C.POINTER(U32)],
             "st_materialize": [P, P, P, P, P],
             "st_materialize_noalloc": [P, P, P, P, P],
             "st_stage_h2d": [P, P, U64, U64, P, P],
@@ -694,6 +695,12 @@ class Plan:
         _check(lib().st_load_files(files.handle, _addr(data_dev), self._h, _addr(dst_ptrs), _addr(scales),
                                    _addr(ring_host), ring_bytes, threads, _stream(copy_stream),
                                    _stream(compute_stream)))
+
+    def copy_bytes(self):
+        """st_plan_copy_bytes: (bytes the loaders copy for this plan, ranges)."""
+        b, r = C.c_uint64(), C.c_uint32()
+        _check(lib().st_plan_copy_bytes(self._h, C.byref(b), C.byref(r)))
+        return b.value, r.value
 
     def check(self, stream=None):
         flags = C.c_uint32()

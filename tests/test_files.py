@@ -286,3 +286,54 @@ def test_host_affinity_binds_to_the_gpu_socket(stmat):
         assert now == listed
     finally:
         os.sched_setaffinity(0, before)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("chunk", [0, 1 << 20, 3 << 20])
+def test_tensor_parallel_rank_copies_only_its_ranges(stmat, oracle, tmp_path, chunk):
+    """A tensor-parallel rank's plan reads under three quarters of the data
+    section, so st_load and both st_load_files modes copy only the byte
+    ranges it reads (bytes outside them keep the device buffer's fill); the
+    outputs equal the oracle's sliced outputs."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    w = synth.llm8b(seed=8, layers=2, hidden=1024, inter=2816, vocab=4000, kv=256, shards=2)
+    paths, datas = write_shards(str(tmp_path), w)
+    files, ix = stmat.Files.of_checkpoint(paths)
+    total = ix.sizes()[1]
+    oix, obases = oracle.concat([oracle.parse_header(l.header, l.data_bytes) for l in w.files])
+    arena = np.zeros(total, np.uint8)
+    for b, d in zip(obases, datas):
+        arena[b:b + d.size] = d
+    host = torch.from_numpy(arena).pin_memory()
+    entries = [e for lay in w.files for e in lay.entries]
+    probe = "model.layers.0.mlp.up_proj.weight"          # split on dim 0: rank 0 never reads its last rows
+    probe_end = [e for e in ix.entries() if e["name"] == probe][0]["end"]
+    for rank in (0, 3):
+        tp = synth.tp_slices(entries, 4, rank)
+        names = list(tp)
+        slices = [tp[n] for n in names]
+        plan = ix.plan(dst="BF16", names=names, slices=slices, chunk_bytes=chunk)
+        sel = oix.select(names=names, dst="BF16", slices=slices)
+        want = [sel.materialize(i, arena) for i in range(len(sel))]
+        for mode in ("pinned", "ringless", "ring"):
+            dev = torch.full((total,), 0xA5, dtype=torch.uint8, device="cuda")
+            outs = stmat.Outputs(plan)
+            copy = torch.cuda.Stream()
+            cur = torch.cuda.current_stream()
+            if mode == "pinned":
+                plan.load(host, dev, outs.ptrs, copy_stream=copy, compute_stream=cur)
+            elif mode == "ringless":
+                plan.load_files(files, dev, outs.ptrs, None, copy_stream=copy, compute_stream=cur)
+            else:
+                C = chunk or total
+                ring = torch.empty(2 * C, dtype=torch.uint8).pin_memory()
+                plan.load_files(files, dev, outs.ptrs, ring, threads=4, copy_stream=copy, compute_stream=cur)
+            torch.cuda.synchronize()
+            assert plan.check() == 0
+            for i in range(len(want)):
+                assert np.array_equal(outs.raw(i).cpu().numpy(), want[i]), (mode, sel.output(i)["name"])
+            if rank == 0:
+                assert int(dev[probe_end - 1].item()) == 0xA5, mode   # never copied: the plan does not read it
+    files.close()

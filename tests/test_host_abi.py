@@ -369,3 +369,26 @@ def test_sliced_pieces_cover_each_output_once(stmat, chunk):
         units = o["numel"] * (1 if o["dtype"] != o["src_dtype"] else isz)   # copies count bytes
         assert len(covered[i]) == units, o["name"]
     assert multi > 0
+
+
+def test_plan_copy_bytes_of_a_tensor_parallel_rank(stmat):
+    """A tensor-parallel rank's plan copies only the byte ranges it reads
+    (under three quarters of the data section); a whole-checkpoint plan
+    copies everything.  Host-only plans, no GPU."""
+    from safetensors_materialization_gb300 import synth
+    w = synth.llm8b(seed=8, layers=2, hidden=1024, inter=2816, vocab=4000, kv=256, shards=1)
+    lay = w.files[0]
+    ix = stmat.Index.from_header(lay.header, lay.data_bytes)
+    full = ix.plan(dst="BF16", workers=64, host_only=True)
+    assert full.copy_bytes() == (lay.data_bytes, 1)
+    tp = synth.tp_slices(lay.entries, 4, 1)
+    names = list(tp)
+    part = ix.plan(dst="BF16", names=names, slices=[tp[n] for n in names], workers=64, host_only=True)
+    b, r = part.copy_bytes()
+    ents = {e["name"]: e for e in ix.entries()}
+    want = 0   # each output's source extent: a dim-0 slice its rows; a dim-1 slice from its first row's
+    for n in names:   # first column to its last row's last column (BF16: 2 bytes an element)
+        (rows, cols), (dim, start, stop) = ents[n]["shape"], tp[n]
+        want += (stop - start) * cols * 2 if dim == 0 else ((rows - 1) * cols + (stop - start)) * 2
+    assert r > 1 and want <= b < lay.data_bytes * 3 // 4
+    assert b <= want + r * 65536                    # plus at most the merged gaps
