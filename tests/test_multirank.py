@@ -2,7 +2,8 @@
 of a checkpoint with st_selection.part/n_parts (host-only plans, no GPU), the
 parts are exchanged over the process group, and their union must be every
 output exactly once, in order, with the same bytes as the oracle's parts.
-The step-time reduction bench.py uses (max over ranks) is checked too.
+The step-time reduction bench.py uses (max over ranks) is checked too, and
+that each rank's loads copy only its part's source bytes.
 """
 import os
 import socket
@@ -31,7 +32,7 @@ def _worker(rank, world, port, q):
         lay = synth.unet().files[0]
         ix = stmat.Index.from_header(lay.header, lay.data_bytes).view_rename([("model.diffusion_model.", "unet.")])
         plan = ix.plan(dst="BF16", part=rank, n_parts=world, workers=1024, host_only=True)
-        mine = [(o["name"], o["bytes"]) for o in plan.outputs()]
+        mine = ([(o["name"], o["bytes"]) for o in plan.outputs()], plan.copy_bytes()[0], lay.data_bytes)
         parts = [None] * world
         dist.all_gather_object(parts, mine)
         t = torch.tensor([1.5 + rank])        # a stand-in step time per rank
@@ -58,8 +59,14 @@ def test_two_ranks_partition_outputs(stmat, oracle):
     for rank, parts, tmax in results:
         assert not isinstance(parts, str), parts
         assert tmax == 2.5                      # max over ranks
-    parts = results[0][1]
-    assert results[1][1] == parts               # every rank sees the same split
+    assert results[1][1] == results[0][1]       # every rank sees the same split
+    # each rank stages only its part's source bytes: under three quarters of the data section each,
+    # together the whole of it (plus at most a merged gap at the boundary)
+    data_bytes = results[0][1][0][2]
+    copied = [c for _, c, _ in results[0][1]]
+    assert all(c < data_bytes * 3 // 4 for c in copied)
+    assert data_bytes <= sum(copied) <= data_bytes + 65536
+    parts = [p for p, _, _ in results[0][1]]
     from safetensors_materialization_gb300 import synth
     lay = synth.unet().files[0]
     full = stmat.Index.from_header(lay.header, lay.data_bytes).view_rename(
