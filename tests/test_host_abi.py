@@ -392,3 +392,29 @@ def test_plan_copy_bytes_of_a_tensor_parallel_rank(stmat):
         want += (stop - start) * cols * 2 if dim == 0 else ((rows - 1) * cols + (stop - start)) * 2
     assert r > 1 and want <= b < lay.data_bytes * 3 // 4
     assert b <= want + r * 65536                    # plus at most the merged gaps
+
+
+def test_plan_copy_ranges_merge_and_threshold(stmat):
+    """The ranges a sparse plan copies: one per output extent, merged when the
+    gap between them is at most 64 KiB; a plan reading three quarters or more
+    of the data section copies all of it."""
+    import json
+    import struct
+    n = 100_000
+    ents = {name: {"dtype": "U8", "shape": [n], "data_offsets": [k * n, (k + 1) * n]}
+            for k, name in enumerate(["a", "b", "c", "d"])}
+    h = json.dumps(ents).encode()
+    img = np.frombuffer(struct.pack("<Q", len(h)) + h + bytes(4 * n), dtype=np.uint8)
+    ix = stmat.Index.from_file(img)
+
+    def copied(sl):
+        names = list(sl)
+        return ix.plan(dst="KEEP", names=names, slices=[sl[k] for k in names], workers=8,
+                       host_only=True).copy_bytes()
+
+    # a[99000:100000] ends at 100000; b's slice starts 65536 (merged) or 65537 (separate) bytes later
+    assert copied({"a": (0, 99_000, n), "b": (0, 65_536, 66_536)}) == (100_000 + 66_536 - 99_000, 1)
+    assert copied({"a": (0, 99_000, n), "b": (0, 65_537, 66_537)}) == (2_000, 2)
+    # three quarters of the data section or more: everything
+    assert copied({"a": (0, 0, n), "b": (0, 0, n), "c": (0, 0, n)}) == (4 * n, 1)
+    assert copied({"a": (0, 0, n), "b": (0, 0, n), "c": (0, 0, n - 1)}) == (3 * n - 1, 1)
