@@ -384,3 +384,44 @@ def test_lazy_row_slice_reads_only_its_rows(stmat, oracle, tmp_path):
     assert sd.cache.stats()["bytes"] == (rows // 2 - rows // 4) * row_bytes
     sel = oix.select(names=[name], dst="BF16", slices=[(0, rows // 4, rows // 2)])
     assert np.array_equal(t.reshape(-1).view(torch.uint8).cpu().numpy(), sel.materialize(0, arena))
+
+
+def test_cache_is_thread_safe(stmat, tmp_path):
+    """Six host threads get and release random ranges of one file through one
+    small RAM tier (evictions all the time): every copy holds its bytes, and
+    once nothing is held the tier is within its bound and its counters add
+    up."""
+    import ctypes
+    import threading
+    path, data = blob_file(tmp_path, n=4 << 20, seed=5)
+    files = stmat.Files([(path, 0, data.size, 0)])
+    c = stmat.Cache(1 << 20, pinned=False)
+    errors, calls = [], []
+
+    def worker(seed):
+        r = np.random.Generator(np.random.PCG64(seed))
+        k = 0
+        for _ in range(150):
+            begin = int(r.integers(0, 64)) * 65536               # a few distinct ranges: hits and misses
+            n = int(r.integers(1, 8)) * 16384
+            n = min(n, data.size - begin)
+            h = c.get(files, begin, n, threads=int(r.integers(1, 4)))
+            got = np.ctypeslib.as_array((ctypes.c_uint8 * n).from_address(h)).copy()
+            c.release(h)
+            k += 1
+            if not np.array_equal(got, data[begin:begin + n]):
+                errors.append((seed, begin, n))
+        calls.append(k)
+
+    ts = [threading.Thread(target=worker, args=(s,)) for s in range(6)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors
+    st = c.stats()
+    assert st["bytes"] <= st["max_bytes"]
+    assert st["hits"] + st["misses"] == sum(calls) == 900
+    c.clear()
+    assert c.stats()["entries"] == 0
+    files.close()
