@@ -1,8 +1,9 @@
 """Builds libstmat.so in-tree for GB300 (sm_103a) with nvcc.
 
-Three translation units compile in parallel (header parser/index, planner +
-C ABI, kernels) and link into one shared library against the shared CUDA
-runtime.  The result lives next to this file; nothing is installed.
+The translation units (header parser and index, file reads and RAM tier,
+planner and C ABI, kernels) compile in parallel and link into one shared
+library against the shared CUDA runtime.  The result lives next to this
+file; nothing is installed.
 """
 import glob
 import os
