@@ -1,5 +1,7 @@
 """Thin Python binding of libstmat (ctypes): the C ABI's names, with
-arguments marshalled from Python objects and torch tensors.
+arguments marshalled from Python objects and torch tensors, and
+StreamStateDict, the lazy mapping on top of st_load_tensors (keys from the
+headers, sd[name], slices and batches on access).
 
 Every step of the path (header parse, views, planning, staging copies and
 the materialize kernel) runs inside libstmat; PyTorch only provides device
