@@ -606,9 +606,11 @@ class StreamStateDict:
         flush()
         return {n: out[n] for n in names}
 
-    def items(self):
-        for n in self._names:
-            yield n, self[n]
+    def items(self, batch=64):
+        """(name, tensor) in key order, loaded `batch` names at a time with
+        load_many (one staging pass and one launch per batch)."""
+        for k in range(0, len(self._names), max(1, batch)):
+            yield from self.load_many(self._names[k:k + max(1, batch)]).items()
 
 
 class Plan:

@@ -425,3 +425,21 @@ def test_cache_is_thread_safe(stmat, tmp_path):
     c.clear()
     assert c.stats()["entries"] == 0
     files.close()
+
+
+@pytest.mark.gpu
+def test_items_in_batches_match_oracle(stmat, oracle, tmp_path):
+    """StreamStateDict.items(): every tensor in key order, loaded in batches,
+    equals the oracle's output."""
+    torch = gpu()
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    sd = stmat.StreamStateDict(paths, dst="BF16", ram_cache_bytes=1 << 30)
+    oix, arena = oracle_joined(oracle, w, paths)
+    names = []
+    for name, t in sd.items(batch=7):
+        names.append(name)
+        torch.cuda.synchronize()
+        sel = oix.select(names=[name], dst="BF16")
+        assert np.array_equal(t.reshape(-1).view(torch.uint8).cpu().numpy(), sel.materialize(0, arena)), name
+    assert names == sd.keys()
