@@ -340,7 +340,9 @@ typedef struct st_file_part {
  * read-only (shared) for ring-less st_load_files; a file that cannot be
  * mapped is still opened (only ring-less loads of its bytes then fail).
  * ST_E_IO on open/stat failures or a file too short, ST_E_INVAL on overlap.
- * The paths are copied.  A file must not shrink while it is open. */
+ * The paths are copied.  A file must not shrink while it is open.  Reads
+ * with several threads use reader threads the files object keeps until it is
+ * closed: a process forked after they started must not use the object. */
 st_status st_files_open(const st_file_part *parts, size_t n, st_files_t **out);
 void st_files_close(st_files_t *files);
 /* Reads arena bytes [begin, begin + bytes) into host[0, bytes) with up to
