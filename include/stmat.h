@@ -478,7 +478,10 @@ st_status st_cache_clear(st_cache_t *cache);
  * exceeded meanwhile.  Without a cache: blocks until the copies are done
  * (the files may then be closed).  The kernel runs asynchronously on
  * `stream`; staging_dev is in use until it has run.  Output dtypes,
- * errors and bit-exact results are those of st_plan + st_materialize. */
+ * errors and bit-exact results are those of st_plan + st_materialize.  The
+ * kernel's device flags (a wait for a staged copy that gave up; lazy
+ * destinations are checked on the host) go to the static array's error word:
+ * read them with st_static_check. */
 st_status st_load_tensors(const st_index_t *index, const st_files_t *files, st_cache_t *cache,
                           const st_selection *sel, st_dtype dst_dtype, void *const *dst_host_ptrs,
                           void *staging_dev, uint64_t staging_bytes, uint32_t threads, void *stream);
@@ -517,36 +520,53 @@ st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t
                         uint32_t threads, void *copy_stream, void *compute_stream);
 
 /* Allocation-free st_materialize.  No counterpart on the pages: it exists for
- * callers that cannot allocate device memory, for example code running while a
- * CUDA stream capture forbids cudaMalloc, or processes whose device memory is
- * entirely held by another allocator (a framework's caching pool, a serving
- * engine's preallocated arena) so that cudaMalloc fails even though memory is
- * free inside that pool.  Such a caller builds the plan with host_only set
- * (st_plan then touches no GPU memory) and calls this instead of
- * st_materialize; arguments are as for st_materialize.
- *   - Scratch: the plan's piece table, warp ranges and error word are copied
- *     (cudaMemcpyAsync from the plan's host memory, cudaMemsetAsync for the
- *     error word) into one static device array of 4 MiB built into the
- *     library.  Every GPU that loads the library holds those 4 MiB until the
- *     process exits.  A plan that needs more (48 bytes per piece plus 4 per
- *     warp per chunk, each part rounded up to 256 bytes) is rejected with
- *     ST_E_INVAL before anything is queued; plan with a larger unit_bytes or
- *     fewer workers to shrink it.
+ * callers that cannot allocate device memory, for example a plugin or
+ * library running inside a host application whose device memory is entirely
+ * held by that application's own allocator (a framework's caching pool, a
+ * serving engine's preallocated arena), so that cudaMalloc fails although
+ * the pool has room; or code that must not allocate once it is running,
+ * because cudaMalloc can block on the device and can fail at a point where
+ * the caller has no way to recover.  Such a caller builds the plan with
+ * host_only set (st_plan then touches no GPU memory) and calls this instead
+ * of st_materialize; arguments are as for st_materialize.
+ *   - Scratch: the plan's tables (piece table, per-chunk warp ranges and, for
+ *     block-scaled outputs, the block-scale table) are copied
+ *     (cudaMemcpyAsync from the plan's host memory) into one static device
+ *     array of 4 MiB built into the library.  Every GPU that loads the
+ *     library holds those 4 MiB until the process exits.  The tables may take
+ *     4 MiB - 256 bytes (the last 256 hold the error word): 48 bytes per
+ *     piece, plus 4 bytes per warp and chunk (plus 4 per chunk), plus 32
+ *     bytes per output for block-scaled plans, each part rounded up to 256
+ *     bytes (st_load_tensors adds 8 bytes per output for its destination
+ *     array).  A plan that needs more is rejected with ST_E_INVAL before
+ *     anything is queued; plan with a larger unit_bytes or fewer workers to
+ *     shrink it.
  *   - Set-up: the first call on a device, with that device current, looks up
- *     the array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.  Under a capture, the table copies read the
- *     plan's host memory when the graph runs: keep the plan alive while the
- *     graph can run.
+ *     the array's device address (cudaGetSymbolAddress) once for that device.
  *   - Sharing: every call, on every stream, uses the same array, and it keeps
- *     the last call's contents; the error word is cleared by each call.  Calls
- *     whose work overlaps on the GPU (different streams, or threads) race on
- *     the array and corrupt each other: order them on one stream.
+ *     the last call's tables.  Calls whose work overlaps on the GPU (different
+ *     streams, or threads) race on the array and corrupt each other: order
+ *     them on one stream.  The tables are rewritten by every call; nothing
+ *     in them needs to start at zero.
+ *   - Device flags: a NULL or misaligned destination is skipped as in
+ *     st_materialize, and a wait of the TMA build for a staged copy that gives
+ *     up stops that warp early (outputs incomplete).  Either sets a bit in the
+ *     array's error word, which keeps the bits of every call (and of
+ *     st_load_tensors) until st_static_check reads and clears it.
  *   - No cudaMalloc, cudaFree or other allocating CUDA or library routine is
- *     called.  A NULL or misaligned destination is skipped as in
- *     st_materialize but not reported (the flag stays in the array).
+ *     called.
  * Returns without synchronizing. */
 st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
                                  const float *scales, void *stream);
+
+/* Reads and clears the error word of the library's static device array on
+ * the current device: the device flags of every st_materialize_noalloc and
+ * st_load_tensors call since the last read (bits as for st_plan_check).
+ * Copies the word to the host on `stream` and waits for the stream, so every
+ * such call queued on it before has finished; calls on other streams are
+ * seen only once they have finished.  Allocates nothing.  Returns
+ * ST_E_DEVICE when any flag was set, ST_E_CUDA if the copy failed. */
+st_status st_static_check(void *stream, uint32_t *flags);
 
 /* Waits for `stream`, then reads and clears the plan's device error flags:
  * bit 0 = a non-empty output had a NULL or misaligned destination;

@@ -152,8 +152,12 @@ st_status kernel_occupancy(uint32_t variant, int *sms, int *blocks_per_sm);
 st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream);
 
 // Size of the device array behind st_materialize_noalloc, and its device
-// address on the current device (looked up on first use per device).
+// address on the current device (looked up on first use per device).  Its
+// last 256 bytes hold the error word of every launch from the array; the
+// kernels only OR bits into it, so it keeps every call's flags until
+// st_static_check reads and clears it.  The tables take the bytes before.
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+constexpr size_t kStaticErrOffset = kStaticScratchBytes - 256;
 st_status static_scratch(void **addr);
 
 // Shard-file reads (st_io.cpp): arena bytes [begin, begin + bytes) into host.

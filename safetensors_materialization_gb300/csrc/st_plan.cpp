@@ -911,8 +911,9 @@ std::map<int, TableMirror> g_mirrors;
 
 // Launches a plan whose tables live in the library's static device array:
 // pieces | warp ranges | block-scale table | destinations (when given on the
-// host) | error word, each 256-byte aligned, filled by stream-ordered copies
-// (with `mirror`, one copy from the device's page-locked mirror).
+// host), each 256-byte aligned, filled by stream-ordered copies (with
+// `mirror`, one copy from the device's page-locked mirror); the error word
+// sits at the array's fixed kStaticErrOffset and is not cleared here.
 st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *dst_dev, void *const *dst_host,
                         const float *scales, void *stream, bool mirror = false) {
   const size_t pieces_bytes = p->pieces.size() * sizeof(Piece);
@@ -922,13 +923,12 @@ st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *d
   const size_t quant_bytes = p->quant.size() * sizeof(QuantInfo);
   const size_t dst_off = (quant_off + quant_bytes + 255) & ~size_t(255);
   const size_t dst_bytes = dst_host ? p->outs.size() * sizeof(void *) : 0;
-  const size_t err_off = (dst_off + dst_bytes + 255) & ~size_t(255);
-  const size_t need = err_off + sizeof(uint32_t);
-  if (need > kStaticScratchBytes)
+  const size_t need = dst_off + dst_bytes;
+  if (need > kStaticErrOffset)
     return set_error(ST_E_INVAL,
-                     "the plan needs %zu bytes of static scratch (%zu pieces, %u warps, %u chunks) but the library "
-                     "holds %zu; plan with a larger unit_bytes or fewer workers",
-                     need, p->pieces.size(), p->workers, p->n_chunks, kStaticScratchBytes);
+                     "the plan needs %zu bytes of static scratch (%zu pieces, %u warps, %u chunks, %zu block-scale "
+                     "records) but the library holds %zu for tables; plan with a larger unit_bytes or fewer workers",
+                     need, p->pieces.size(), p->workers, p->n_chunks, p->quant.size(), kStaticErrOffset);
   void *scratch = nullptr;
   st_status s = static_scratch(&scratch);
   if (s != ST_OK) return s;
@@ -973,7 +973,6 @@ st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *d
       std::memcpy(h + parts_off, p->parts.data(), parts_bytes);
       if (quant_bytes) std::memcpy(h + quant_off, p->quant.data(), quant_bytes);
       if (dst_bytes) std::memcpy(h + dst_off, dst_host, dst_bytes);
-      std::memset(h + err_off, 0, sizeof(uint32_t));
       e = cudaMemcpyAsync(base, h, need, cudaMemcpyHostToDevice, st);
     }
     if (e == cudaSuccess) e = cudaEventRecord(m.done[k], st);
@@ -983,7 +982,6 @@ st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *d
     if (e == cudaSuccess && quant_bytes)
       e = cudaMemcpyAsync(base + quant_off, p->quant.data(), quant_bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess && dst_bytes) e = cudaMemcpyAsync(base + dst_off, dst_host, dst_bytes, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(base + err_off, 0, sizeof(uint32_t), st);  // left over from the last call
   }
   if (e != cudaSuccess) return set_error(ST_E_CUDA, "filling the static scratch: %s", cuda_msg(e).c_str());
   for (uint32_t k = 0; k < p->n_chunks; ++k) {
@@ -997,7 +995,7 @@ st_status launch_static(const st_plan_t *p, const void *data_dev, void *const *d
     a.workers = p->workers;
     a.dst = dst_host ? reinterpret_cast<void *const *>(base + dst_off) : dst_dev;
     a.scales = scales;
-    a.err = reinterpret_cast<uint32_t *>(base + err_off);
+    a.err = reinterpret_cast<uint32_t *>(base + kStaticErrOffset);
     a.quant = quant_bytes ? reinterpret_cast<const QuantInfo *>(base + quant_off) : nullptr;
     s = launch_materialize(a, p->kernel, stream);
     if (s != ST_OK) return s;
@@ -1377,6 +1375,27 @@ st_status st_plan_check(const st_plan_t *p, void *stream, uint32_t *flags) {
   *flags = v;
   if (v)
     return set_error(ST_E_DEVICE, "device flags 0x%x:%s%s", v,
+                     (v & kErrBadDst) ? " a non-empty output had a NULL or misaligned destination;" : "",
+                     (v & kErrTimeout) ? " a wait for a staged copy gave up;" : "");
+  return ST_OK;
+}
+
+st_status st_static_check(void *stream, uint32_t *flags) {
+  if (!flags) return set_error(ST_E_INVAL, "NULL argument");
+  void *scratch = nullptr;
+  st_status s = static_scratch(&scratch);
+  if (s != ST_OK) return s;
+  uint32_t *err = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(scratch) + kStaticErrOffset);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, err, sizeof v, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && v) e = cudaMemsetAsync(err, 0, sizeof v, st);
+  if (e == cudaSuccess && v) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return set_error(ST_E_CUDA, "reading the static error word: %s", cuda_msg(e).c_str());
+  *flags = v;
+  if (v)
+    return set_error(ST_E_DEVICE, "static-scratch device flags 0x%x:%s%s", v,
                      (v & kErrBadDst) ? " a non-empty output had a NULL or misaligned destination;" : "",
                      (v & kErrTimeout) ? " a wait for a staged copy gave up;" : "");
   return ST_OK;

@@ -16,8 +16,7 @@ import os
 import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-# STMAT_LIB may point at another build of the library (e.g. a tuning variant).
-LIB_PATH = os.environ.get("STMAT_LIB") or os.path.join(HERE, "libstmat.so")
+LIB_PATH = os.path.join(HERE, "libstmat.so")
 
 DTYPES = ["BOOL", "U8", "I8", "I16", "U16", "I32", "U32", "I64", "U64", "F16", "BF16", "F32", "F64",
           "F8_E4M3", "F8_E5M2", "KEEP"]
@@ -33,7 +32,7 @@ EXPORTS = [
     "st_plan",
     "st_plan_free", "st_plan_count", "st_plan_output", "st_plan_arena", "st_plan_stats",
     "st_plan_piece", "st_plan_worker", "st_plan_copy_bytes", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
-    "st_materialize_noalloc", "st_index_open", "st_files_open", "st_files_close", "st_files_read",
+    "st_materialize_noalloc", "st_static_check", "st_index_open", "st_files_open", "st_files_close", "st_files_read",
     "st_load_files", "st_cache_create", "st_cache_free", "st_cache_get", "st_cache_release",
     "st_cache_stats", "st_cache_clear", "st_load_tensors", "st_host_affinity", "st_device_reads_pageable",
     "st_files_prefetch",
@@ -137,6 +136,7 @@ def lib():
             "st_stage_h2d": [P, P, U64, U64, P, P],
             "st_load": [P, P, P, P, P, P, P],
             "st_plan_check": [P, P, C.POINTER(U32)],
+            "st_static_check": [P, C.POINTER(U32)],
             "st_index_open": [C.c_char_p, PP, C.POINTER(U64)],
             "st_files_open": [C.POINTER(FilePart), S, PP],
             "st_files_read": [P, U64, U64, P, U32],
@@ -353,7 +353,10 @@ class Index:
                      scale_names=None, scale_suffix=None, quant=None, slices=None):
         """st_load_tensors: the lazy path for a few named tensors (read through
         `cache`, staged in `staging`, one launch on `stream`); dst_ptrs: one
-        device address per output, in output order; slices as for plan()."""
+        device address per output, in output order; slices as for plan().
+        Its tables go into the library's static device array, shared with
+        every other lazy load and st_materialize_noalloc call: keep them on
+        one stream.  Device flags: static_check()."""
         sel, keep = _selection(names, scale_names, scale_suffix, 0, 0, slices, quant)
         ptrs = (C.c_void_p * max(1, len(dst_ptrs)))(*dst_ptrs)
         nbytes = staging.numel() if hasattr(staging, "numel") else len(staging)
@@ -470,7 +473,13 @@ class StreamStateDict:
 
     paths: shard files; dst: output float dtype; rename/prefix: views;
     scale_suffix / quant: as for Index.plan (quant: name -> (kind, scales,
-    global scale, block))."""
+    global scale, block)).
+
+    Every load runs on torch's current stream and takes its kernel's tables
+    from the library's one static device array, which st_materialize_noalloc
+    uses too: keep every lazy load and allocation-free call of a process on
+    one stream, or they race on that array.  check() reads the device flags
+    the loads left there."""
 
     def __init__(self, paths, dst="BF16", device="cuda", ram_cache_bytes=1 << 30, pinned=True, threads=16,
                  rename=None, prefix=None, scale_suffix=None, quant=None, align=256):
@@ -491,6 +500,12 @@ class StreamStateDict:
 
     def keys(self):
         return list(self._names)
+
+    def check(self):
+        """Device flags of the loads so far (st_static_check on torch's
+        current stream, which it waits for); 0 when every load completed."""
+        import torch
+        return static_check(torch.cuda.current_stream())
 
     def __iter__(self):
         return iter(self._names)
@@ -678,7 +693,10 @@ class Plan:
 
     def materialize_noalloc(self, data, dst_ptrs, scales=None, stream=None):
         """st_materialize_noalloc: as materialize(), with the plan's tables in
-        the library's static device scratch instead of allocated memory."""
+        the library's static device scratch instead of allocated memory (plan
+        with host_only=True).  The scratch is one array shared by every such
+        call and every lazy load: keep them all on one stream.  Device flags
+        are read with static_check()."""
         _check(lib().st_materialize_noalloc(_addr(data), self._h, _addr(dst_ptrs), _addr(scales),
                                             _stream(stream)))
 
@@ -712,6 +730,18 @@ class Plan:
         if code not in (0, 14):
             _check(code)
         return flags.value
+
+
+def static_check(stream=None):
+    """st_static_check: reads and clears the device flags that
+    st_materialize_noalloc and st_load_tensors calls left in the library's
+    static array on the current device (waits for `stream` first); 0 when
+    none (bit 0: bad destination, bit 1: a wait for a staged copy gave up)."""
+    flags = C.c_uint32()
+    code = lib().st_static_check(_stream(stream), C.byref(flags))
+    if code not in (0, 14):
+        _check(code)
+    return flags.value
 
 
 def host_affinity(device=0, apply=True):

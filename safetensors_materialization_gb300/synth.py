@@ -177,6 +177,29 @@ class Workload:
     slices: dict | None = None                   # name -> (dim, start, stop) for sliced loads
     quant: dict | None = None                    # name -> (kind, scales, global scale, block) for block-scaled weights
 
+    def view(self, ix):
+        """The workload's view of an index (library or oracle: both spell
+        view_rename / view_prefix the same way)."""
+        if self.rename:
+            ix = ix.view_rename(self.rename)
+        if self.prefix:
+            ix = ix.view_prefix(self.prefix)
+        return ix
+
+    def selection(self, ix):
+        """Keyword arguments naming the workload's selection of a viewed index:
+        explicit names with slices or block-scale descriptions where it has
+        them, else {} (every entry, in index order)."""
+        if not self.slices and not self.quant:
+            return {}
+        names = [e["name"] for e in ix.entries()]
+        sel = {"names": names}
+        if self.slices:
+            sel["slices"] = [self.slices.get(n) for n in names]
+        if self.quant:
+            sel["quant"] = [self.quant.get(n) for n in names]
+        return sel
+
 
 def tiny(seed=0):
     """16 tensors model.t{i}: shapes from {[64],[256,256],[128,64,3,3],[1024,32]},

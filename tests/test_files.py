@@ -11,6 +11,7 @@ import os
 import numpy as np
 import pytest
 
+from oracle_compare import GuardedOutputs
 from safetensors_materialization_gb300 import synth
 
 
@@ -184,7 +185,7 @@ def test_load_files_matches_oracle(stmat, oracle, tmp_path, chunk, slots):
         C = chunk or total
         ring = torch.empty(C * slots, dtype=torch.uint8).pin_memory() if slots else None
         dev = torch.full((total,), 0xA5, dtype=torch.uint8, device="cuda")
-        outs = stmat.Outputs(plan)
+        outs = GuardedOutputs(plan)
         copy = torch.cuda.Stream()
         plan.load_files(files, dev, outs.ptrs, ring, threads=4, copy_stream=copy,
                         compute_stream=torch.cuda.current_stream())
@@ -197,6 +198,7 @@ def test_load_files_matches_oracle(stmat, oracle, tmp_path, chunk, slots):
         sel = oix.select(dst=dst)
         for i in range(len(sel)):
             assert np.array_equal(outs.raw(i).cpu().numpy(), sel.materialize(i, arena)), sel.output(i)["name"]
+        outs.check_guards()
 
 
 @pytest.mark.gpu
@@ -219,7 +221,7 @@ def test_load_files_ringless_block_scaled_and_errors(stmat, oracle, tmp_path):
         names, q = TB.selection(ix, quant)
         plan = ix.plan(dst="BF16", names=names, quant=q, chunk_bytes=chunk)
         dev = torch.empty(data.size, dtype=torch.uint8, device="cuda")
-        outs = stmat.Outputs(plan)
+        outs = GuardedOutputs(plan)
         plan.load_files(files, dev, outs.ptrs, None, copy_stream=torch.cuda.Stream(),
                         compute_stream=torch.cuda.current_stream())
         files.close()                                      # the copies are done when load_files returns
@@ -228,10 +230,11 @@ def test_load_files_ringless_block_scaled_and_errors(stmat, oracle, tmp_path):
         sel = oix.select(names=names, dst="BF16", quant=q)
         for i in range(len(sel)):
             assert np.array_equal(outs.raw(i).cpu().numpy(), sel.materialize(i, data)), sel.output(i)["name"]
+        outs.check_guards()
     files, ix = stmat.Files.of_checkpoint([path])
     plan = ix.plan(dst="F32")
     dev = torch.empty(data.size, dtype=torch.uint8, device="cuda")
-    outs = stmat.Outputs(plan)
+    outs = GuardedOutputs(plan)
     ring = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
     for args in ((None, 4096), (ring, 0)):
         with pytest.raises(stmat.StmatError) as e:
@@ -257,7 +260,7 @@ def test_load_files_empty_data_sections(stmat, tmp_path):
         files, ix = stmat.Files.of_checkpoint([path])
         assert ix.sizes()[1] == 0
         plan = ix.plan(dst="BF16", chunk_bytes=1 << 20)
-        outs = stmat.Outputs(plan)
+        outs = GuardedOutputs(plan)
         dev = torch.empty(16, dtype=torch.uint8, device="cuda")
         ring = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
         plan.load_files(files, dev, outs.ptrs)
@@ -319,7 +322,7 @@ def test_tensor_parallel_rank_copies_only_its_ranges(stmat, oracle, tmp_path, ch
         want = [sel.materialize(i, arena) for i in range(len(sel))]
         for mode in ("pinned", "ringless", "ring"):
             dev = torch.full((total,), 0xA5, dtype=torch.uint8, device="cuda")
-            outs = stmat.Outputs(plan)
+            outs = GuardedOutputs(plan)
             copy = torch.cuda.Stream()
             cur = torch.cuda.current_stream()
             if mode == "pinned":
@@ -334,6 +337,7 @@ def test_tensor_parallel_rank_copies_only_its_ranges(stmat, oracle, tmp_path, ch
             assert plan.check() == 0
             for i in range(len(want)):
                 assert np.array_equal(outs.raw(i).cpu().numpy(), want[i]), (mode, sel.output(i)["name"])
+            outs.check_guards()
             if rank == 0:
                 assert int(dev[probe_end - 1].item()) == 0xA5, mode   # never copied: the plan does not read it
     files.close()

@@ -1,10 +1,11 @@
 """GPU parity: libstmat's CUDA path against the oracle, byte for byte (0 ULP).
 
 Every test calls the product through the C ABI (ctypes binding) and compares
-with the oracle on the same seeded bytes.  Small cases are compared in full;
-the full-size workloads are compared on windows of every tensor (head, tail
-and seeded random windows) and, at full size, on properties that hold for
-any size (a raw copy equals its source bytes).
+with the oracle on the same seeded bytes, in full (the large workloads are
+compared in full in test_full_parity.py).  Every destination arena is filled
+with a guard value first, and every byte that no output owns (alignment
+padding, gaps between packed outputs, the tail) must still hold it after the
+launch; the device copy of the source must be unchanged.
 """
 import json
 import struct
@@ -13,6 +14,7 @@ import numpy as np
 import pytest
 
 from conftest import golden, small_file
+from oracle_compare import FILL, GuardedOutputs, assert_device_equals_host, assert_guards, compare_full
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -53,12 +55,15 @@ class Packed:
             offs.append(at)
             at += o["bytes"]
         self.offsets = offs
-        self.arena = torch.full((at + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+        self.arena = torch.full((at + 64,), FILL, dtype=torch.uint8, device="cuda")
         self.ptrs = torch.tensor([self.arena.data_ptr() + o for o in offs] or [0], dtype=torch.int64,
                                  device="cuda")
 
     def raw(self, i):
         return self.arena[self.offsets[i]:self.offsets[i] + self.infos[i]["bytes"]]
+
+    def check_guards(self):
+        assert_guards(self.arena, self.offsets, [o["bytes"] for o in self.infos])
 
 
 def run(stmat, image, dst="BF16", view=None, scale_suffix=None, whole=True, offset=0, packed=False,
@@ -69,10 +74,15 @@ def run(stmat, image, dst="BF16", view=None, scale_suffix=None, whole=True, offs
     plan = ix.plan(dst=dst, scale_suffix=scale_suffix, workers=workers, kernel=kernel)
     hlen, dbytes = ix.sizes()
     buf, data_ptr = to_device(image, offset, whole, 8 + hlen)
-    outs = Packed(plan) if packed else stmat.Outputs(plan)
+    outs = Packed(plan) if packed else GuardedOutputs(plan)
     plan.materialize(data_ptr, outs.ptrs, scales=scales)
     torch.cuda.synchronize()
     assert plan.check() == 0
+    outs.check_guards()
+    if whole:
+        assert_device_equals_host(buf[offset:offset + image.size], image)
+    else:
+        assert_device_equals_host(buf[:image.size - 8 - hlen], image[8 + hlen:])
     return plan, outs, buf
 
 
@@ -86,7 +96,10 @@ def oracle_all(oracle, image, dst="BF16", view=None, scale_suffix=None):
 
 
 def assert_same(plan, outs, sel, expected):
+    """Every output equals the oracle's bytes; guard bytes untouched."""
     assert [o["name"] for o in plan.outputs()] == [o["name"] for o in sel.outputs()]
+    if hasattr(outs, "check_guards"):
+        outs.check_guards()
     for i, want in enumerate(expected):
         got = outs.raw(i).cpu().numpy()
         if not np.array_equal(got, want):
@@ -116,7 +129,7 @@ def test_golden_small_file(stmat, oracle, dst):
 def special_image(seed=0):
     """Every f16, bf16 and fp8 bit pattern, a structured f32 sweep, and fp8
     tensors under special scales (2^k, random, subnormal-producing, overflowing,
-    zero, negative)."""
+    zero, negative, NaN, +inf, -inf)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     parts, ents, off = [], {}, 0
 
@@ -137,7 +150,7 @@ def special_image(seed=0):
     add("f32_rand", "F32", rng.integers(0, 1 << 32, size=1 << 18, dtype=np.uint64).astype(np.uint32))
     all8 = np.arange(256, dtype=np.uint8)
     scales = [1.0, 0.5, 2.0 ** -7, 1024.0, 0.0371, float(np.float32(rng.uniform(1e-3, 1e-1))), 3.0e-39,
-              1.7e38, 0.0, -0.25]
+              1.7e38, 0.0, -0.25, float("nan"), float("inf"), float("-inf")]
     for fmt in ("F8_E4M3", "F8_E5M2"):
         add(f"{fmt}.raw.weight", fmt, all8)
         for j, s in enumerate(scales):
@@ -221,7 +234,7 @@ def test_data_section_edges(stmat, oracle):
             for shift in (1, 5, 9, 15):
                 buf = torch.zeros(data.size + 32, dtype=torch.uint8, device="cuda")
                 buf[shift:shift + data.size].copy_(torch.from_numpy(data.copy()))
-                outs = stmat.Outputs(plan)
+                outs = GuardedOutputs(plan)
                 plan.materialize(buf.data_ptr() + shift, outs.ptrs)
                 torch.cuda.synchronize()
                 assert plan.check() == 0
@@ -230,72 +243,31 @@ def test_data_section_edges(stmat, oracle):
 
 # ------------------------------------------------------------- workloads
 
-def window_compare(oracle_sel, plan, outs, data, rng, width=4096, windows=3):
-    """Compares every output on its first and last `width` elements and on
-    seeded random windows."""
-    for i, o in enumerate(plan.outputs()):
-        n = o["numel"]
-        if n == 0:
-            continue
-        isz = o["bytes"] // n
-        starts = {0, max(0, n - width)} | {int(x) for x in rng.integers(0, max(1, n - width), size=windows)}
-        got_all = outs.raw(i)
-        for s in sorted(starts):
-            k = min(width, n - s)
-            want = oracle_sel.materialize_range(i, data, s, k)
-            got = got_all[s * isz:(s + k) * isz].cpu().numpy()
-            assert np.array_equal(got, want), (o["name"], s)
-
-
-def workload_case(stmat, oracle, name, shard=0, dst_index=0, full=False, kernel=0):
+def workload_case(stmat, oracle, name, kernel=0):
+    """A whole workload through run() (guard-banded outputs, source checked
+    unchanged), every element against the oracle on all host cores."""
     from safetensors_materialization_gb300 import synth
     w = synth.WORKLOADS[name]()
-    lay = w.files[shard]
-    img = synth.build_workload_file(w, shard)
-    view = None
-    if w.rename:
-        view = lambda ix: ix.view_rename(w.rename)  # noqa: E731
-    if w.prefix:
-        view = lambda ix: ix.view_prefix(w.prefix)  # noqa: E731
-    dst = w.dst[dst_index]
-    plan, outs, buf = run(stmat, img, dst=dst, view=view, scale_suffix=w.scale_suffix,
+    lay = w.files[0]
+    img = synth.build_workload_file(w, 0)
+    dst = w.dst[0]
+    plan, outs, buf = run(stmat, img, dst=dst, view=w.view, scale_suffix=w.scale_suffix,
                           whole=w.whole_file_on_device, kernel=kernel)
-    oix = oracle.parse(img)
-    if view:
-        oix = view(oix)
-    sel = oix.select(dst=dst, scale_suffix=w.scale_suffix)
+    sel = w.view(oracle.parse_header(lay.header, lay.data_bytes)).select(dst=dst, scale_suffix=w.scale_suffix)
     assert [o["name"] for o in plan.outputs()] == [o["name"] for o in sel.outputs()]
-    data = img[lay.data_start:]
-    if full:
-        assert_same(plan, outs, sel, [sel.materialize(i, data) for i in range(len(sel))])
-    else:
-        window_compare(sel, plan, outs, data, np.random.Generator(np.random.PCG64(11)))
+    assert compare_full(sel, img[lay.data_start:], {f"kernel {kernel}": outs}) == \
+        sum(o["bytes"] for o in sel.outputs())
     return plan, outs, buf, lay, img
 
 
 def test_tiny_workload_full(stmat, oracle):
-    workload_case(stmat, oracle, "tiny", full=True)
+    workload_case(stmat, oracle, "tiny")
 
 
 @pytest.mark.parametrize("kernel", [0, 2])
 def test_stress_workload_full(stmat, oracle, kernel):
     """100k tensors, 7 dtypes, every source 1-15 bytes off 16-byte alignment."""
-    workload_case(stmat, oracle, "stress", full=True, kernel=kernel)
-
-
-@pytest.mark.parametrize("kernel", [0, 3])
-def test_unet_workload(stmat, oracle, kernel):
-    plan, outs, buf, lay, img = workload_case(stmat, oracle, "unet", kernel=kernel)
-    # full size: F16 -> BF16 of N(0, 0.02) data (no NaN) equals torch's cast on every element
-    data = buf[:lay.data_bytes]
-    for i, o in enumerate(plan.outputs()):
-        src = data[o["begin"]:o["begin"] + o["numel"] * 2].view(torch.float16)
-        assert torch.equal(outs.raw(i).view(torch.int16), src.to(torch.bfloat16).view(torch.int16)), o["name"]
-
-
-@pytest.mark.parametrize("kernel", [0, 3])
-def test_scaled_fp8_workload(stmat, oracle, kernel):
-    workload_case(stmat, oracle, "scaled_fp8", kernel=kernel)
+    workload_case(stmat, oracle, "stress", kernel=kernel)
 
 
 def joined(stmat, oracle, w, align=256):
@@ -324,50 +296,12 @@ def test_joined_shards_one_launch(stmat, oracle, align, kernel):
     for dst in ("BF16", "F16", "F32"):
         plan = ix.plan(dst=dst, kernel=kernel)
         assert plan.stats()["chunks"] == 1
-        outs = stmat.Outputs(plan)
+        outs = GuardedOutputs(plan)
         plan.materialize(dev.data_ptr(), outs.ptrs)
         torch.cuda.synchronize()
         assert plan.check() == 0
         sel = oix.select(dst=dst)
         assert_same(plan, outs, sel, [sel.materialize(i, arena) for i in range(len(sel))])
-
-
-@pytest.fixture(scope="module")
-def llm_joined(stmat, oracle):
-    """The full 8B LLM checkpoint: 4 shard files, 16.06 GB, joined."""
-    from safetensors_materialization_gb300 import synth
-    ix, oix, arena = joined(stmat, oracle, synth.llm8b())
-    dev = torch.from_numpy(arena).cuda()
-    yield ix, oix, arena, dev
-    del dev
-    torch.cuda.empty_cache()
-
-
-def test_llm_copy_is_byte_identical(stmat, oracle, llm_joined):
-    """BF16 -> BF16 over all 4 shards in one launch is a raw copy: at full
-    size every output equals its source bytes; windows match the oracle."""
-    ix, oix, arena, dev = llm_joined
-    plan = ix.plan(dst="BF16")
-    outs = stmat.Outputs(plan)
-    plan.materialize(dev.data_ptr(), outs.ptrs)
-    torch.cuda.synchronize()
-    assert plan.check() == 0
-    for i, o in enumerate(plan.outputs()):
-        assert torch.equal(outs.raw(i), dev[o["begin"]:o["begin"] + o["bytes"]]), o["name"]
-    window_compare(oix.select(dst="BF16"), plan, outs, arena, np.random.Generator(np.random.PCG64(12)),
-                   windows=1)
-
-
-def test_llm_cast_to_f16(stmat, oracle, llm_joined):
-    """BF16 -> F16 over all 4 shards in one launch, compared with the oracle on
-    windows of every tensor."""
-    ix, oix, arena, dev = llm_joined
-    plan = ix.plan(dst="F16")
-    outs = stmat.Outputs(plan)
-    plan.materialize(dev.data_ptr(), outs.ptrs)
-    torch.cuda.synchronize()
-    assert plan.check() == 0
-    window_compare(oix.select(dst="F16"), plan, outs, arena, np.random.Generator(np.random.PCG64(13)))
 
 
 # ------------------------------------------------------ pipeline and misc
@@ -385,13 +319,14 @@ def test_load_pipeline_matches_materialize(stmat, oracle, chunk):
     assert plan.stats()["chunks"] == (lay.data_bytes + chunk - 1) // chunk
     host = torch.from_numpy(img[lay.data_start:].copy()).pin_memory()
     dev = torch.empty(lay.data_bytes, dtype=torch.uint8, device="cuda")
-    outs = stmat.Outputs(plan)
+    outs = GuardedOutputs(plan)
     copy = torch.cuda.Stream()
     plan.load(host, dev, outs.ptrs, copy_stream=copy, compute_stream=torch.cuda.current_stream())
     torch.cuda.synchronize()
     assert plan.check() == 0
-    sel, want = oracle_all(oracle, img, dst="BF16")
-    assert_same(plan, outs, sel, want)
+    outs.check_guards()
+    sel = oracle.parse_header(lay.header, lay.data_bytes).select(dst="BF16")
+    assert compare_full(sel, img[lay.data_start:], {f"chunk {chunk}": outs}) == sum(o["bytes"] for o in sel.outputs())
     assert torch.equal(dev.cpu(), host)
 
 
@@ -411,7 +346,7 @@ def test_scale_override(stmat, oracle):
     plan = ix.plan(dst="BF16", scale_suffix=sfx)
     hlen = ix.sizes()[0]
     buf, data_ptr = to_device(img, 0, True, 8 + hlen)
-    outs = stmat.Outputs(plan)
+    outs = GuardedOutputs(plan)
     scales = torch.full((len(plan),), 0.125, dtype=torch.float32, device="cuda")
     plan.materialize(data_ptr, outs.ptrs, scales=scales)
     torch.cuda.synchronize()
@@ -420,6 +355,7 @@ def test_scale_override(stmat, oracle):
             raw = img[8 + hlen + o["begin"]:8 + hlen + o["begin"] + o["numel"]]
             want = oracle.convert(o["src_dtype"], "BF16", raw, scale=0.125)
             assert np.array_equal(outs.raw(i).cpu().numpy(), want), o["name"]
+    outs.check_guards()
 
 
 def test_bad_destinations_are_flagged_and_skipped(stmat, oracle):
@@ -428,7 +364,7 @@ def test_bad_destinations_are_flagged_and_skipped(stmat, oracle):
     ix = stmat.Index.from_file(img)
     plan = ix.plan(dst="BF16")
     buf, data_ptr = to_device(img, 0, True, 8 + ix.sizes()[0])
-    outs = stmat.Outputs(plan)
+    outs = GuardedOutputs(plan)
     outs.arena.fill_(0xA5)
     ptrs = outs.ptrs.clone()
     ptrs[0] = 0                      # NULL destination for "a"
@@ -497,7 +433,7 @@ def test_sliced_outputs(stmat, oracle, kernel):
         want = [sel.materialize(i, data) for i in range(len(sel))]
         plan = ix.plan(dst=dst, names=names, slices=slices, kernel=kernel, unit_bytes=[2048, 32768][trial % 2])
         buf, data_ptr = to_device(img, trial % 16, True, 8 + hlen)
-        outs = Packed(plan) if trial % 3 == 0 else stmat.Outputs(plan)
+        outs = Packed(plan) if trial % 3 == 0 else GuardedOutputs(plan)
         plan.materialize(data_ptr, outs.ptrs)
         torch.cuda.synchronize()
         assert plan.check() == 0
@@ -508,7 +444,7 @@ def test_sliced_outputs(stmat, oracle, kernel):
 def test_tensor_parallel_shard_load(stmat, oracle):
     """Rank 0 of 4 tensor-parallel ranks of an LLM shard file at full size:
     every sliced output equals torch's slice of the source tensor (a byte
-    copy), and windows equal the oracle."""
+    copy) and, every element, the oracle's."""
     from safetensors_materialization_gb300 import synth
     w = synth.llm8b_tp4()
     lay = w.files[0]
@@ -518,7 +454,7 @@ def test_tensor_parallel_shard_load(stmat, oracle):
     slices = [w.slices.get(n) for n in names]
     plan = ix.plan(dst="BF16", names=names, slices=slices)
     buf, data_ptr = to_device(img, 0, False, lay.data_start)
-    outs = stmat.Outputs(plan)
+    outs = GuardedOutputs(plan)
     plan.materialize(data_ptr, outs.ptrs)
     torch.cuda.synchronize()
     assert plan.check() == 0
@@ -532,4 +468,5 @@ def test_tensor_parallel_shard_load(stmat, oracle):
         assert torch.equal(outs.tensor(i).view(torch.int16), src.contiguous().view(torch.int16)), o["name"]
     oix = oracle.parse(img)
     sel = oix.select(dst="BF16", names=names, slices=slices)
-    window_compare(sel, plan, outs, img[lay.data_start:], np.random.Generator(np.random.PCG64(5)), windows=2)
+    outs.check_guards()
+    assert compare_full(sel, img[lay.data_start:], {"tp rank 0": outs}) == sum(o["bytes"] for o in plan.outputs())

@@ -143,6 +143,7 @@ def test_stream_state_dict_loads_every_tensor(stmat, oracle, tmp_path, cache_byt
             torch.cuda.synchronize()
             sel = oix.select(names=[name], dst="BF16")
             assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), name
+    assert sd.check() == 0                                 # no device flag left in the static array
     if cache_bytes:
         st = sd.cache.stats()
         assert st["bytes"] <= cache_bytes
@@ -322,6 +323,7 @@ def test_load_many_matches_oracle(stmat, oracle, tmp_path, cache_bytes):
         for name, t in got.items():
             sel = oix.select(names=[name], dst="F16")
             assert np.array_equal(t.view(torch.uint8).reshape(-1).cpu().numpy(), sel.materialize(0, arena)), name
+        assert sd.check() == 0
     spath, simg, suffix = scaled_fp8_file(tmp_path)
     sds = stmat.StreamStateDict([spath], dst="BF16", scale_suffix=suffix)
     soix = oracle.parse(simg)
@@ -443,3 +445,30 @@ def test_items_in_batches_match_oracle(stmat, oracle, tmp_path):
         sel = oix.select(names=[name], dst="BF16")
         assert np.array_equal(t.reshape(-1).view(torch.uint8).cpu().numpy(), sel.materialize(0, arena)), name
     assert names == sd.keys()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cache_bytes", [0, 1 << 30])
+def test_lazy_batch_into_guarded_arena(stmat, oracle, tmp_path, cache_bytes):
+    """One st_load_tensors call for every tensor of a checkpoint into one
+    guard-banded arena: every output equals the oracle's and no byte outside
+    the outputs is written."""
+    torch = gpu()
+    from oracle_compare import GuardedOutputs
+    w = small_llm()
+    paths = write_shards(tmp_path, w)
+    sd = stmat.StreamStateDict(paths, dst="BF16", ram_cache_bytes=cache_bytes)
+    oix, arena = oracle_joined(oracle, w, paths)
+    names = sd.keys()
+    plan = sd.index.plan(dst="BF16", names=names, workers=1, host_only=True)
+    outs = GuardedOutputs(plan)
+    staging = torch.empty(2 * arena.size + (1 << 20), dtype=torch.uint8, device="cuda")
+    ptrs = [outs.arena.data_ptr() + o for o in outs.offsets]
+    sd.index.load_tensors(sd.files, ptrs, staging, names, dst="BF16", cache=sd.cache,
+                          stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert sd.check() == 0
+    outs.check_guards()
+    sel = oix.select(names=names, dst="BF16")
+    for i in range(len(sel)):
+        assert np.array_equal(outs.raw(i).cpu().numpy(), sel.materialize(i, arena)), names[i]

@@ -158,8 +158,11 @@ def test_fp8_decode_matches_torch(oracle, src):
 def test_fp8_scaled_random_matches_torch(oracle, src, out):
     bits = np.arange(256, dtype=np.uint8)
     rng = np.random.Generator(np.random.PCG64(7))
+    # random scales, a subnormal and a near-overflow one, then the special scales (zero, negative,
+    # NaN and both infinities: IEEE binary32 products, NaN results canonical)
     scales = list(rng.uniform(1e-3, 1e-1, size=24).astype(np.float32)) + [np.float32(3.0e-39),
                                                                             np.float32(1.7e38)]
+    scales += [np.float32(x) for x in (0.0, -0.25, "nan", "inf", "-inf")]
     for s in scales:
         x = torch.from_numpy(bits.copy()).view(FP8[src]).float() * torch.tensor(float(s), dtype=torch.float32)
         got = conv(oracle, src, out, bits, scale=float(s))

@@ -1,12 +1,15 @@
-"""The allocation-free entry point (st_materialize_noalloc) against the
-regular one (st_materialize), through the C ABI.
+"""The allocation-free entry point (st_materialize_noalloc), through the C ABI.
 
-st_materialize_noalloc serves callers that cannot allocate device memory
-(a stream capture that forbids cudaMalloc, or device memory fully held by
-another allocator): the plan is built host-only and its tables go into the
-library's static device scratch.  Its output must equal st_materialize's
-byte for byte (the same tolerance as every parity test here: 0 ULP), also on
-two calls in a row that reuse the scratch with different plans.
+Some callers cannot allocate device memory: a plugin running inside an
+application whose device memory is all held by that application's own pool,
+or code that must not allocate once it runs because cudaMalloc can block and
+fail where nothing can recover.  For them the plan is built host-only and its
+tables go into the library's static device scratch.  Its output must equal
+the regular entry point's (st_materialize) and the oracle's byte for byte
+(the tolerance of every parity test here: 0 ULP) on two calls in a row that
+reuse the scratch with different plans; free device memory must not change
+across a call; the scratch's error word must report a skipped destination
+through st_static_check.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test; it also passes on its own in a fresh process.
@@ -16,6 +19,8 @@ import struct
 
 import numpy as np
 import pytest
+
+from oracle_compare import GuardedOutputs
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -41,7 +46,7 @@ def mixed_image(seed, n):
 
 
 def case(stmat, image, dst, workers, kernel=0):
-    """(device data pointer holder, host-only plan, device plan, outputs for each)."""
+    """(device copy of the image, data pointer, host-only plan, device plan)."""
     ix = stmat.Index.from_file(image)
     hlen, dbytes = ix.sizes()
     buf = torch.empty(image.size + 16, dtype=torch.uint8, device="cuda")
@@ -58,27 +63,58 @@ def _cuda():
         pytest.skip("needs a CUDA GPU")
 
 
-def test_noalloc_matches_materialize_on_two_calls(stmat):
+def test_noalloc_matches_materialize_and_oracle_on_two_calls(stmat, oracle):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     stream = torch.cuda.current_stream()
-    cases = [case(stmat, mixed_image(1, 300), "BF16", sms * 3 * 8),
-             case(stmat, mixed_image(2, 120), "F32", sms * 6 * 8),
-             case(stmat, mixed_image(3, 200), "F16", sms * 2 * 8, kernel=3)]
-    results = []
-    for buf, data, host_plan, dev_plan in cases:
-        outs = stmat.Outputs(host_plan)
-        outs.arena.fill_(0x5A)
-        host_plan.materialize_noalloc(data, outs.ptrs, stream=stream)   # no sync between the two calls
-        results.append(outs)
+    specs = [(mixed_image(1, 300), "BF16", sms * 3 * 8, 0),
+             (mixed_image(2, 120), "F32", sms * 6 * 8, 0),
+             (mixed_image(3, 200), "F16", sms * 2 * 8, 3)]
+    cases = [case(stmat, img, dst, workers, kernel) for img, dst, workers, kernel in specs]
+    # a first call on this device, then every buffer the calls below use
+    warm = GuardedOutputs(cases[0][2])
+    cases[0][2].materialize_noalloc(cases[0][1], warm.ptrs, stream=stream)
+    results = [GuardedOutputs(host_plan) for _, _, host_plan, _ in cases]
     torch.cuda.synchronize()
+    assert stmat.static_check(stream) == 0
+    free0 = torch.cuda.mem_get_info()[0]
     for (buf, data, host_plan, dev_plan), outs in zip(cases, results):
-        ref = stmat.Outputs(dev_plan)
+        host_plan.materialize_noalloc(data, outs.ptrs, stream=stream)   # no sync between the calls
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0, "free device memory changed across the calls"
+    assert stmat.static_check(stream) == 0
+    for (img, dst, _, _), (buf, data, host_plan, dev_plan), outs in zip(specs, cases, results):
+        outs.check_guards()
+        ref = GuardedOutputs(dev_plan)
         dev_plan.materialize(data, ref.ptrs, stream=stream)
         torch.cuda.synchronize()
         assert dev_plan.check() == 0
         assert [o["name"] for o in host_plan.outputs()] == [o["name"] for o in dev_plan.outputs()]
+        oix = oracle.parse(img)
+        sel = oix.select(dst=dst)
+        data_host = img[8 + oix.header_len:]
         for i in range(len(ref.infos)):
             assert torch.equal(outs.raw(i), ref.raw(i)), host_plan.output(i)["name"]
+            assert np.array_equal(outs.raw(i).cpu().numpy(), sel.materialize(i, data_host)), \
+                host_plan.output(i)["name"]
+
+
+def test_noalloc_reports_a_skipped_destination(stmat):
+    """A NULL destination is skipped and its flag stays in the scratch's
+    error word until st_static_check reads (and clears) it; the other
+    outputs are still written."""
+    buf, data, host_plan, dev_plan = case(stmat, mixed_image(5, 40), "BF16", 1024)
+    outs = GuardedOutputs(host_plan)
+    ref = GuardedOutputs(dev_plan)
+    dev_plan.materialize(data, ref.ptrs)
+    ptrs = outs.ptrs.clone()
+    ptrs[3] = 0
+    stream = torch.cuda.current_stream()
+    host_plan.materialize_noalloc(data, ptrs, stream=stream)
+    host_plan.materialize_noalloc(data, outs.ptrs, stream=stream)   # a clean call does not clear it
+    assert stmat.static_check(stream) == 1
+    assert stmat.static_check(stream) == 0
+    for i in range(len(ref.infos)):
+        assert torch.equal(outs.raw(i), ref.raw(i)), host_plan.output(i)["name"]
 
 
 def test_noalloc_rejects_a_plan_larger_than_its_scratch(stmat):
@@ -96,28 +132,3 @@ def test_noalloc_rejects_a_plan_larger_than_its_scratch(stmat):
         big.materialize_noalloc(data, ptrs)
     assert e.value.status == "ST_E_INVAL"
     assert "static scratch" in str(e.value)
-
-
-def test_noalloc_under_stream_capture(stmat):
-    """Captured into a CUDA graph (after a first call outside the capture, as
-    the header asks) and replayed: the outputs equal st_materialize's.  The
-    captured table copies read the plan's host memory when the graph runs."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    buf, data, host_plan, dev_plan = case(stmat, mixed_image(4, 250), "BF16", sms * 3 * 8)
-    outs = stmat.Outputs(host_plan)
-    side = torch.cuda.Stream()
-    with torch.cuda.stream(side):
-        host_plan.materialize_noalloc(data, outs.ptrs, stream=side)
-    torch.cuda.synchronize()
-    ref = stmat.Outputs(dev_plan)
-    dev_plan.materialize(data, ref.ptrs)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        host_plan.materialize_noalloc(data, outs.ptrs, stream=torch.cuda.current_stream())
-    for _ in range(2):
-        outs.arena.fill_(0x5A)
-        graph.replay()
-        torch.cuda.synchronize()
-        for i in range(len(ref.infos)):
-            assert torch.equal(outs.raw(i), ref.raw(i)), host_plan.output(i)["name"]
