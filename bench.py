@@ -150,10 +150,10 @@ def profiled_traffic(workload):
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_sha256") != kernel_sha():
+    r = rec.get("workloads", {}).get(workload)
+    if not r or r.get("kernel_sha256") != kernel_sha():
         return None
-    v = rec.get("traffic_per_launch", {}).get(workload)
-    return int(v) if v else None
+    return int(r["traffic_per_launch"])
 
 
 class ClockSampler:

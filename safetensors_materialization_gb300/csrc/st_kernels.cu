@@ -119,21 +119,22 @@ __device__ __forceinline__ float2 decode2(const uint32_t (&s)[NS], int j) {
 }
 
 // Two binary32 -> one packed 16-bit pair (lower address in the low half).
+// A converted half is NaN exactly when its input was (rounding keeps
+// infinities and never makes a NaN), so one packed unordered compare of the
+// result with itself marks the NaN halves, which become the canonical NaN.
 template <int D>
 __device__ __forceinline__ uint32_t encode2_16(float2 f) {
-  uint32_t r;
+  uint32_t r, m;
   if constexpr (D == D_BF16) {
     __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
     r = *reinterpret_cast<uint32_t *>(&v);
-    const uint32_t lo = f.x != f.x ? kNanBF16 : (r & 0xFFFFu);
-    const uint32_t hi = f.y != f.y ? kNanBF16 : (r >> 16);
-    return lo | (hi << 16);
+    m = __hneu2_mask(v, v);
+    return (r & ~m) | (m & (kNanBF16 | (kNanBF16 << 16)));
   } else {
     __half2 v = __floats2half2_rn(f.x, f.y);
     r = *reinterpret_cast<uint32_t *>(&v);
-    const uint32_t lo = f.x != f.x ? kNanF16 : (r & 0xFFFFu);
-    const uint32_t hi = f.y != f.y ? kNanF16 : (r >> 16);
-    return lo | (hi << 16);
+    m = __hneu2_mask(v, v);
+    return (r & ~m) | (m & (kNanF16 | (kNanF16 << 16)));
   }
 }
 

@@ -21,11 +21,12 @@ def test_traffic_record_parses_and_names_known_workloads():
     names = {f().name for f in synth.WORKLOADS.values()}
     with open(bench.TRAFFIC) as f:
         rec = json.load(f)
-    assert set(rec) >= {"kernel_sha256", "command", "traffic_per_launch"}
-    assert len(rec["traffic_per_launch"]) >= 8
-    for w, v in rec["traffic_per_launch"].items():
+    assert set(rec) >= {"command", "workloads"}
+    assert len(rec["workloads"]) >= 8
+    for w, r in rec["workloads"].items():
         assert w in names, w
-        assert isinstance(v, int) and v > 0, w
+        assert set(r) == {"kernel_sha256", "traffic_per_launch"}, w
+        assert isinstance(r["traffic_per_launch"], int) and r["traffic_per_launch"] > 0, w
 
 
 def test_headline_workload_has_traffic_for_the_current_kernel():
