@@ -310,7 +310,11 @@ st_status st_plan_copy_bytes(const st_plan_t *plan, uint64_t *bytes, uint32_t *r
 st_status st_plan_piece(const st_plan_t *plan, uint64_t k, uint64_t *src, uint64_t *dst,
                         uint64_t *scale, uint32_t *count, uint32_t *output, uint32_t *cls,
                         uint32_t *rows, uint64_t *pitch);
-/* Pieces of worker w in chunk c: [first, last). */
+/* Pieces of worker w < workers in chunk c: [first, last), the warp's own
+ * share; w == workers gives the chunk's claimed pieces, which the TMA builds'
+ * warps take in source order while the kernel runs, whichever warp is free
+ * (empty for the streaming builds).  The ranges of w = 0 .. workers cover the
+ * chunk's pieces once. */
 st_status st_plan_worker(const st_plan_t *plan, uint32_t chunk, uint32_t w, uint64_t *first,
                          uint64_t *last);
 
@@ -393,7 +397,11 @@ st_status st_device_reads_pageable(int device, int32_t *yes);
  *             outputs are ignored).  With NULL, fp8 outputs use their paired
  *             scale tensor's value from the data section, or 1.0.
  * Errors: ST_E_INVAL (NULL plan/data/dst_ptrs, host-only plan), ST_E_CUDA
- * (launch failure).  Outputs may not overlap each other or the data section. */
+ * (launch failure).  Outputs may not overlap each other or the data section.
+ * Launches of one plan (this call, st_load, st_load_files) must not overlap
+ * on the GPU: the TMA builds' warps claim pieces through two words the plan
+ * owns, which each launch leaves at zero for the next (order them on one
+ * stream, or with events). */
 st_status st_materialize(const void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
                          const float *scales, void *stream);
 
@@ -534,7 +542,8 @@ st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t
  *     (cudaMemcpyAsync from the plan's host memory) into one static device
  *     array of 4 MiB built into the library.  Every GPU that loads the
  *     library holds those 4 MiB until the process exits.  The tables may take
- *     4 MiB - 256 bytes (the last 256 hold the error word): 48 bytes per
+ *     4 MiB - 256 bytes (the last 256 hold the error word and the claim
+ *     words of the TMA builds, which every launch leaves at zero): 48 bytes per
  *     piece, plus 4 bytes per warp and chunk (plus 4 per chunk), plus 32
  *     bytes per output for block-scaled plans, each part rounded up to 256
  *     bytes (st_load_tensors adds 8 bytes per output for its destination

@@ -95,6 +95,12 @@ struct LaunchArgs {
   const float *scales;     // device array of per-output scales, or nullptr
   uint32_t *err;           // device error word
   const QuantInfo *quant;  // device array indexed by output (block-scaled outputs), or nullptr
+  // TMA builds: pieces [parts[workers], claim_end) are claimed while the
+  // launch runs, in source order, through two device words that are zero
+  // before the launch (pieces claimed, warps done); the last warp to finish
+  // sets them back to zero.
+  uint32_t claim_end;
+  uint32_t *claim;
 };
 
 // Bytes written per counted unit of a class.
@@ -144,6 +150,7 @@ constexpr uint32_t kKernelStream = 1;
 constexpr uint32_t kKernelLatency = 2;
 constexpr uint32_t kKernelTma = 3;
 constexpr uint32_t kKernelTmaWide = 4;  // the TMA build with fewer slots per warp and more warps per SM
+constexpr bool is_tma_build(uint32_t variant) { return variant == kKernelTma || variant == kKernelTmaWide; }
 
 // Resident 256-thread blocks per SM for a kernel build, and the SM count of
 // the current device.
@@ -158,6 +165,7 @@ st_status launch_materialize(const LaunchArgs &a, uint32_t variant, void *stream
 // st_static_check reads and clears it.  The tables take the bytes before.
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;
 constexpr size_t kStaticErrOffset = kStaticScratchBytes - 256;
+constexpr size_t kStaticClaimOffset = kStaticErrOffset + 64;
 st_status static_scratch(void **addr);
 
 // Shard-file reads (st_io.cpp): arena bytes [begin, begin + bytes) into host.

@@ -539,7 +539,13 @@ __global__ void __launch_bounds__(kThreads, ST_LAT_MIN_BLOCKS) materialize_laten
 //    window's byte offset, converts, and stores one 16- or 8-byte vector;
 //    elements before the first aligned destination vector or after the
 //    last are converted one by one from shared memory.
-//  - Piece descriptors arrive the same way, 32 at a time, one batch ahead.
+//  - Piece descriptors arrive the same way, up to 32 at a time, one batch
+//    ahead: first the warp's own pieces (its interleaved units), then pieces
+//    of the plan's claimed tail, taken in source order from the launch's
+//    claim word (a warp asks for the batch after next as it enters a batch,
+//    so the answer is there when needed), so warps that run fast take more
+//    and all finish together.  The last warp to finish zeroes the claim
+//    words for the next launch.
 //  - One warp is both producer and consumer, so a slot is refilled only
 //    after the warp has finished reading it (program order, __syncwarp and
 //    a proxy fence).  Every wait is bounded: a wait that gives up sets
@@ -567,6 +573,9 @@ constexpr uint32_t kSeg = ST_TMA_SEG;
 constexpr uint32_t kBatch = 32;  // piece descriptors fetched per bulk copy (one per lane)
 constexpr uint32_t kSlotBytes = kSeg + 32;  // a clipped window is at most kSeg + 16 bytes
 constexpr uint32_t kSpinLimit = 1u << 22;
+// A claim takes about (pieces left to claim) / (kClaimSpread * warps) pieces,
+// at least one and at most kBatch: larger claims early, single pieces at the end.
+constexpr uint32_t kClaimSpread = 8;
 static_assert(kSeg % 16 == 0 && kSeg >= 64, "segment size");
 
 // One staged segment: a run of one piece, elements [0, len); elements
@@ -985,22 +994,72 @@ struct Cursor {
 // aligned interior, so its segments skip the clipping arithmetic (measured:
 // +2 % on many small tensors with the 4-slot shape; -1..3 % on the
 // register-capped wide shape, which keeps the general path).
+// The last warp of a launch to finish zeroes its claim words (every warp has
+// made its last claim by then).
+__device__ __forceinline__ void release_claims(const LaunchArgs &a, uint32_t lane) {
+  if (lane == 0) {
+    __threadfence();
+    if (atomicAdd(a.claim + 1, 1u) == a.workers - 1) {
+      atomicExch(a.claim, 0u);
+      atomicExch(a.claim + 1, 0u);
+    }
+  }
+}
+
 template <int kSlots, bool kInterior>
 __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   const uint32_t lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const uint32_t w = blockIdx.x * kWarpsPerBlock + wib;
   if (w >= a.workers) return;
-  const uint32_t p0 = a.parts[w], p1 = a.parts[w + 1];
-  if (p0 >= p1) return;
   WarpSmem<kSlots> &ws = reinterpret_cast<WarpSmem<kSlots> *>(smem)[wib];
-  const uint32_t nbatch = (p1 - p0 + kBatch - 1) / kBatch;
+  // The warp's own pieces [p0, p1), then pieces of the claimed tail
+  // [dyn0, dyn0 + dtotal), in batches of at most kBatch.
+  const uint32_t p0 = a.parts[w], p1 = a.parts[w + 1];
+  const uint32_t dyn0 = a.parts[a.workers], dtotal = a.claim_end - dyn0;
+  const uint32_t spread = kClaimSpread * a.workers;
+  uint32_t sp = p0;                // the next own piece not yet in a batch
+  bool claiming = false;           // a claim has been made and not yet taken
+  uint32_t next_at = 0, next_k = 0;  // lane 0: that claim
+  auto start_claim = [&](uint32_t from) {  // claim about (left) / spread pieces, from = claimed so far
+    if (lane == 0) {
+      const uint32_t left = from < dtotal ? dtotal - from : 0;
+      next_k = max(1u, min(kBatch, left / spread));
+      next_at = atomicAdd(a.claim, next_k);
+    }
+    claiming = true;
+  };
+  // The next batch: own pieces first; the claim for the tail's first batch
+  // goes out with the last own batch, and each claimed batch makes the next
+  // claim, so a claim's answer is read one batch after it was asked for.
+  auto next_batch = [&](uint32_t &start) -> uint32_t {
+    if (sp < p1) {
+      start = sp;
+      const uint32_t n = min(kBatch, p1 - sp);
+      sp += n;
+      if (sp == p1 && dtotal) start_claim(0);
+      return n;
+    }
+    if (!claiming) return 0;
+    claiming = false;
+    const uint32_t at = __shfl_sync(0xFFFFFFFFu, next_at, 0), k = __shfl_sync(0xFFFFFFFFu, next_k, 0);
+    if (at >= dtotal) return 0;
+    start = dyn0 + at;
+    start_claim(at + k);
+    return min(k, dtotal - at);
+  };
+  if (p0 == p1 && dtotal) start_claim(0);
+  uint32_t bs0 = 0, bs1 = 0, bn0 = 0, bn1 = 0;  // the batches in the two descriptor slots
+  bn0 = next_batch(bs0);
+  if (bn0 == 0) {
+    release_claims(a, lane);
+    return;
+  }
   const uintptr_t lo16 = (reinterpret_cast<uintptr_t>(a.data) + 15) & ~uintptr_t(15);
   const uintptr_t hi16 = (reinterpret_cast<uintptr_t>(a.data) + a.data_bytes) & ~uintptr_t(15);
 
   auto issue_desc = [&](uint32_t bb) {  // lane 0
-    const uint32_t cnt = min(kBatch, p1 - p0 - kBatch * bb);
-    bulk_load(ws.desc[bb & 1], a.pieces + p0 + kBatch * bb, cnt * static_cast<uint32_t>(sizeof(Piece)),
-              &ws.dbar[bb & 1]);
+    bulk_load(ws.desc[bb & 1], a.pieces + ((bb & 1) ? bs1 : bs0),
+              ((bb & 1) ? bn1 : bn0) * static_cast<uint32_t>(sizeof(Piece)), &ws.dbar[bb & 1]);
   };
   if (lane == 0) {
     for (int k = 0; k < kSlots; ++k) mbar_init(&ws.bar[k]);
@@ -1010,6 +1069,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
     issue_desc(0);
   }
   uint32_t dissued = 1, dseen = 0;  // descriptor batches fetched / waited for
+  bool later = true;                // a batch follows the one entered last (known once it is entered)
   __syncwarp();
 
   // Waits for descriptor batch b, resolves its destinations and scales, and
@@ -1017,7 +1077,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   auto enter_batch = [&](uint32_t b) -> bool {
     if (!mbar_wait(&ws.dbar[b & 1], (b >> 1) & 1)) return false;
     dseen = b + 1;
-    const uint32_t cnt = min(kBatch, p1 - p0 - kBatch * b);
+    const uint32_t cnt = (b & 1) ? bn1 : bn0;
     if (lane < cnt) {
       const Piece &pc = ws.desc[b & 1][lane];
       const uint32_t out = pc.out_cls >> kClsBits, cls = pc.out_cls & ((1u << kClsBits) - 1);
@@ -1038,7 +1098,17 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
       ws.scl[b & 1][lane] = scale;
     }
     __syncwarp();
-    if (b + 1 < nbatch) {
+    uint32_t st = 0;
+    const uint32_t n = next_batch(st);
+    later = n > 0;
+    if (later) {
+      if ((b + 1) & 1) {
+        bs1 = st;
+        bn1 = n;
+      } else {
+        bs0 = st;
+        bn0 = n;
+      }
       if (lane == 0) {
         proxy_fence();
         issue_desc(b + 1);
@@ -1051,7 +1121,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   // The piece being cut into segments: its fields are loaded once, when the
   // cursor reaches it, and the run's source/output addresses advance by the
   // pitch / run size, so a segment costs no divisions or multiplications.
-  Cursor cur{0, 0, 0, min(kBatch, p1 - p0), 0};
+  Cursor cur{0, 0, 0, bn0, 0};
   const uint8_t *run_src = nullptr;  // source of the current run's element 0
   uint8_t *run_dst = nullptr;        // output address of the current run's element 0
   uint64_t pitch = 0;
@@ -1092,12 +1162,13 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   auto produce = [&](int slot) -> int {  // 1 issued, 0 done, -1 timed out
     for (;;) {
       if (cur.i == cur.n) {
-        if (++cur.b == nbatch) return 0;
+        if (!later) return 0;
+        ++cur.b;
         cur.i = 0;
         cur.r = 0;
         cur.e = 0;
-        cur.n = min(kBatch, p1 - p0 - kBatch * cur.b);
         if (!enter_batch(cur.b)) return -1;
+        cur.n = (cur.b & 1) ? bn1 : bn0;
         continue;
       }
       if (!loaded) {
@@ -1231,6 +1302,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
     for (; jc < jp; ++jc) mbar_wait(&ws.bar[jc % kSlots], (jc / kSlots) & 1);
     for (; dseen < dissued; ++dseen) mbar_wait(&ws.dbar[dseen & 1], (dseen >> 1) & 1);
   }
+  release_claims(a, lane);
 }
 
 __global__ void __launch_bounds__(kThreads, ST_TMA_MIN_BLOCKS) materialize_tma(const LaunchArgs a) {

@@ -277,7 +277,7 @@ def test_chunked_plans_wait_for_block_scales(stmat, chunk):
     outs = plan.outputs()
     st = plan.stats()
     for c in range(st["chunks"]):
-        for w in range(st["workers"]):
+        for w in range(st["workers"] + 1):   # own shares and the claimed pieces
             a, b = plan.worker(c, w)
             for k in range(a, b):
                 p = plan.piece(k)

@@ -252,7 +252,7 @@ def test_pieces_cover_outputs_once(stmat, wl, workers, chunk):
     cls_of = {}
     for chunk_i in range(st["chunks"]):
         prev = None
-        for wk in range(st["workers"]):
+        for wk in range(st["workers"] + 1):    # the warps' own shares, then the claimed pieces
             a, b = plan.worker(chunk_i, wk)
             assert prev is None or a == prev   # workers' ranges are consecutive
             prev = b

@@ -246,15 +246,17 @@ def check_plan(plan, data_base, dst_align, data_bytes):
         for r in range(p["rows"]):
             check_run(p, r, bases, outs, data_base, lo, hi)
     for c in range(st["chunks"]):
-        for w in range(st["workers"]):
+        # each warp's own share, then the claimed pieces (any warp may take a
+        # claimed batch; the windows depend on the piece alone)
+        for w in range(st["workers"] + 1):
             a, b = plan.worker(c, w)
             tma_warp(plan, pieces[a:b], bases, data_base, lo, hi)
     # grid: blocks of 8 warps cover every worker; parts arrays have workers + 1 entries
     blocks = (st["workers"] + 7) // 8
     assert blocks * 8 >= st["workers"]
     for c in range(st["chunks"]):
-        a, b = plan.worker(c, st["workers"] - 1)
-        assert b <= st["pieces"]
+        a, b = plan.worker(c, st["workers"])
+        assert plan.worker(c, st["workers"] - 1)[1] == a and b <= st["pieces"]
 
 
 def check_run(p, r, bases, outs, data_base, lo, hi):
@@ -413,6 +415,6 @@ def test_blockscaled_plans_in_bounds(stmat, lead):
                     at = (at + 255) // 256 * 256 + ({"BF16": 2, "F32": 4}[dst] if odd else 0)
                     bases.append(at)
                     at += o["bytes"]
-                for w in range(st["workers"]):
+                for w in range(st["workers"] + 1):
                     a, b = plan.worker(0, w)
                     tma_warp(plan, pieces[a:b], bases, base, base, base + dbytes, quant=qinfo)
