@@ -10,11 +10,14 @@
 //
 // Design (HBM-bound; no tensor cores, there is no contraction):
 //  - the planner cut outputs into pieces and balanced them by bytes over W
-//    warps; warp w walks pieces [parts[w], parts[w+1]) with no inter-warp
-//    synchronization and no waits, so the kernel cannot stall on a peer.  A
-//    warp stages up to 32 piece descriptors at a time in shared memory (one
-//    per lane), with their destination pointers and scales, so the dependent
-//    loads of a piece are paid once per 32 pieces;
+//    warps; warp w walks its own pieces [parts[w], parts[w+1]) with no
+//    inter-warp synchronization and no waits, so the kernel cannot stall on a
+//    peer, then claims pieces of the plan's tail [parts[W], claim_end) in
+//    source order from a claim word (warps that ran fast take more, so all
+//    finish together; the last one out zeroes the word).  A warp stages up to
+//    32 piece descriptors at a time in shared memory (one per lane), with
+//    their destination pointers and scales, so the dependent loads of a piece
+//    are paid once per 32 pieces;
 //  - each lane moves one 16-byte source chunk per step (K = 16 / itemsize
 //    elements) with 16-byte vector loads; consecutive lanes take consecutive
 //    chunks, so every warp access is one contiguous run; a batch of up to 4
@@ -454,6 +457,11 @@ struct Staged {
   float scale[32];
 };
 
+__device__ __forceinline__ void release_claims(const LaunchArgs &a, uint32_t lane);
+// A claim takes about (pieces left to claim) / (kClaimSpread * warps) pieces,
+// at least one and at most 32: larger claims early, single pieces at the end.
+constexpr uint32_t kClaimSpread = 8;
+
 template <class Cfg>
 __device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
   __shared__ Staged stage[kWarpsPerBlock];
@@ -462,9 +470,37 @@ __device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
   const uint32_t w = blockIdx.x * kWarpsPerBlock + wib;
   if (w >= a.workers) return;
   const uint32_t p0 = a.parts[w], p1 = a.parts[w + 1];
+  const uint32_t dyn0 = a.parts[a.workers], dtotal = a.claim_end - dyn0;
+  const uint32_t spread = kClaimSpread * a.workers;
   Staged &st = stage[wib];
-  for (uint32_t base = p0; base < p1; base += 32) {
-    const uint32_t n = min(32u, p1 - base);
+  // Own pieces [p0, p1) in batches of 32, then batches claimed from the tail
+  // [dyn0, dyn0 + dtotal); each claim is asked for one batch ahead.
+  uint32_t next_at = 0, next_k = 0;  // lane 0: the claim in flight
+  bool claiming = false;
+  auto start_claim = [&](uint32_t from) {
+    if (lane == 0) {
+      const uint32_t left = from < dtotal ? dtotal - from : 0;
+      next_k = max(1u, min(32u, left / spread));
+      next_at = atomicAdd(a.claim, next_k);
+    }
+    claiming = true;
+  };
+  uint32_t base = p0;
+  if (p0 == p1 && dtotal) start_claim(0);
+  for (;;) {
+    uint32_t n;
+    if (base < p1) {
+      n = min(32u, p1 - base);
+      if (base + n == p1 && dtotal) start_claim(0);
+    } else {
+      if (!claiming) break;
+      claiming = false;
+      const uint32_t at = __shfl_sync(0xFFFFFFFFu, next_at, 0), k = __shfl_sync(0xFFFFFFFFu, next_k, 0);
+      if (at >= dtotal) break;
+      base = dyn0 + at;
+      n = min(k, dtotal - at);
+      start_claim(at + k);
+    }
     // Lane i fetches piece base+i, then its destination and scale: two
     // dependent round trips shared by up to 32 pieces.
     __syncwarp();
@@ -509,7 +545,9 @@ __device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
           if (lane == 0) atomicOr(a.err, kErrBadDst);
       }
     }
+    base += n;
   }
+  release_claims(a, lane);
 }
 
 __global__ void __launch_bounds__(kThreads) materialize_stream(const LaunchArgs a) { materialize_body<StreamCfg>(a); }
@@ -573,9 +611,6 @@ constexpr uint32_t kSeg = ST_TMA_SEG;
 constexpr uint32_t kBatch = 32;  // piece descriptors fetched per bulk copy (one per lane)
 constexpr uint32_t kSlotBytes = kSeg + 32;  // a clipped window is at most kSeg + 16 bytes
 constexpr uint32_t kSpinLimit = 1u << 22;
-// A claim takes about (pieces left to claim) / (kClaimSpread * warps) pieces,
-// at least one and at most kBatch: larger claims early, single pieces at the end.
-constexpr uint32_t kClaimSpread = 8;
 static_assert(kSeg % 16 == 0 && kSeg >= 64, "segment size");
 
 // One staged segment: a run of one piece, elements [0, len); elements

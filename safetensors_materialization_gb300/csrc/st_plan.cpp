@@ -41,11 +41,14 @@ constexpr uint64_t kPieceCost = 1024;       // fixed cost of a piece, in bytes o
 constexpr uint64_t kMinWorkerCost = 4096;   // no more warps than total cost / this
 constexpr uint64_t kMaxPieceUnits = 1ull << 30;
 constexpr uint64_t kDefaultUnitBytes = 32768;  // cost of one interleaved unit
-// Percent of the units (whole rounds) that the TMA builds' warps claim while
-// they run instead of owning them (measured best: 100k tiny tensors 15 %,
-// 0.851 -> 0.876 of the copy peak; block-scaled weights on the wide build
-// 40 %, block FP8 0.896 -> 0.974, NVFP4 0.843 -> 0.965).
-constexpr uint64_t kClaimedPct = 15, kClaimedPctWide = 40;
+// Percent of the units (whole rounds) that warps claim while they run instead
+// of owning them, by build (measured best, fractions of the copy peak):
+// TMA, 100k tiny tensors 15 % (0.851 -> 0.876); wide TMA, block-scaled
+// weights 40 % (block FP8 0.896 -> 0.974, NVFP4 0.843 -> 0.965); streaming,
+// long contiguous runs 20 % (scaled FP8 0.972 -> 0.992, LLM 0.968 -> 1.02,
+// UNet 0.971 -> 0.977).  Short runs on the streaming build (tensor-parallel
+// slices, 3 blocks per SM) measured 0.923 -> 0.915 with any tail: none.
+constexpr uint64_t kClaimedPct = 15, kClaimedPctWide = 40, kClaimedPctStream = 20;
 constexpr uint64_t kLazyBytesPerWarp = 16384;  // st_load_tensors: traffic per warp
 constexpr uint64_t kLazyMaxWarps = 2432;        // ... and at most this many warps (2 blocks on each of 152 SMs)
 constexpr uint32_t kStreamBlocksPerSm = 3;     // streaming build: fewer, deeper warps ...
@@ -126,6 +129,7 @@ struct st_plan_s {
   uint64_t chunk_bytes = 0;
   uint64_t unit_bytes = kDefaultUnitBytes;
   bool class_major = false;
+  bool long_runs = false;  // the outputs' contiguous runs average kLongRunBytes or more
   uint32_t n_chunks = 1;
   // Data-section byte ranges the plan reads (sorted, merged); `sparse` when
   // they cover under three quarters of it (a tensor-parallel rank's load):
@@ -588,14 +592,17 @@ void build_pieces(st_plan_s *p) {
     const uint64_t N = rounds * W;
     cut_units(*p, segs, N, total, &units, &ub);
     uint32_t *parts = &p->parts[static_cast<size_t>(k) * (W + 1)];
-    // The TMA builds leave the last rounds' units to be claimed while the
-    // kernel runs (in source order, by whichever warps are free): with fixed
+    // The last rounds' units are claimed while the kernel runs (in source
+    // order, by whichever warps are free) instead of dealt: with fixed
     // shares the warps' finishing times spread by where they run more than
     // by their shares (measured on 100k tiny tensors: blocks' mean end times
     // 155-179 us, the last warp 14 % after the median, each warp's end time
     // repeatable to 0.5 us).
-    const uint64_t pct = p->kernel == kKernelTmaWide ? kClaimedPctWide : kClaimedPct;
-    const uint64_t dyn_rounds = is_tma_build(p->kernel) && rounds >= 2 ? std::max<uint64_t>(1, rounds * pct / 100) : 0;
+    const uint64_t pct = p->kernel == kKernelTmaWide ? kClaimedPctWide
+                         : is_tma_build(p->kernel)   ? kClaimedPct
+                         : p->kernel == kKernelStream && p->long_runs ? kClaimedPctStream
+                                                                      : 0;
+    const uint64_t dyn_rounds = rounds >= 2 && pct ? std::max<uint64_t>(1, rounds * pct / 100) : 0;
     const uint64_t Ns = (rounds - dyn_rounds) * W;
     for (uint32_t w = 0; w < W; ++w) {
       parts[w] = static_cast<uint32_t>(p->pieces.size());
@@ -702,7 +709,12 @@ st_status plan_host(std::shared_ptr<const IndexData> index, const st_selection *
   // per-class code is large, and mixing classes stalls on instruction
   // fetch); the TMA build's code is small, and source order keeps DRAM
   // rows local.
-  p->class_major = order == 2 || (order == 0 && p->kernel != kKernelTma && p->kernel != kKernelTmaWide);
+  p->class_major = order == 2 || (order == 0 && !is_tma_build(p->kernel));
+  {
+    uint64_t runs = 0;
+    for (const Output &o : p->outs) runs += o.units ? o.runs : 0;
+    p->long_runs = runs && traffic / runs >= kLongRunBytes;
+  }
   int sms = 0, blocks = 0;
   if (!host_only || workers == 0) {
     if (host_only) return set_error(ST_E_INVAL, "a host-only plan needs options.workers");
@@ -714,10 +726,7 @@ st_status plan_host(std::shared_ptr<const IndexData> index, const st_selection *
       // Measured: long contiguous runs (whole large tensors) stream best at 2
       // blocks per SM (scaled FP8 91.7 -> 95.6 %, 4-shard LLM 96.9 -> 98.0 %);
       // many short runs (row-sliced tensor-parallel shards) at 3.
-      uint64_t runs = 0;
-      for (const Output &o : p->outs) runs += o.units ? o.runs : 0;
-      const bool long_runs = runs && traffic / runs >= kLongRunBytes;
-      bps = std::min(bps, long_runs ? kStreamBlocksPerSmLong : kStreamBlocksPerSm);
+      bps = std::min(bps, p->long_runs ? kStreamBlocksPerSmLong : kStreamBlocksPerSm);
     }
     if (workers == 0) workers = static_cast<uint32_t>(sms) * bps * kWarpsPerBlock;
   }
