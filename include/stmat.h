@@ -304,12 +304,24 @@ st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chun
  * output's source extent and its scales, merged across gaps under 64 KiB),
  * in *ranges pieces (may be NULL). */
 st_status st_plan_copy_bytes(const st_plan_t *plan, uint64_t *bytes, uint32_t *ranges);
+/* Range i < *ranges of st_plan_copy_bytes: data-section bytes [begin, end),
+ * ascending and disjoint (more than 64 KiB apart).  ST_E_INVAL for i out of
+ * range. */
+st_status st_plan_copy_range(const st_plan_t *plan, uint32_t i, uint64_t *begin, uint64_t *end);
 /* Piece k (host copy): `rows` runs of `count` counted units; run r reads
  * from data-section offset src + r * pitch and writes output bytes from
  * dst + r * count * out_itemsize; scale offset (or ~0), output, class. */
 st_status st_plan_piece(const st_plan_t *plan, uint64_t k, uint64_t *src, uint64_t *dst,
                         uint64_t *scale, uint32_t *count, uint32_t *output, uint32_t *cls,
                         uint32_t *rows, uint64_t *pitch);
+/* Conversion class `cls` (st_plan_piece's class, 0 .. 21): bytes per counted
+ * unit read (src_item) and written (out_item), and one lane step of the
+ * kernels' vector bodies: step_src source bytes, step_units counted units,
+ * step_out output bytes (one 16- or 8-byte vector).  The kernels' codecs are
+ * checked against these when the library is compiled.  Any pointer may be
+ * NULL; ST_E_INVAL for an unknown class. */
+st_status st_class_step(uint32_t cls, uint32_t *src_item, uint32_t *out_item, uint32_t *step_src,
+                        uint32_t *step_units, uint32_t *step_out);
 /* Pieces of worker w < workers in chunk c: [first, last), the warp's own
  * share; w == workers gives the chunk's claimed pieces, which the TMA builds'
  * warps take in source order while the kernel runs, whichever warp is free

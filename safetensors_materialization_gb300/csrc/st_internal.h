@@ -143,6 +143,20 @@ constexpr uint64_t kInShifts = pack_shifts(false), kOutShifts = pack_shifts(true
 ST_HD constexpr uint32_t cls_in_shift(uint32_t c) { return static_cast<uint32_t>(kInShifts >> (2 * c)) & 3u; }
 ST_HD constexpr uint32_t cls_out_shift(uint32_t c) { return static_cast<uint32_t>(kOutShifts >> (2 * c)) & 3u; }
 
+// A lane step of a class in the kernels' vector bodies reads cls_step_src
+// source bytes (cls_step_units counted units) and writes cls_step_out bytes,
+// one 16- or 8-byte vector: widening classes read fewer source bytes.
+// Block-scaled classes step over 8 fp8 bytes (4 for F32 outputs) or 4 NVFP4
+// bytes.  The kernels' codec types are checked against these at compile time.
+ST_HD constexpr uint32_t cls_step_src(uint32_t c) {
+  return cls_nvfp4(c)   ? 4u
+         : cls_quant(c) ? (cls_out_size(c) == 4 ? 4u : 8u)
+         : cls_out_size(c) > cls_in_size(c) ? static_cast<uint32_t>(16 * cls_in_size(c) / cls_out_size(c))
+                                            : 16u;
+}
+ST_HD constexpr uint32_t cls_step_units(uint32_t c) { return cls_step_src(c) / cls_in_size(c); }
+ST_HD constexpr uint32_t cls_step_out(uint32_t c) { return cls_step_units(c) * cls_out_size(c); }
+
 // Kernel builds (st_kernels.cu): deep unroll for large tensors, higher
 // occupancy for many small tensors, or source bytes staged in shared memory
 // by the bulk-copy (TMA) engine.

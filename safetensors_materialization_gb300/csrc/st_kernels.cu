@@ -991,6 +991,26 @@ __device__ __forceinline__ void consume_quant(const uint8_t *buf, const SegMeta 
   }
 }
 
+// The codec types' lane steps are the ones the host describes (cls_step_*).
+template <class CV, uint32_t C>
+constexpr bool step_is() {
+  return CV::SB == cls_step_src(C) && CV::KS == cls_step_units(C) && CV::OS == cls_step_out(C);
+}
+static_assert(step_is<CopyBytes, CLS_COPY>() && step_is<Conv<S_F32, D_BF16>, CLS_F32_BF16>() &&
+                  step_is<Conv<S_F32, D_F16>, CLS_F32_F16>() && step_is<Conv<S_F16, D_BF16>, CLS_F16_BF16>() &&
+                  step_is<Conv<S_F16, D_F32>, CLS_F16_F32>() && step_is<Conv<S_BF16, D_F16>, CLS_BF16_F16>() &&
+                  step_is<Conv<S_BF16, D_F32>, CLS_BF16_F32>() && step_is<Conv<S_E4M3, D_BF16>, CLS_E4M3_BF16>() &&
+                  step_is<Conv<S_E4M3, D_F16>, CLS_E4M3_F16>() && step_is<Conv<S_E4M3, D_F32>, CLS_E4M3_F32>() &&
+                  step_is<Conv<S_E5M2, D_BF16>, CLS_E5M2_BF16>() && step_is<Conv<S_E5M2, D_F16>, CLS_E5M2_F16>() &&
+                  step_is<Conv<S_E5M2, D_F32>, CLS_E5M2_F32>(),
+              "per-tensor codec steps");
+static_assert(step_is<QConv<S_E4M3, D_BF16>, CLS_QE4M3_BF16>() && step_is<QConv<S_E4M3, D_F16>, CLS_QE4M3_F16>() &&
+                  step_is<QConv<S_E4M3, D_F32>, CLS_QE4M3_F32>() && step_is<QConv<S_E5M2, D_BF16>, CLS_QE5M2_BF16>() &&
+                  step_is<QConv<S_E5M2, D_F16>, CLS_QE5M2_F16>() && step_is<QConv<S_E5M2, D_F32>, CLS_QE5M2_F32>() &&
+                  step_is<QConv<S_NV, D_BF16>, CLS_NVFP4_BF16>() && step_is<QConv<S_NV, D_F16>, CLS_NVFP4_F16>() &&
+                  step_is<QConv<S_NV, D_F32>, CLS_NVFP4_F32>(),
+              "block-scaled codec steps");
+
 __device__ __forceinline__ void consume_any(const uint8_t *buf, const SegMeta &m, float *qsc, uint32_t lane) {
   switch (m.cls) {
     case CLS_COPY: consume_seg<CopyBytes>(buf, m, lane); break;

@@ -31,7 +31,7 @@ EXPORTS = [
     "st_index_metadata_get", "st_view_prefix", "st_view_filter", "st_view_rename", "st_index_concat",
     "st_plan",
     "st_plan_free", "st_plan_count", "st_plan_output", "st_plan_arena", "st_plan_stats",
-    "st_plan_piece", "st_plan_worker", "st_plan_copy_bytes", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
+    "st_plan_piece", "st_plan_worker", "st_plan_copy_bytes", "st_plan_copy_range", "st_class_step", "st_materialize", "st_stage_h2d", "st_load", "st_plan_check",
     "st_materialize_noalloc", "st_static_check", "st_index_open", "st_files_open", "st_files_close", "st_files_read",
     "st_load_files", "st_cache_create", "st_cache_free", "st_cache_get", "st_cache_release",
     "st_cache_stats", "st_cache_clear", "st_load_tensors", "st_host_affinity", "st_device_reads_pageable",
@@ -131,6 +131,8 @@ def lib():
                               C.POINTER(U32), C.POINTER(U32), C.POINTER(U32), C.POINTER(U64)],
             "st_plan_worker": [P, U32, U32, C.POINTER(U64), C.POINTER(U64)],
             "st_plan_copy_bytes": [P, C.POINTER(U64), C.POINTER(U32)],
+            "st_plan_copy_range": [P, U32, C.POINTER(U64), C.POINTER(U64)],
+            "st_class_step": [U32] + [C.POINTER(U32)] * 5,
             "st_materialize": [P, P, P, P, P],
             "st_materialize_noalloc": [P, P, P, P, P],
             "st_stage_h2d": [P, P, U64, U64, P, P],
@@ -724,12 +726,30 @@ class Plan:
         _check(lib().st_plan_copy_bytes(self._h, C.byref(b), C.byref(r)))
         return b.value, r.value
 
+    def copy_ranges(self):
+        """st_plan_copy_range for every range: [(begin, end)] of the data
+        section that the loaders copy."""
+        out = []
+        for i in range(self.copy_bytes()[1]):
+            a, b = C.c_uint64(), C.c_uint64()
+            _check(lib().st_plan_copy_range(self._h, i, C.byref(a), C.byref(b)))
+            out.append((a.value, b.value))
+        return out
+
     def check(self, stream=None):
         flags = C.c_uint32()
         code = lib().st_plan_check(self._h, _stream(stream), C.byref(flags))
         if code not in (0, 14):
             _check(code)
         return flags.value
+
+
+def class_step(cls):
+    """st_class_step: (source itemsize, output itemsize, lane-step source
+    bytes, counted units, output bytes) of conversion class `cls`."""
+    v = [C.c_uint32() for _ in range(5)]
+    _check(lib().st_class_step(cls, *[C.byref(x) for x in v]))
+    return tuple(x.value for x in v)
 
 
 def static_check(stream=None):

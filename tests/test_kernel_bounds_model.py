@@ -7,10 +7,12 @@ the plans the GPU tests and the benchmark run, every byte the kernel reads
 lies in the data section, every byte it writes lies in the piece's output,
 and head + body + tail cover the piece's elements exactly once.  Data bases
 are taken at every residue mod 16 and destinations at 256-byte and at
-itemsize-only alignment.  This must be kept in step with
-csrc/st_kernels.cu (run_piece; produce and consume_seg of the TMA build,
-whose bulk copies also need 16-byte aligned windows inside the data
-section that fit the warp's shared-memory slot).
+itemsize-only alignment.  The item sizes and lane steps it uses are checked
+against the library's st_class_step (which the kernels' codecs are checked
+against at compile time); the address arithmetic restates csrc/st_kernels.cu
+(run_piece; produce and consume_seg of the TMA builds, whose bulk copies also
+need 16-byte aligned windows inside the data section that fit the warp's
+shared-memory slot).
 """
 import numpy as np
 import pytest
@@ -33,12 +35,30 @@ def step_shape(cls):
     return sb, sb // si, (sb // si) * so
 
 
+def stream_step(si, so):
+    """(SB, KS, OS) of a per-tensor class's lane step in the streaming body."""
+    sb = 16 * si // so if so > si else 16
+    return sb, sb // si, (sb // si) * so
+
+
+def test_model_steps_match_the_library(stmat):
+    """The model's item sizes and lane steps are the constants the library
+    exports (which its kernels' codecs are checked against when compiled), so
+    the model cannot drift from the kernels silently."""
+    for cls, (si, so) in CLS.items():
+        lib = stmat.class_step(cls)
+        assert lib[:2] == (si, so), cls
+        assert lib[2:] == step_shape(cls), cls
+        if cls < 13:
+            assert lib[2:] == stream_step(si, so), cls
+    with pytest.raises(stmat.StmatError):
+        stmat.class_step(len(CLS))
+
+
 def split(src, dst, n, si, so, lo, hi):
     """Mirror of run_piece: returns (head, steps, elements per step, source
     window of the vector body, destination range of the body, its alignment)."""
-    SB = 16 * si // so if so > si else 16   # source bytes per lane step
-    KS = SB // si
-    OS = KS * so
+    SB, KS, OS = stream_step(si, so)   # source bytes, elements and output bytes per lane step
     A = OS
     head = ((A - (dst & (A - 1))) & (A - 1)) // so
     head = min(head, n)

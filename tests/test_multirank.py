@@ -32,7 +32,8 @@ def _worker(rank, world, port, q):
         lay = synth.unet().files[0]
         ix = stmat.Index.from_header(lay.header, lay.data_bytes).view_rename([("model.diffusion_model.", "unet.")])
         plan = ix.plan(dst="BF16", part=rank, n_parts=world, workers=1024, host_only=True)
-        mine = ([(o["name"], o["bytes"]) for o in plan.outputs()], plan.copy_bytes()[0], lay.data_bytes)
+        mine = ([(o["name"], o["bytes"]) for o in plan.outputs()], plan.copy_bytes()[0], lay.data_bytes,
+                plan.copy_ranges())
         parts = [None] * world
         dist.all_gather_object(parts, mine)
         t = torch.tensor([1.5 + rank])        # a stand-in step time per rank
@@ -63,10 +64,11 @@ def test_two_ranks_partition_outputs(stmat, oracle):
     # each rank stages only its part's source bytes: under three quarters of the data section each,
     # together the whole of it (plus at most a merged gap at the boundary)
     data_bytes = results[0][1][0][2]
-    copied = [c for _, c, _ in results[0][1]]
+    copied = [c for _, c, _, _ in results[0][1]]
     assert all(c < data_bytes * 3 // 4 for c in copied)
     assert data_bytes <= sum(copied) <= data_bytes + 65536
-    parts = [p for p, _, _ in results[0][1]]
+    parts = [p for p, _, _, _ in results[0][1]]
+    ranges = [r for _, _, _, r in results[0][1]]
     from safetensors_materialization_gb300 import synth
     lay = synth.unet().files[0]
     full = stmat.Index.from_header(lay.header, lay.data_bytes).view_rename(
@@ -77,7 +79,18 @@ def test_two_ranks_partition_outputs(stmat, oracle):
     biggest = max(b for _, b in everything)
     for p in parts:
         assert abs(sum(b for _, b in p) - total / world) <= biggest
-    # the oracle's parts are the same
+    # the oracle's parts are the same, and each rank copies exactly its outputs' source extents
+    # (taken from the oracle's index), merged across gaps under 64 KiB
     oix = oracle.parse_header(lay.header, lay.data_bytes).view_rename([("model.diffusion_model.", "unet.")])
     for r in range(world):
-        assert [(o["name"], o["bytes"]) for o in oix.select(dst="BF16", part=r, nparts=world).outputs()] == parts[r]
+        sel = oix.select(dst="BF16", part=r, nparts=world)
+        assert [(o["name"], o["bytes"]) for o in sel.outputs()] == parts[r]
+        ext = sorted((oix.entry(o["entry"])["begin"], oix.entry(o["entry"])["end"]) for o in sel.outputs())
+        merged = []
+        for a, b in ext:
+            if merged and a <= merged[-1][1] + 65536:
+                merged[-1][1] = max(merged[-1][1], b)
+            else:
+                merged.append([a, b])
+        assert [tuple(m) for m in merged] == ranges[r]
+        assert sum(b - a for a, b in ranges[r]) == copied[r]
