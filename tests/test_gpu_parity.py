@@ -470,3 +470,40 @@ def test_tensor_parallel_shard_load(stmat, oracle):
     sel = oix.select(dst="BF16", names=names, slices=slices)
     outs.check_guards()
     assert compare_full(sel, img[lay.data_start:], {"tp rank 0": outs}) == sum(o["bytes"] for o in plan.outputs())
+
+
+@pytest.mark.parametrize("name", ["unet_small", "stress"])
+def test_partition_parts_load_only_their_bytes(stmat, oracle, name):
+    """The multi-GPU split on one GPU: each of 3 parts (st_selection.part /
+    n_parts) is loaded by st_load from pinned host memory into a device data
+    buffer that holds garbage everywhere else; a part copies only its own
+    byte ranges (st_plan_copy_range), and its outputs equal the oracle's
+    selection of the same part, every element."""
+    from safetensors_materialization_gb300 import synth
+    w = synth.WORKLOADS[name]()
+    lay = w.files[0]
+    img = synth.build_workload_file(w, 0)
+    data = img[lay.data_start:]
+    ix = w.view(stmat.Index.from_header(lay.header, lay.data_bytes))
+    oix = w.view(oracle.parse_header(lay.header, lay.data_bytes))
+    host = torch.from_numpy(data.copy()).pin_memory()
+    names = []
+    for part in range(3):
+        plan = ix.plan(dst="BF16", part=part, n_parts=3, chunk_bytes=64 << 20)
+        ranges = plan.copy_ranges()
+        assert sum(b - a for a, b in ranges) == plan.copy_bytes()[0] < lay.data_bytes
+        dev = torch.full((lay.data_bytes,), 0x7F, dtype=torch.uint8, device="cuda")
+        outs = GuardedOutputs(plan)
+        plan.load(host, dev, outs.ptrs, copy_stream=torch.cuda.Stream(), compute_stream=torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        outs.check_guards()
+        copied = torch.zeros(lay.data_bytes, dtype=torch.bool, device="cuda")
+        for a, b in ranges:
+            copied[a:b] = True
+            assert torch.equal(dev[a:b], host[a:b].cuda())
+        assert torch.all(dev[~copied] == 0x7F)              # nothing outside the ranges was copied
+        sel = oix.select(dst="BF16", part=part, nparts=3)
+        assert compare_full(sel, data, {f"part {part}": outs}) == sum(o["bytes"] for o in sel.outputs())
+        names += [o["name"] for o in plan.outputs()]
+    assert names == [o["name"] for o in oix.select(dst="BF16").outputs()]   # the parts cover every output once
