@@ -248,7 +248,8 @@ typedef struct st_plan_options {
   uint32_t blocks_per_sm; /* 0 = for the streaming build 2 when the outputs' contiguous runs
                              average >= 64 KiB of traffic, else 3; the most that fit for the
                              other builds */
-  uint64_t unit_bytes;    /* traffic per interleaved unit; 0 = 32768 */
+  uint64_t unit_bytes;    /* traffic per interleaved unit; 0 = 16384 for the TMA build, 32768
+                             otherwise */
   uint32_t kernel;        /* 0 = choose: the TMA build when outputs average under 64 KiB of
                              traffic (many small tensors), else the streaming build; 1 = streaming
                              build (deep unroll); 2 = latency build (high occupancy); 3 = TMA
@@ -265,11 +266,15 @@ typedef struct st_plan_options {
 } st_plan_options;
 
 /* Builds the plan: outputs, then pieces (output element ranges).  Each chunk
- * is cut, in class-major source order, into units of about unit_bytes of
- * traffic (source plus destination bytes), and unit j is given to warp
- * j mod workers, so that all warps sweep the data section together.  Unless host_only, allocates the
+ * is cut, in the unit order of `order`, into units of about unit_bytes of
+ * traffic (source plus destination bytes) in rounds of `workers` units, and
+ * unit j is given to warp j mod workers, so that all warps sweep the data
+ * section together; the last rounds (15 % for the TMA build, 40 % for the
+ * wide TMA build, 20 % for the streaming build when runs are long, none
+ * otherwise) are left as a claimed tail that whichever warps finish their own
+ * units first take while the kernel runs.  Unless host_only, allocates the
  * plan's device tables on the current device (cudaMalloc) and uploads them
- * synchronously; call it outside stream capture.  opts may be NULL. */
+ * synchronously.  opts may be NULL. */
 st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst_dtype,
                   const st_plan_options *opts, st_plan_t **out);
 void st_plan_free(st_plan_t *plan);
@@ -323,9 +328,9 @@ st_status st_plan_piece(const st_plan_t *plan, uint64_t k, uint64_t *src, uint64
 st_status st_class_step(uint32_t cls, uint32_t *src_item, uint32_t *out_item, uint32_t *step_src,
                         uint32_t *step_units, uint32_t *step_out);
 /* Pieces of worker w < workers in chunk c: [first, last), the warp's own
- * share; w == workers gives the chunk's claimed pieces, which the TMA builds'
- * warps take in source order while the kernel runs, whichever warp is free
- * (empty for the streaming builds).  The ranges of w = 0 .. workers cover the
+ * share; w == workers gives the chunk's claimed pieces, which the warps take
+ * in source order while the kernel runs, whichever warp is free (empty for
+ * plans without a claimed tail).  The ranges of w = 0 .. workers cover the
  * chunk's pieces once. */
 st_status st_plan_worker(const st_plan_t *plan, uint32_t chunk, uint32_t w, uint64_t *first,
                          uint64_t *last);
