@@ -309,7 +309,9 @@ st_status st_plan_stats(const st_plan_t *plan, uint32_t *workers, uint32_t *chun
  * output's source extent and its scales, merged across gaps under 64 KiB),
  * in *ranges pieces (may be NULL). */
 st_status st_plan_copy_bytes(const st_plan_t *plan, uint64_t *bytes, uint32_t *ranges);
-/* Range i < *ranges of st_plan_copy_bytes: data-section bytes [begin, end),
+/* The range reads of "Range reads and tiering" (Disk tier safetensors
+ * streaming design audit) as the loaders perform them for a plan.  Range
+ * i < *ranges of st_plan_copy_bytes: data-section bytes [begin, end),
  * ascending and disjoint (more than 64 KiB apart).  ST_E_INVAL for i out of
  * range. */
 st_status st_plan_copy_range(const st_plan_t *plan, uint32_t i, uint64_t *begin, uint64_t *end);
@@ -319,7 +321,8 @@ st_status st_plan_copy_range(const st_plan_t *plan, uint32_t i, uint64_t *begin,
 st_status st_plan_piece(const st_plan_t *plan, uint64_t k, uint64_t *src, uint64_t *dst,
                         uint64_t *scale, uint32_t *count, uint32_t *output, uint32_t *cls,
                         uint32_t *rows, uint64_t *pitch);
-/* Conversion class `cls` (st_plan_piece's class, 0 .. 21): bytes per counted
+/* No counterpart on the pages (a description of the kernels' work split).
+ * Conversion class `cls` (st_plan_piece's class, 0 .. 21): bytes per counted
  * unit read (src_item) and written (out_item), and one lane step of the
  * kernels' vector bodies: step_src source bytes, step_units counted units,
  * step_out output bytes (one 16- or 8-byte vector).  The kernels' codecs are
@@ -585,9 +588,11 @@ st_status st_load_files(const st_files_t *files, void *data_dev, const st_plan_t
 st_status st_materialize_noalloc(const void *data_dev, const st_plan_t *plan, void *const *dst_ptrs,
                                  const float *scales, void *stream);
 
-/* Reads and clears the error word of the library's static device array on
- * the current device: the device flags of every st_materialize_noalloc and
- * st_load_tensors call since the last read (bits as for st_plan_check).
+/* No counterpart on the pages (the library's own status for the two calls
+ * that use its static array).  Reads and clears the error word of the
+ * library's static device array on the current device: the device flags of
+ * every st_materialize_noalloc and st_load_tensors call since the last read
+ * (bits as for st_plan_check).
  * Copies the word to the host on `stream` and waits for the stream, so every
  * such call queued on it before has finished; calls on other streams are
  * seen only once they have finished.  Allocates nothing.  Returns
