@@ -245,9 +245,8 @@ typedef struct st_plan_options {
   uint64_t chunk_bytes;   /* 0 = one launch over the whole data section; otherwise the data
                              section is split in chunks of this size for st_load's pipeline */
   int32_t host_only;      /* nonzero: build the plan without touching the GPU (requires workers) */
-  uint32_t blocks_per_sm; /* 0 = for the streaming build 2 when the outputs' contiguous runs
-                             average >= 64 KiB of traffic, else 3; the most that fit for the
-                             other builds */
+  uint32_t blocks_per_sm; /* 0 = 2 for the streaming build; the most that fit for the other
+                             builds */
   uint64_t unit_bytes;    /* traffic per interleaved unit; 0 = 16384 for the TMA build, 32768
                              otherwise */
   uint32_t kernel;        /* 0 = choose: the TMA build when outputs average under 64 KiB of
@@ -270,8 +269,9 @@ typedef struct st_plan_options {
  * traffic (source plus destination bytes) in rounds of `workers` units, and
  * unit j is given to warp j mod workers, so that all warps sweep the data
  * section together; the last rounds (15 % for the TMA build, 40 % for the
- * wide TMA build, 20 % for the streaming build when runs are long, none
- * otherwise) are left as a claimed tail that whichever warps finish their own
+ * wide TMA build, 20 % for the streaming build when the outputs' contiguous
+ * runs average 64 KiB of traffic or more, else 30 %; none for the latency
+ * build) are left as a claimed tail that whichever warps finish their own
  * units first take while the kernel runs.  Unless host_only, allocates the
  * plan's device tables on the current device (cudaMalloc) and uploads them
  * synchronously.  opts may be NULL. */

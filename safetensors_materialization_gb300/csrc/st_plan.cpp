@@ -51,13 +51,13 @@ constexpr uint64_t kTmaUnitBytes = 16384;
 // TMA, 100k tiny tensors 15 % (0.851 -> 0.876); wide TMA, block-scaled
 // weights 40 % (block FP8 0.896 -> 0.974, NVFP4 0.843 -> 0.965); streaming,
 // long contiguous runs 20 % (scaled FP8 0.972 -> 0.992, LLM 0.968 -> 1.02,
-// UNet 0.971 -> 0.977).  Short runs on the streaming build (tensor-parallel
-// slices, 3 blocks per SM) measured 0.923 -> 0.915 with any tail: none.
-constexpr uint64_t kClaimedPct = 15, kClaimedPctWide = 40, kClaimedPctStream = 20;
+// UNet 0.971 -> 0.977; 30-40 % the same within 0.3 %), short runs (a
+// tensor-parallel rank's row slices) 30 % (0.923 at 3 blocks per SM with
+// fixed shares -> 0.988 at 2 blocks per SM; 15 % 0.91, 20 % 0.982, 40 % 0.990).
+constexpr uint64_t kClaimedPct = 15, kClaimedPctWide = 40, kClaimedPctStream = 20, kClaimedPctStreamShort = 30;
 constexpr uint64_t kLazyBytesPerWarp = 16384;  // st_load_tensors: traffic per warp
 constexpr uint64_t kLazyMaxWarps = 2432;        // ... and at most this many warps (2 blocks on each of 152 SMs)
-constexpr uint32_t kStreamBlocksPerSm = 3;     // streaming build: fewer, deeper warps ...
-constexpr uint32_t kStreamBlocksPerSmLong = 2;  // ... and fewer still when the contiguous runs are long
+constexpr uint32_t kStreamBlocksPerSm = 2;  // streaming build: fewer, deeper warps
 constexpr uint64_t kLongRunBytes = 65536;       // mean traffic per contiguous run that counts as long
 constexpr uint64_t kSmallOutputBytes = 65536;  // mean traffic per output below which the
                                                // latency build is chosen
@@ -605,8 +605,8 @@ void build_pieces(st_plan_s *p) {
     // repeatable to 0.5 us).
     const uint64_t pct = p->kernel == kKernelTmaWide ? kClaimedPctWide
                          : is_tma_build(p->kernel)   ? kClaimedPct
-                         : p->kernel == kKernelStream && p->long_runs ? kClaimedPctStream
-                                                                      : 0;
+                         : p->kernel == kKernelStream ? (p->long_runs ? kClaimedPctStream : kClaimedPctStreamShort)
+                                                      : 0;
     const uint64_t dyn_rounds = rounds >= 2 && pct ? std::max<uint64_t>(1, rounds * pct / 100) : 0;
     const uint64_t Ns = (rounds - dyn_rounds) * W;
     for (uint32_t w = 0; w < W; ++w) {
@@ -729,10 +729,11 @@ st_status plan_host(std::shared_ptr<const IndexData> index, const st_selection *
     uint32_t bps = static_cast<uint32_t>(blocks);
     if (opts && opts->blocks_per_sm) bps = std::min(bps, opts->blocks_per_sm);
     else if (p->kernel == kKernelStream) {
-      // Measured: long contiguous runs (whole large tensors) stream best at 2
-      // blocks per SM (scaled FP8 91.7 -> 95.6 %, 4-shard LLM 96.9 -> 98.0 %);
-      // many short runs (row-sliced tensor-parallel shards) at 3.
-      bps = std::min(bps, p->long_runs ? kStreamBlocksPerSmLong : kStreamBlocksPerSm);
+      // Measured: the streaming build runs best at 2 blocks per SM (scaled FP8
+      // 91.7 -> 95.6 %, 4-shard LLM 96.9 -> 98.0 % against 3); many short runs
+      // (row-sliced tensor-parallel shards) did better at 3 with fixed shares
+      // (0.92 against 0.90) but best at 2 with a claimed tail (0.988).
+      bps = std::min(bps, kStreamBlocksPerSm);
     }
     if (workers == 0) workers = static_cast<uint32_t>(sms) * bps * kWarpsPerBlock;
   }
