@@ -135,10 +135,37 @@ def measured_peak():
         return 6800.0, "fallback 6.8 TB/s"
 
 
+def kernel_code(text):
+    """The kernel source without its comments and blank space: what a DRAM
+    traffic record depends on (a comment edit leaves the kernel unchanged)."""
+    import re
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":                      # a literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_sha():
+    """sha256 prefix of the kernel code (st_kernels.cu, comments and blank
+    space removed) that profiles/traffic.json records are keyed to."""
     import hashlib
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(KERNEL_SRC, encoding="utf-8") as f:
+        return hashlib.sha256(kernel_code(f.read()).encode()).hexdigest()[:16]
 
 
 def profiled_traffic(workload):

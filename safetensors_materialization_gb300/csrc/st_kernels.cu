@@ -37,10 +37,12 @@
 //  - code size matters: one kernel serves every class, and workloads that
 //    mix classes (many small tensors) otherwise stall on instruction fetch,
 //    so each class has just an aligned and a misaligned body.
-// Three builds share the codecs: streaming (deep register batches, for large
-// tensors), latency (shallow batches at high occupancy) and TMA (source bytes
-// staged in shared memory by bulk copies, for many small tensors; see "the
-// TMA build" below).
+// Four builds share the codecs: streaming (deep register batches, for large
+// tensors and sliced runs), latency (shallow batches at high occupancy, on
+// request) and two shapes of the TMA build (source bytes staged in shared
+// memory by bulk copies: four slots per warp for many small tensors, two
+// slots at more warps per SM for block-scaled weights; see "the TMA build"
+// below).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>

@@ -66,3 +66,14 @@ def test_gpus_flag_is_honoured_or_refused(monkeypatch):
     assert bench.launch_command(bench.parse_args(["--gpus", "2"]), 2, []) is None
     with pytest.raises(SystemExit, match="WORLD_SIZE"):
         bench.launch_command(bench.parse_args(["--gpus", "4"]), 2, [])
+
+
+def test_traffic_key_ignores_comments_only():
+    """A traffic record stays valid across comment edits and is voided by any
+    code edit."""
+    import bench
+    src = 'int f(int a) { // add one\n  return a + 1; /* "x" */ }\nconst char *s = "a // b";\n'
+    assert bench.kernel_code(src) == 'int f(int a) { return a + 1; } const char *s = "a // b";'
+    assert bench.kernel_code(src.replace("add one", "plus 1")) == bench.kernel_code(src)
+    assert bench.kernel_code(src.replace("a + 1", "a + 2")) != bench.kernel_code(src)
+    assert bench.kernel_code(src.replace('"a // b"', '"a // c"')) != bench.kernel_code(src)
