@@ -268,11 +268,11 @@ typedef struct st_plan_options {
  * is cut, in the unit order of `order`, into units of about unit_bytes of
  * traffic (source plus destination bytes) in rounds of `workers` units, and
  * unit j is given to warp j mod workers, so that all warps sweep the data
- * section together; the last rounds (15 % for the TMA build, 40 % for the
- * wide TMA build, 20 % for the streaming build when the outputs' contiguous
- * runs average 64 KiB of traffic or more, else 30 %; none for the latency
- * build) are left as a claimed tail that whichever warps finish their own
- * units first take while the kernel runs.  Unless host_only, allocates the
+ * section together; the last rounds, about a share of the chunk's cost (8 %
+ * for the TMA build, 40 % for the wide TMA build, 20 % for the streaming
+ * build when the outputs' contiguous runs average 64 KiB of traffic or more,
+ * else 30 %; none for the latency build), are left as a claimed tail that
+ * whichever warps finish their own units first take while the kernel runs.  Unless host_only, allocates the
  * plan's device tables on the current device (cudaMalloc) and uploads them
  * synchronously.  opts may be NULL. */
 st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst_dtype,

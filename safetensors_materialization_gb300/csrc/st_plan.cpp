@@ -46,15 +46,16 @@ constexpr uint64_t kDefaultUnitBytes = 32768;  // cost of one interleaved unit
 // 16 KiB; 8-20 KiB all within 0.88-0.89; block-scaled weights on the wide
 // build measured 0.93-0.96 at 16 KiB against 0.96-0.97 at 32 KiB).
 constexpr uint64_t kTmaUnitBytes = 16384;
-// Percent of the units (whole rounds) that warps claim while they run instead
-// of owning them, by build (measured best, fractions of the copy peak):
-// TMA, 100k tiny tensors 15 % (0.851 -> 0.876); wide TMA, block-scaled
+// Percent of a chunk's cost (whole rounds of units) that warps claim while
+// they run instead of owning it, by build (measured best, fractions of the
+// copy peak): TMA, 100k tiny tensors 8 % (0.851 with fixed shares -> 0.895-0.903;
+// 4-6 % 0.89-0.895, 10-12 % 0.886-0.894, 14 % 0.874-0.883); wide TMA, block-scaled
 // weights 40 % (block FP8 0.896 -> 0.974, NVFP4 0.843 -> 0.965); streaming,
 // long contiguous runs 20 % (scaled FP8 0.972 -> 0.992, LLM 0.968 -> 1.02,
 // UNet 0.971 -> 0.977; 30-40 % the same within 0.3 %), short runs (a
 // tensor-parallel rank's row slices) 30 % (0.923 at 3 blocks per SM with
 // fixed shares -> 0.988 at 2 blocks per SM; 15 % 0.91, 20 % 0.982, 40 % 0.990).
-constexpr uint64_t kClaimedPct = 15, kClaimedPctWide = 40, kClaimedPctStream = 20, kClaimedPctStreamShort = 30;
+constexpr uint64_t kClaimedPct = 8, kClaimedPctWide = 40, kClaimedPctStream = 20, kClaimedPctStreamShort = 30;
 constexpr uint64_t kLazyBytesPerWarp = 16384;  // st_load_tensors: traffic per warp
 constexpr uint64_t kLazyMaxWarps = 2432;        // ... and at most this many warps (2 blocks on each of 152 SMs)
 constexpr uint32_t kStreamBlocksPerSm = 2;  // streaming build: fewer, deeper warps
@@ -413,6 +414,12 @@ struct Segment {
   uint64_t u0, u1;
 };
 
+// A piece's cost in the balance: a fixed cost plus its bytes of traffic.
+double piece_cost(const Piece &pc) {
+  const uint32_t cls = pc.out_cls & ((1u << kClsBits) - 1);
+  return double(kPieceCost) + double(pc.count) * pc.rows * (cls_in_size(cls) + cls_out_size(cls));
+}
+
 // Cuts `segs` (in source order) into n consecutive units of about equal cost
 // (`total` = the segments' cost): appends the units' pieces to *units and the
 // n + 1 unit boundaries to *ub.  Cuts inside an output fall on multiples of
@@ -607,8 +614,23 @@ void build_pieces(st_plan_s *p) {
                          : is_tma_build(p->kernel)   ? kClaimedPct
                          : p->kernel == kKernelStream ? (p->long_runs ? kClaimedPctStream : kClaimedPctStreamShort)
                                                       : 0;
-    const uint64_t dyn_rounds = rounds >= 2 && pct ? std::max<uint64_t>(1, rounds * pct / 100) : 0;
-    const uint64_t Ns = (rounds - dyn_rounds) * W;
+    // The own units are whole rounds up to where the units' cumulative cost
+    // reaches (100 - pct) % of the chunk's cost (rounded to the nearest round,
+    // leaving at least one round to claim): units are not always filled
+    // evenly (a unit below the 2 KiB cut granule takes more than its share,
+    // and the last rounds can then be empty), so the tail is found by cost,
+    // not by counting rounds.
+    uint64_t Ns = N;
+    if (rounds >= 2 && pct) {
+      const double keep = total * double(100 - pct) / 100.0;
+      double acc = 0;
+      uint64_t j = 0;
+      for (; j < N; ++j) {
+        for (uint32_t q = ub[j]; q < ub[j + 1]; ++q) acc += piece_cost(units[q]);
+        if (acc >= keep) break;
+      }
+      Ns = std::min<uint64_t>(rounds - 1, (j + W / 2) / W) * W;
+    }
     for (uint32_t w = 0; w < W; ++w) {
       parts[w] = static_cast<uint32_t>(p->pieces.size());
       for (uint64_t j = w; j < Ns; j += W) p->pieces.insert(p->pieces.end(), units.begin() + ub[j], units.begin() + ub[j + 1]);

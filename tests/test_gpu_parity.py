@@ -507,3 +507,41 @@ def test_partition_parts_load_only_their_bytes(stmat, oracle, name):
         assert compare_full(sel, data, {f"part {part}": outs}) == sum(o["bytes"] for o in sel.outputs())
         names += [o["name"] for o in plan.outputs()]
     assert names == [o["name"] for o in oix.select(dst="BF16").outputs()]   # the parts cover every output once
+
+
+@pytest.mark.parametrize("kernel", [1, 3, 4])
+def test_claimed_tail_on_every_launch(stmat, oracle, kernel):
+    """Warps claim a plan's tail through two words that the last warp of each
+    launch zeroes: five launches of one plan in a row (and a chunked st_load
+    whose chunk launches share the words) each produce every output, equal to
+    the oracle's, with the arena cleared in between."""
+    img = sweep_image(3, seed=40 + kernel)
+    ix = stmat.Index.from_file(img)
+    hlen = ix.sizes()[0]
+    sel, want = oracle_all(oracle, img, dst="BF16")
+    buf, data_ptr = to_device(img, 0, True, 8 + hlen)
+    plan = ix.plan(dst="BF16", kernel=kernel, workers=64, unit_bytes=2048)
+    st = plan.stats()
+    tail = plan.worker(0, st["workers"])
+    assert tail[1] > tail[0], "the plan has a claimed tail"
+    outs = GuardedOutputs(plan)
+    for _ in range(5):
+        outs.arena.fill_(0xA5)
+        plan.materialize(data_ptr, outs.ptrs)
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        assert_same(plan, outs, sel, want)
+    data = img[8 + hlen:]
+    chunked = ix.plan(dst="BF16", kernel=kernel, workers=64, unit_bytes=2048, chunk_bytes=1 << 16)
+    cst = chunked.stats()
+    assert cst["chunks"] > 1 and any(chunked.worker(c, cst["workers"])[1] > chunked.worker(c, cst["workers"])[0]
+                                     for c in range(cst["chunks"]))
+    host = torch.from_numpy(data.copy()).pin_memory()
+    dev = torch.empty(data.size, dtype=torch.uint8, device="cuda")
+    couts = GuardedOutputs(chunked)
+    for _ in range(2):
+        couts.arena.fill_(0xA5)
+        chunked.load(host, dev, couts.ptrs, copy_stream=torch.cuda.Stream(), compute_stream=torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert chunked.check() == 0
+        assert_same(chunked, couts, sel, want)
