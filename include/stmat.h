@@ -272,7 +272,9 @@ typedef struct st_plan_options {
  * for the TMA build, 40 % for the wide TMA build, 20 % for the streaming
  * build when the outputs' contiguous runs average 64 KiB of traffic or more,
  * else 30 %; none for the latency build), are left as a claimed tail that
- * whichever warps finish their own units first take while the kernel runs.  Unless host_only, allocates the
+ * whichever warps finish their own units first take while the kernel runs
+ * (the TMA build's tail cut further into pieces of at most 2 KiB of source,
+ * claimed at least two at a time).  Unless host_only, allocates the
  * plan's device tables on the current device (cudaMalloc) and uploads them
  * synchronously.  opts may be NULL. */
 st_status st_plan(const st_index_t *index, const st_selection *sel, st_dtype dst_dtype,

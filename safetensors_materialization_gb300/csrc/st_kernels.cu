@@ -1074,13 +1074,16 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   const uint32_t p0 = a.parts[w], p1 = a.parts[w + 1];
   const uint32_t dyn0 = a.parts[a.workers], dtotal = a.claim_end - dyn0;
   const uint32_t spread = kClaimSpread * a.workers;
+  // The 4-slot build (kInterior) gets tail pieces of at most one segment
+  // (the planner cuts them so); its warps claim two or more at a time.
+  constexpr uint32_t kClaimMin = kInterior ? 2 : 1;
   uint32_t sp = p0;                // the next own piece not yet in a batch
   bool claiming = false;           // a claim has been made and not yet taken
   uint32_t next_at = 0, next_k = 0;  // lane 0: that claim
   auto start_claim = [&](uint32_t from) {  // claim about (left) / spread pieces, from = claimed so far
     if (lane == 0) {
       const uint32_t left = from < dtotal ? dtotal - from : 0;
-      next_k = max(1u, min(kBatch, left / spread));
+      next_k = max(kClaimMin, min(kBatch, left / spread));
       next_at = atomicAdd(a.claim, next_k);
     }
     claiming = true;

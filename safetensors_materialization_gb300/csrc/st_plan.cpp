@@ -46,6 +46,15 @@ constexpr uint64_t kDefaultUnitBytes = 32768;  // cost of one interleaved unit
 // 16 KiB; 8-20 KiB all within 0.88-0.89; block-scaled weights on the wide
 // build measured 0.93-0.96 at 16 KiB against 0.96-0.97 at 32 KiB).
 constexpr uint64_t kTmaUnitBytes = 16384;
+// The TMA build's claimed tail is cut further, into pieces of at most this
+// many source bytes (one 2 KiB segment), which its warps claim at least two
+// at a time: a warp that claims the last whole 16 KiB unit finishes up to
+// 8 segments after the others.  Measured on 100k tiny tensors: 0.899-0.902
+// -> 0.912-0.915 of the copy peak; 3 KiB pieces 0.905, 1 KiB 0.843, claims of
+// one piece 0.904-0.907, the same claims of whole units 0.886.  The wide
+// build keeps whole units (its 40 % tail cut to 2-8 KiB pieces: block FP8
+// 0.974 -> 0.945-0.966, NVFP4 0.973 -> 0.934-0.973).
+constexpr uint64_t kTmaTailPieceBytes = 2048;
 // Percent of a chunk's cost (whole rounds of units) that warps claim while
 // they run instead of owning it, by build (measured best, fractions of the
 // copy peak): TMA, 100k tiny tensors 8 % (0.851 with fixed shares -> 0.895-0.903;
@@ -520,6 +529,21 @@ void cut_units(const st_plan_s &p, const std::vector<Segment> &segs, uint64_t n,
 }
 
 // Builds pieces and per-chunk worker partitions.
+// Appends a one-run piece cut into pieces of at most `bytes` source bytes
+// (at least one element each), in order.
+void split_piece(const Piece &pc, uint64_t bytes, std::vector<Piece> *out) {
+  const uint32_t cls = pc.out_cls & ((1u << kClsBits) - 1);
+  const uint64_t si = cls_in_size(cls), so = cls_out_size(cls);
+  const uint32_t step = static_cast<uint32_t>(std::max<uint64_t>(1, bytes / si));
+  for (uint32_t e = 0; e < pc.count; e += std::min(step, pc.count - e)) {
+    Piece x = pc;
+    x.count = std::min(step, pc.count - e);
+    x.src = pc.src + e * si;
+    x.dst = pc.dst + e * so;
+    out->push_back(x);
+  }
+}
+
 void build_pieces(st_plan_s *p) {
   const Core &core = *p->index->core;
   const uint64_t C = p->chunk_bytes;
@@ -636,7 +660,14 @@ void build_pieces(st_plan_s *p) {
       for (uint64_t j = w; j < Ns; j += W) p->pieces.insert(p->pieces.end(), units.begin() + ub[j], units.begin() + ub[j + 1]);
     }
     parts[W] = static_cast<uint32_t>(p->pieces.size());
-    p->pieces.insert(p->pieces.end(), units.begin() + ub[Ns], units.begin() + ub[N]);
+    for (size_t q = ub[Ns]; q < ub[N]; ++q) {
+      const Piece &pc = units[q];
+      if (p->kernel != kKernelTma || pc.rows != 1) {
+        p->pieces.push_back(pc);
+        continue;
+      }
+      split_piece(pc, kTmaTailPieceBytes, &p->pieces);
+    }
     p->claim_end[k] = static_cast<uint32_t>(p->pieces.size());
   }
 }

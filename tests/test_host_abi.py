@@ -297,6 +297,34 @@ def test_worker_balance(stmat):
         assert max(loads) <= mean + biggest_unsplit + 2048, (wl, max(loads), mean)
 
 
+def test_tma_claimed_tail_is_cut_into_segment_pieces(stmat):
+    """The TMA build's claimed tail holds pieces of at most 2 KiB of source
+    (one segment: its warps claim two or more at a time), while its own
+    shares keep whole 16 KiB units; the streaming build's claimed tail keeps
+    whole units.  The pieces still cover every output once (checked for
+    these plans by test_pieces_cover_outputs_once)."""
+    from safetensors_materialization_gb300 import synth
+    lay = synth.stress().files[0]
+    ix = stmat.Index.from_header(lay.header, lay.data_bytes)
+    W = 2432
+
+    def src_bytes(p):
+        return p["count"] * CLS_SIZES[p["cls"]][0]
+
+    plan = ix.plan(dst="BF16", workers=W, host_only=True)
+    assert plan.stats()["kernel"] == "tma"
+    pieces, st = piece_table(plan)
+    a, b = plan.worker(0, st["workers"])
+    tail, own = pieces[a:b], pieces[:a]
+    assert len(tail) > 1000
+    assert all(p["rows"] == 1 and 1 <= src_bytes(p) <= 2048 for p in tail)
+    assert max(src_bytes(p) for p in own) > 8192
+    stream = ix.plan(dst="BF16", workers=W, host_only=True, kernel=1)
+    spieces, sst = piece_table(stream)
+    a, b = stream.worker(0, sst["workers"])
+    assert b > a and max(src_bytes(p) for p in spieces[a:b]) > 8192
+
+
 # ------------------------------------------------------------- slicing
 
 def sliced_layout(seed):
