@@ -549,7 +549,7 @@ __device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
     }
     base += n;
   }
-  release_claims(a, lane);
+  if (dtotal) release_claims(a, lane);
 }
 
 __global__ void __launch_bounds__(kThreads) materialize_stream(const LaunchArgs a) { materialize_body<StreamCfg>(a); }
@@ -1052,7 +1052,9 @@ struct Cursor {
 // +2 % on many small tensors with the 4-slot shape; -1..3 % on the
 // register-capped wide shape, which keeps the general path).
 // The last warp of a launch to finish zeroes its claim words (every warp has
-// made its last claim by then).
+// made its last claim by then).  Launches without a claimed tail never touch
+// them and skip this (its fence and atomic cost a warp about 1 us, the 16
+// tiny tensors' launch 10 %).
 __device__ __forceinline__ void release_claims(const LaunchArgs &a, uint32_t lane) {
   if (lane == 0) {
     __threadfence();
@@ -1111,7 +1113,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   uint32_t bs0 = 0, bs1 = 0, bn0 = 0, bn1 = 0;  // the batches in the two descriptor slots
   bn0 = next_batch(bs0);
   if (bn0 == 0) {
-    release_claims(a, lane);
+    if (dtotal) release_claims(a, lane);
     return;
   }
   const uintptr_t lo16 = (reinterpret_cast<uintptr_t>(a.data) + 15) & ~uintptr_t(15);
@@ -1362,7 +1364,7 @@ __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
     for (; jc < jp; ++jc) mbar_wait(&ws.bar[jc % kSlots], (jc / kSlots) & 1);
     for (; dseen < dissued; ++dseen) mbar_wait(&ws.dbar[dseen & 1], (dseen >> 1) & 1);
   }
-  release_claims(a, lane);
+  if (dtotal) release_claims(a, lane);
 }
 
 __global__ void __launch_bounds__(kThreads, ST_TMA_MIN_BLOCKS) materialize_tma(const LaunchArgs a) {
