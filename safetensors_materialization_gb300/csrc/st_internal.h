@@ -101,6 +101,15 @@ struct LaunchArgs {
   // sets them back to zero.
   uint32_t claim_end;
   uint32_t *claim;
+  // Small single-chunk plans: the launch's piece table and destination array
+  // (block 0) and the data-section bytes [pf_data_off, pf_data_off +
+  // pf_data_bytes) (a slice per block) are prefetched into L2 as it starts;
+  // pf_data_bytes 0: nothing.
+  const void *pf_table = nullptr;
+  uint32_t pf_table_bytes = 0;
+  uint32_t pf_dst_bytes = 0;
+  uint64_t pf_data_off = 0;
+  uint64_t pf_data_bytes = 0;
 };
 
 // Bytes written per counted unit of a class.

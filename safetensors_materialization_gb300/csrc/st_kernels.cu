@@ -464,12 +464,34 @@ __device__ __forceinline__ void release_claims(const LaunchArgs &a, uint32_t lan
 // at least one and at most 32: larger claims early, single pieces at the end.
 constexpr uint32_t kClaimSpread = 8;
 
+// L2 prefetch of the 16-byte-aligned interior of [p, p + bytes).
+__device__ __forceinline__ void l2_prefetch(const void *p, uint64_t bytes) {
+  uintptr_t lo = (reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15);
+  const uintptr_t hi = (reinterpret_cast<uintptr_t>(p) + bytes) & ~uintptr_t(15);
+  while (lo < hi) {
+    const uint32_t n = static_cast<uint32_t>(hi - lo < 65536 ? hi - lo : 65536);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"(n) : "memory");
+    lo += n;
+  }
+}
+__device__ __forceinline__ void prefetch_inputs(const LaunchArgs &a) {
+  if (threadIdx.x != 0 || a.pf_data_bytes == 0) return;
+  if (blockIdx.x == 0) {
+    l2_prefetch(a.pf_table, a.pf_table_bytes);
+    l2_prefetch(a.dst, a.pf_dst_bytes);
+  }
+  const uint64_t slice = (a.pf_data_bytes + gridDim.x - 1) / gridDim.x;
+  const uint64_t b0 = a.pf_data_bytes < slice * blockIdx.x ? a.pf_data_bytes : slice * blockIdx.x;
+  l2_prefetch(a.data + a.pf_data_off + b0, slice < a.pf_data_bytes - b0 ? slice : a.pf_data_bytes - b0);
+}
+
 template <class Cfg>
 __device__ __forceinline__ void materialize_body(const LaunchArgs &a) {
   __shared__ Staged stage[kWarpsPerBlock];
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t wib = threadIdx.x >> 5;
   const uint32_t w = blockIdx.x * kWarpsPerBlock + wib;
+  prefetch_inputs(a);
   if (w >= a.workers) return;
   const uint32_t p0 = a.parts[w], p1 = a.parts[w + 1];
   const uint32_t dyn0 = a.parts[a.workers], dtotal = a.claim_end - dyn0;
@@ -1069,6 +1091,7 @@ template <int kSlots, bool kInterior>
 __device__ __forceinline__ void tma_body(const LaunchArgs &a, uint8_t *smem) {
   const uint32_t lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const uint32_t w = blockIdx.x * kWarpsPerBlock + wib;
+  prefetch_inputs(a);
   if (w >= a.workers) return;
   WarpSmem<kSlots> &ws = reinterpret_cast<WarpSmem<kSlots> *>(smem)[wib];
   // The warp's own pieces [p0, p1), then pieces of the claimed tail

@@ -55,6 +55,12 @@ constexpr uint64_t kTmaUnitBytes = 16384;
 // build keeps whole units (its 40 % tail cut to 2-8 KiB pieces: block FP8
 // 0.974 -> 0.945-0.966, NVFP4 0.973 -> 0.934-0.973).
 constexpr uint64_t kTmaTailPieceBytes = 2048;
+// Single-chunk plans whose source bytes span at most this much of the data
+// section (and fill at least half of that span) prefetch their piece table,
+// destination array and that span into L2 as the launch starts, so that the
+// dependent reads after the warp's first (parts) read hit L2 (16 tiny
+// tensors, L2 flushed before each launch: 9.8 -> 9.0 us).
+constexpr uint64_t kPrefetchMaxBytes = 16ull << 20;
 // Percent of a chunk's cost (whole rounds of units) that warps claim while
 // they run instead of owning it, by build (measured best, fractions of the
 // copy peak): TMA, 100k tiny tensors 8 % (0.851 with fixed shares -> 0.895-0.903;
@@ -151,6 +157,7 @@ struct st_plan_s {
   // the loaders then copy only these.
   std::vector<std::pair<uint64_t, uint64_t>> ranges;
   bool sparse = false;
+  uint64_t pf_lo = 0, pf_hi = 0;  // the span a single-chunk launch prefetches (empty: none)
   std::vector<Piece> pieces;
   std::vector<uint32_t> parts;  // n_chunks * (workers + 1)
   std::vector<uint32_t> claim_end;  // per chunk: end of the pieces claimed at run time (TMA builds)
@@ -704,6 +711,14 @@ void compute_ranges(st_plan_s *p) {
   }
   for (const auto &x : p->ranges) covered += x.second - x.first;
   p->sparse = covered < core.data_bytes / 4 * 3;
+  p->pf_lo = p->pf_hi = 0;
+  if (!p->ranges.empty()) {
+    const uint64_t lo = p->ranges.front().first, hi = p->ranges.back().second;
+    if (hi - lo <= kPrefetchMaxBytes && covered * 2 >= hi - lo) {
+      p->pf_lo = lo;
+      p->pf_hi = hi;
+    }
+  }
 }
 
 // Calls fn(lo, hi) for the plan's read ranges within [off, off + n): all of
@@ -1003,6 +1018,13 @@ st_status launch_chunk(const st_plan_t *p, uint32_t k, const void *data_dev, voi
   a.quant = p->d_quant;
   a.claim_end = p->claim_end[k];
   a.claim = p->d_claim;
+  if (p->n_chunks == 1 && p->pf_hi > p->pf_lo) {
+    a.pf_table = p->d_pieces + parts[0];
+    a.pf_table_bytes = static_cast<uint32_t>((p->claim_end[k] - parts[0]) * sizeof(Piece));
+    a.pf_dst_bytes = static_cast<uint32_t>(p->outs.size() * sizeof(void *));
+    a.pf_data_off = p->pf_lo;
+    a.pf_data_bytes = p->pf_hi - p->pf_lo;
+  }
   return launch_materialize(a, p->kernel, stream);
 }
 
