@@ -14,7 +14,11 @@
 //    inter-warp synchronization and no waits, so the kernel cannot stall on a
 //    peer, then claims pieces of the plan's tail [parts[W], claim_end) in
 //    source order from a claim word (warps that ran fast take more, so all
-//    finish together; the last one out zeroes the word).  A warp stages up to
+//    finish together; the last one out zeroes the word; launches without a
+//    tail leave it alone).  Small plans (a source span of at most 16 MiB)
+//    first prefetch that span, the piece table and the destination array
+//    into L2, one slice per block, so the reads that follow a warp's first
+//    one hit L2.  A warp stages up to
 //    32 piece descriptors at a time in shared memory (one per lane), with
 //    their destination pointers and scales, so the dependent loads of a piece
 //    are paid once per 32 pieces;
