@@ -412,6 +412,37 @@ def sliced_image(seed):
     return image_of(ents, b"".join(parts), pad=5), shapes, rng
 
 
+def test_data_section_in_host_memory(stmat, oracle):
+    """A data section in page-locked host memory, which the kernel reads over
+    the host link: the register builds materialize it exactly (the L2
+    prefetch of small plans, which targets only this GPU's memory, is left
+    out), and the TMA builds refuse it with ST_E_INVAL before any launch."""
+    g, f = small_file()
+    img = np.frombuffer(f, dtype=np.uint8).copy()
+    host = torch.empty(img.size, dtype=torch.uint8, pin_memory=True)
+    host.numpy()[:] = img
+    ix = stmat.Index.from_file(img)
+    hlen, _ = ix.sizes()
+    data_ptr = host.data_ptr() + 8 + hlen
+    suffix = (".weight", ".scale_weight")
+    sel, expected = oracle_all(oracle, img, dst="BF16", scale_suffix=suffix)
+    for kernel in (1, 2):
+        plan = ix.plan(dst="BF16", scale_suffix=suffix, kernel=kernel)
+        outs = GuardedOutputs(plan)
+        plan.materialize(data_ptr, outs.ptrs)
+        torch.cuda.synchronize()
+        assert plan.check() == 0
+        assert_same(plan, outs, sel, expected)
+    for kernel in (3, 4):
+        plan = ix.plan(dst="BF16", scale_suffix=suffix, kernel=kernel)
+        outs = GuardedOutputs(plan)
+        with pytest.raises(stmat.StmatError) as e:
+            plan.materialize(data_ptr, outs.ptrs)
+        assert e.value.status == "ST_E_INVAL"
+        outs.check_guards()
+    assert np.array_equal(host.numpy(), img)
+
+
 @pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 def test_sliced_outputs(stmat, oracle, kernel):
     """Slices on every dimension (contiguous and strided runs) at misaligned

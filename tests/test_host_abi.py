@@ -301,8 +301,8 @@ def test_tma_claimed_tail_is_cut_into_segment_pieces(stmat):
     """The TMA build's claimed tail holds pieces of at most 2 KiB of source
     (one segment: its warps claim two or more at a time), while its own
     shares keep whole 16 KiB units; the streaming build's claimed tail keeps
-    whole units.  The pieces still cover every output once (checked for
-    these plans by test_pieces_cover_outputs_once)."""
+    whole units.  (test_pieces_cover_outputs_once checks that TMA plans of
+    this workload still cover every output once.)"""
     from safetensors_materialization_gb300 import synth
     lay = synth.stress().files[0]
     ix = stmat.Index.from_header(lay.header, lay.data_bytes)
